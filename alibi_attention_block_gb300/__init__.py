@@ -1,0 +1,217 @@
+"""GB300 (sm_103a) prefill forward of one decoder block.
+
+A thin torch-facing binding over the C ABI in ``include/blk.h``
+(``lib/libblk.so``): it checks tensors, passes device pointers and the current
+CUDA stream, and raises ``BlkError`` on a non-OK status. Every step of the
+block runs in the library's CUDA kernels; nothing here computes.
+
+Block variants (nnterp encyclopedia "stablelm", 03 Notes; "OLMo-2: reordered
+(post) normalization", section 1; "Bloom in a sovereign engine",
+Contribution): sequential pre-norm, parallel residual, reordered post-norm;
+LayerNorm-with-bias or RMSNorm; stacked or head-interleaved QKV with bias;
+full-width or per-head qk-norm; partial NeoX rotary or ALiBi.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _abi
+from ._abi import BlkError  # noqa: F401
+
+__all__ = ["layernorm_bias", "rmsnorm", "qkv_bias_rope_partial", "rope_inplace", "attn_prefill",
+           "linear", "mlp", "block_desc", "forward_workspace_size", "forward",
+           "check_device_status", "BlkError", "library_path"]
+
+library_path = _abi.LIB_PATH
+
+
+def _lib():
+    return _abi.load()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return _abi.BLK_F16
+    if t.dtype == torch.bfloat16:
+        return _abi.BLK_BF16
+    raise TypeError(f"storage dtype must be float16 or bfloat16, got {t.dtype}")
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the block library must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the block library must be contiguous")
+    return t.data_ptr()
+
+
+def _same(dt_tensor, *ts):
+    for t in ts:
+        if t is not None and t.dtype != dt_tensor.dtype:
+            raise TypeError(f"all tensors must share dtype {dt_tensor.dtype}, got {t.dtype}")
+
+
+def _stream():
+    return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def layernorm_bias(x, gamma, beta=None, residual=None, eps=1e-5, out=None):
+    """y = LN(x) * gamma + beta [+ residual] over the last axis."""
+    _same(x, gamma, beta, residual, out)
+    out = torch.empty_like(x) if out is None else out
+    cols = x.shape[-1]
+    _abi.check(_lib().blk_layernorm_bias(_p(x), _p(residual), _p(gamma), _p(beta), _p(out),
+                                         x.numel() // cols, cols, eps, _dt(x), _stream()),
+               "blk_layernorm_bias")
+    return out
+
+
+def rmsnorm(x, weight, residual=None, eps=1e-6, out=None):
+    """y = x / rms(x) * weight [+ residual] over the last axis."""
+    _same(x, weight, residual, out)
+    out = torch.empty_like(x) if out is None else out
+    cols = x.shape[-1]
+    _abi.check(_lib().blk_rmsnorm(_p(x), _p(residual), _p(weight), _p(out), x.numel() // cols,
+                                  cols, eps, _dt(x), _stream()), "blk_rmsnorm")
+    return out
+
+
+_LAYOUT = {"stacked": _abi.BLK_QKV_STACKED, "head_interleaved": _abi.BLK_QKV_HEAD_INTERLEAVED}
+_QKN = {"none": _abi.BLK_QKNORM_NONE, "rms_full": _abi.BLK_QKNORM_RMS_FULL,
+        "ln_per_head": _abi.BLK_QKNORM_LN_PER_HEAD}
+
+
+def _qkv_desc(batch, seq, hidden, n_heads, n_kv_heads, head_dim, layout, qk_norm, qk_norm_eps,
+              rotary_span, rope_base):
+    return _abi.QkvDesc(batch, seq, hidden, n_heads, n_kv_heads, head_dim, _LAYOUT[layout],
+                        _QKN[qk_norm], qk_norm_eps, rotary_span, rope_base)
+
+
+def qkv_bias_rope_partial(x, w_qkv, b_qkv=None, *, n_heads, n_kv_heads, head_dim,
+                          layout="stacked", qk_norm="none", qk_norm_eps=1e-5, rotary_span=0,
+                          rope_base=10000.0, q_norm_w=None, k_norm_w=None):
+    """x [B, S, D] -> head-split q [B, H, S, d], k and v [B, Hk, S, d]."""
+    _same(x, w_qkv, b_qkv, q_norm_w, k_norm_w)
+    B, S, D = x.shape
+    desc = _qkv_desc(B, S, D, n_heads, n_kv_heads, head_dim, layout, qk_norm, qk_norm_eps,
+                     rotary_span, rope_base)
+    q = torch.empty((B, n_heads, S, head_dim), dtype=x.dtype, device=x.device)
+    k = torch.empty((B, n_kv_heads, S, head_dim), dtype=x.dtype, device=x.device)
+    v = torch.empty_like(k)
+    _abi.check(_lib().blk_qkv_bias_rope_partial(C.byref(desc), _p(x), _p(w_qkv), _p(b_qkv),
+                                                _p(q_norm_w), _p(k_norm_w), _p(q), _p(k), _p(v),
+                                                _dt(x), _stream()), "blk_qkv_bias_rope_partial")
+    return q, k, v
+
+
+def rope_inplace(x, bias=None, rotary_span=0, rope_base=10000.0):
+    """In place on x [B, n, S, d]: x += bias (per head), then partial NeoX rotary."""
+    _same(x, bias)
+    B, n, S, d = x.shape
+    _abi.check(_lib().blk_rope_inplace(_p(x), _p(bias), B, n, S, d, rotary_span, rope_base,
+                                       _dt(x), _stream()), "blk_rope_inplace")
+    return x
+
+
+def attn_prefill(q, k, v, alibi=False, slopes=None, scale=None, out=None):
+    """Causal attention: q [B, H, S, d], k/v [B, Hk, S, d] -> o [B, S, H, d]."""
+    _same(q, k, v, out)
+    B, H, S, d = q.shape
+    Hk = k.shape[1]
+    if slopes is not None and slopes.dtype != torch.float32:
+        raise TypeError("ALiBi slopes are fp32")
+    desc = _abi.AttnDesc(B, S, H, Hk, d, -1.0 if scale is None else scale, 1, 1 if alibi else 0)
+    o = torch.empty((B, S, H, d), dtype=q.dtype, device=q.device) if out is None else out
+    _abi.check(_lib().blk_attn_prefill(C.byref(desc), _p(q), _p(k), _p(v), _p(slopes), _p(o),
+                                       _dt(q), _stream()), "blk_attn_prefill")
+    return o
+
+
+def linear(x, w, bias=None, res1=None, res2=None, out=None):
+    """y = x W^T [+ bias] [+ res1] [+ res2]; x [..., k], w [n, k]."""
+    _same(x, w, bias, res1, res2, out)
+    k = x.shape[-1]
+    n = w.shape[0]
+    m = x.numel() // k
+    out = torch.empty((*x.shape[:-1], n), dtype=x.dtype, device=x.device) if out is None else out
+    _abi.check(_lib().blk_linear(_p(x), _p(w), _p(bias), _p(res1), _p(res2), _p(out), m, n, k,
+                                 _dt(x), _stream()), "blk_linear")
+    return out
+
+
+def mlp(x, w_up, w_down, w_gate=None, b_up=None, b_down=None, res1=None, res2=None,
+        act="swiglu", workspace=None, out=None):
+    """SwiGLU or GELU(tanh) MLP with optional biases and residual adds."""
+    _same(x, w_up, w_down, w_gate, b_up, b_down, res1, res2, out)
+    D = x.shape[-1]
+    T = x.numel() // D
+    F = w_up.shape[0]
+    desc = _abi.MlpDesc(T, D, F, _abi.BLK_ACT_SWIGLU if act == "swiglu" else _abi.BLK_ACT_GELU_TANH)
+    need = C.c_size_t(0)
+    _abi.check(_lib().blk_mlp_workspace_size(C.byref(desc), C.byref(need)), "blk_mlp_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need.value, dtype=torch.uint8, device=x.device)
+    out = torch.empty_like(x) if out is None else out
+    _abi.check(_lib().blk_mlp(C.byref(desc), _p(x), _p(w_gate), _p(w_up), _p(b_up), _p(w_down),
+                              _p(b_down), _p(res1), _p(res2), _p(out), _p(workspace),
+                              workspace.numel(), _dt(x), _stream()), "blk_mlp")
+    return out
+
+
+def block_desc(cfg, batch: int, seq: int) -> _abi.BlockDesc:
+    """Descriptor from a config object with the block's fields (hidden,
+    n_heads, n_kv_heads, head_dim, intermediate, norm, norm_place, residual,
+    eps, qkv_layout, qk_norm, qk_norm_eps, rotary_span, rope_base, alibi, act)."""
+    q = _qkv_desc(batch, seq, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim,
+                  cfg.qkv_layout, cfg.qk_norm, cfg.qk_norm_eps, cfg.rotary_span, cfg.rope_base)
+    return _abi.BlockDesc(
+        q,
+        _abi.BLK_NORM_LAYERNORM if cfg.norm == "layernorm" else _abi.BLK_NORM_RMS,
+        _abi.BLK_NORM_PRE if cfg.norm_place == "pre" else _abi.BLK_NORM_POST,
+        _abi.BLK_RESIDUAL_SEQUENTIAL if cfg.residual == "sequential" else _abi.BLK_RESIDUAL_PARALLEL,
+        cfg.eps, 1 if cfg.alibi else 0, cfg.intermediate,
+        _abi.BLK_ACT_SWIGLU if cfg.act == "swiglu" else _abi.BLK_ACT_GELU_TANH)
+
+
+def forward_workspace_size(cfg, batch: int, seq: int) -> int:
+    desc = block_desc(cfg, batch, seq)
+    need = C.c_size_t(0)
+    _abi.check(_lib().blk_forward_workspace_size(C.byref(desc), C.byref(need)),
+               "blk_forward_workspace_size")
+    return need.value
+
+
+def forward(cfg, weights: dict, x, workspace=None, out=None):
+    """The block's prefill forward: x [B, S, D] -> y [B, S, D].
+
+    weights maps slot names (``attn_norm_w``, ``w_qkv``, ...) to CUDA tensors;
+    absent slots are NULL. workspace: a uint8 CUDA tensor of at least
+    ``forward_workspace_size`` bytes (allocated here when None).
+    """
+    B, S, _ = x.shape
+    desc = block_desc(cfg, B, S)
+    ws_need = forward_workspace_size(cfg, B, S)
+    if workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=x.device)
+    unknown = set(weights) - set(_abi.WEIGHT_SLOTS)
+    if unknown:
+        raise KeyError(f"unknown weight slots: {sorted(unknown)}")
+    for name, t in weights.items():
+        if name != "alibi_slopes":
+            _same(x, t)
+    w = _abi.BlockWeights(*[_p(weights.get(n)) for n in _abi.WEIGHT_SLOTS])
+    out = torch.empty_like(x) if out is None else out
+    _abi.check(_lib().blk_forward(C.byref(desc), C.byref(w), _p(x), _p(out), _p(workspace),
+                                  workspace.numel(), _dt(x), _stream()), "blk_forward")
+    return out
+
+
+def check_device_status():
+    """Synchronise the current stream and raise if an in-kernel wait timed out."""
+    _abi.check(_lib().blk_check_device_status(_stream()), "blk_check_device_status")

@@ -1,0 +1,771 @@
+// C ABI of the block library (include/blk.h): argument validation (before any
+// CUDA call, so a rejected call has no side effects), TMA descriptor set-up,
+// kernel dispatch and the blk_forward step sequence.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/blk.h"
+#include "internal.h"
+
+namespace blk {
+
+// Device error word, set by kernels whose bounded waits give up.
+__device__ unsigned int g_dev_err;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+blk_status fail(blk_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+blk_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(BLK_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DevState {
+    bool init = false;
+    int sms = 0;
+    unsigned* err = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+blk_status dev_state(DevState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(BLK_EUNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState& d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(BLK_EUNSUPPORTED, "kernels are built for sm_103a; device is sm_%d%d", major,
+                        minor);
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_dev_err);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+        d.err = static_cast<unsigned*>(p);
+        d.init = true;
+    }
+    *out = &d;
+    return BLK_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dt(blk_dtype dt) { return dt == BLK_F16 || dt == BLK_BF16; }
+
+DType to_dt(blk_dtype dt) { return dt == BLK_F16 ? DType::F16 : DType::BF16; }
+
+RopeParams make_rope(int span, float base) {
+    RopeParams rp;
+    std::memset(&rp, 0, sizeof(rp));
+    rp.span = span;
+    const double two_pi = 6.283185307179586476925286766559;
+    rp.c1 = 6.28125f;  // 201/32: 8 significant bits, so k * c1 is exact for k < 2^16
+    const double r1 = two_pi - 6.28125;
+    rp.c2 = static_cast<float>(r1);
+    rp.c3 = static_cast<float>(r1 - static_cast<double>(rp.c2));
+    rp.inv_2pi = static_cast<float>(1.0 / two_pi);
+    for (int j = 0; j < span / 2; ++j) {
+        const double th = std::pow(static_cast<double>(base), -2.0 * j / span);
+        const float hi = static_cast<float>(th);
+        rp.theta_hi[j] = hi;
+        rp.theta_lo[j] = static_cast<float>(th - static_cast<double>(hi));
+    }
+    return rp;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+constexpr int64_t kI32 = 0x7fffffff;
+
+}  // namespace
+
+bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, dt == DType::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_3d(CUtensorMap* m, DType dt, const void* base, uint64_t planes, uint64_t rows,
+                  uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {cols, rows, planes};
+    const cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, dt == DType::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace blk
+
+using namespace blk;
+
+// ------------------------------------------------------------ validation --
+namespace {
+
+#define BLK_REQUIRE(cond, ...)                              \
+    do {                                                    \
+        if (!(cond)) return fail(BLK_EINVAL, __VA_ARGS__);  \
+    } while (0)
+
+blk_status check_ptr(const void* p, const char* name, bool required) {
+    if (!p) return required ? fail(BLK_EINVAL, "%s is NULL", name) : BLK_OK;
+    if (!aligned16(p)) return fail(BLK_EINVAL, "%s is not 16-byte aligned", name);
+    return BLK_OK;
+}
+
+#define BLK_CHECK_PTR(p, required)                                     \
+    do {                                                               \
+        blk_status st_ = check_ptr((p), #p, (required));               \
+        if (st_ != BLK_OK) return st_;                                 \
+    } while (0)
+
+blk_status validate_norm(const void* x, const void* res, const void* g, const void* b,
+                         const void* y, int64_t rows, int64_t cols, float eps, blk_dtype dt) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    BLK_REQUIRE(rows >= 0 && rows <= kI32 * 16, "rows out of range");
+    BLK_REQUIRE(cols >= 8 && cols % 8 == 0 && cols <= 16384, "cols must be a multiple of 8 in [8, 16384]");
+    BLK_REQUIRE(std::isfinite(eps) && eps >= 0.f, "eps must be finite and >= 0");
+    BLK_CHECK_PTR(x, true);
+    BLK_CHECK_PTR(res, false);
+    BLK_CHECK_PTR(g, true);
+    BLK_CHECK_PTR(b, false);
+    BLK_CHECK_PTR(y, true);
+    return BLK_OK;
+}
+
+blk_status validate_qkv_desc(const blk_qkv_desc* d) {
+    BLK_REQUIRE(d, "descriptor is NULL");
+    BLK_REQUIRE(d->batch >= 1 && d->seq >= 1 && d->batch * d->seq <= kI32, "batch*seq out of range");
+    BLK_REQUIRE(d->hidden >= 8 && d->hidden % 8 == 0 && d->hidden <= kI32, "hidden must be a positive multiple of 8");
+    BLK_REQUIRE(d->n_heads >= 1 && d->n_kv_heads >= 1 && d->n_heads % d->n_kv_heads == 0,
+                "n_heads must be a positive multiple of n_kv_heads");
+    BLK_REQUIRE(d->head_dim >= 32 && d->head_dim % 32 == 0 && d->head_dim <= 256,
+                "head_dim must be a multiple of 32 in [32, 256]");
+    BLK_REQUIRE(d->qkv_layout == BLK_QKV_STACKED || d->qkv_layout == BLK_QKV_HEAD_INTERLEAVED,
+                "unknown qkv_layout");
+    BLK_REQUIRE(d->qkv_layout == BLK_QKV_STACKED || d->n_heads == d->n_kv_heads,
+                "head-interleaved QKV needs n_heads == n_kv_heads");
+    BLK_REQUIRE(d->qk_norm >= BLK_QKNORM_NONE && d->qk_norm <= BLK_QKNORM_LN_PER_HEAD,
+                "unknown qk_norm");
+    BLK_REQUIRE(std::isfinite(d->qk_norm_eps) && d->qk_norm_eps >= 0.f, "qk_norm_eps must be >= 0");
+    BLK_REQUIRE(d->rotary_span >= 0 && d->rotary_span % 2 == 0 && d->rotary_span <= d->head_dim &&
+                    d->rotary_span / 2 <= kMaxRotaryPairs,
+                "rotary_span must be even and in [0, head_dim]");
+    BLK_REQUIRE(d->rotary_span == 0 || (std::isfinite(d->rope_base) && d->rope_base > 1.f),
+                "rope_base must be > 1 when rotary is on");
+    BLK_REQUIRE((d->n_heads + d->n_kv_heads) * d->head_dim * 4 <= 200 * 1024,
+                "(n_heads + n_kv_heads) * head_dim too large for the qk-norm kernel");
+    return BLK_OK;
+}
+
+blk_status validate_attn_desc(const blk_attn_desc* d) {
+    BLK_REQUIRE(d, "descriptor is NULL");
+    BLK_REQUIRE(d->batch >= 1 && d->seq >= 1 && d->batch * d->seq <= kI32, "batch*seq out of range");
+    BLK_REQUIRE(d->n_heads >= 1 && d->n_kv_heads >= 1 && d->n_heads % d->n_kv_heads == 0,
+                "n_heads must be a positive multiple of n_kv_heads");
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 160)
+        return fail(BLK_EUNSUPPORTED, "attention head_dim must be 64, 128 or 160 (got %lld)",
+                    static_cast<long long>(d->head_dim));
+    if (d->causal != 1) return fail(BLK_EUNSUPPORTED, "only causal prefill attention is implemented");
+    BLK_REQUIRE(d->alibi == 0 || d->alibi == 1, "alibi must be 0 or 1");
+    BLK_REQUIRE(std::isfinite(d->softmax_scale), "softmax_scale must be finite");
+    const int64_t nq = (d->seq + 127) / 128;
+    BLK_REQUIRE(nq * d->batch * d->n_heads <= kI32, "grid too large");
+    return BLK_OK;
+}
+
+blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w) {
+    BLK_REQUIRE(d && w, "descriptor or weights is NULL");
+    blk_status st = validate_qkv_desc(&d->qkv);
+    if (st != BLK_OK) return st;
+    const auto& q = d->qkv;
+    if (q.head_dim != 64 && q.head_dim != 128 && q.head_dim != 160)
+        return fail(BLK_EUNSUPPORTED, "head_dim must be 64, 128 or 160");
+    BLK_REQUIRE(d->norm_kind == BLK_NORM_LAYERNORM || d->norm_kind == BLK_NORM_RMS, "unknown norm_kind");
+    BLK_REQUIRE(d->norm_place == BLK_NORM_PRE || d->norm_place == BLK_NORM_POST, "unknown norm_place");
+    BLK_REQUIRE(d->residual == BLK_RESIDUAL_SEQUENTIAL || d->residual == BLK_RESIDUAL_PARALLEL,
+                "unknown residual");
+    BLK_REQUIRE(d->act == BLK_ACT_SWIGLU || d->act == BLK_ACT_GELU_TANH, "unknown act");
+    BLK_REQUIRE(d->alibi == 0 || d->alibi == 1, "alibi must be 0 or 1");
+    BLK_REQUIRE(std::isfinite(d->eps) && d->eps >= 0.f, "eps must be >= 0");
+    BLK_REQUIRE(d->intermediate >= 8 && d->intermediate % 8 == 0 && d->intermediate <= kI32,
+                "intermediate must be a positive multiple of 8");
+    BLK_REQUIRE(q.hidden <= 16384, "hidden must be <= 16384");
+    if (d->alibi && q.rotary_span != 0)
+        return fail(BLK_EUNSUPPORTED,
+                    "rotary and ALiBi are exclusive: set rotary_span = 0 for an ALiBi block");
+    if (d->alibi && !w->alibi_slopes && !is_pow2(q.n_heads))
+        return fail(BLK_EUNSUPPORTED, "standard ALiBi slopes need a power-of-two head count");
+    if (d->norm_place == BLK_NORM_POST) {
+        if (d->norm_kind != BLK_NORM_RMS || d->residual != BLK_RESIDUAL_SEQUENTIAL)
+            return fail(BLK_EUNSUPPORTED, "post-norm blocks are RMSNorm, sequential");
+    }
+    const bool pre = d->norm_place == BLK_NORM_PRE;
+    const bool seq_pre = pre && d->residual == BLK_RESIDUAL_SEQUENTIAL;
+    const bool ln = d->norm_kind == BLK_NORM_LAYERNORM;
+    const bool swiglu = d->act == BLK_ACT_SWIGLU;
+    // Every slot is either used (and then required, except optional biases) or
+    // must be NULL: a weight handed to the wrong slot is an error, not ignored.
+    struct Slot {
+        const void* p;
+        const char* name;
+        bool used;
+        bool required;
+    } slots[] = {
+        {w->attn_norm_w, "attn_norm_w", pre, pre},
+        {w->attn_norm_b, "attn_norm_b", pre && ln, false},
+        {w->mlp_norm_w, "mlp_norm_w", seq_pre, seq_pre},
+        {w->mlp_norm_b, "mlp_norm_b", seq_pre && ln, false},
+        {w->post_attn_norm_w, "post_attn_norm_w", !pre, !pre},
+        {w->post_mlp_norm_w, "post_mlp_norm_w", !pre, !pre},
+        {w->w_qkv, "w_qkv", true, true},
+        {w->b_qkv, "b_qkv", true, false},
+        {w->q_norm_w, "q_norm_w", q.qk_norm != BLK_QKNORM_NONE, q.qk_norm != BLK_QKNORM_NONE},
+        {w->k_norm_w, "k_norm_w", q.qk_norm != BLK_QKNORM_NONE, q.qk_norm != BLK_QKNORM_NONE},
+        {w->w_o, "w_o", true, true},
+        {w->b_o, "b_o", true, false},
+        {w->w_gate, "w_gate", swiglu, swiglu},
+        {w->w_up, "w_up", true, true},
+        {w->b_up, "b_up", !swiglu, false},
+        {w->w_down, "w_down", true, true},
+        {w->b_down, "b_down", true, false},
+        {w->alibi_slopes, "alibi_slopes", d->alibi != 0, false},
+    };
+    for (const Slot& s : slots) {
+        if (!s.used && s.p) return fail(BLK_EINVAL, "weight slot %s is not used by this block and must be NULL", s.name);
+        if (s.required && !s.p) return fail(BLK_EINVAL, "weight slot %s is required", s.name);
+        if (s.p && !aligned16(s.p)) return fail(BLK_EINVAL, "weight slot %s is not 16-byte aligned", s.name);
+    }
+    return BLK_OK;
+}
+
+struct FwdLayout {
+    size_t n1, q, k, v, o, h, n2, a, tmp, total;
+};
+
+FwdLayout forward_layout(const blk_block_desc* d) {
+    const auto& q = d->qkv;
+    const size_t T = static_cast<size_t>(q.batch) * q.seq;
+    const size_t D = q.hidden, Hd = q.n_heads * q.head_dim, Kd = q.n_kv_heads * q.head_dim;
+    FwdLayout L;
+    size_t off = 0;
+    auto take = [&](size_t elems) {
+        const size_t at = off;
+        off += align256(elems * 2);
+        return at;
+    };
+    L.n1 = take(T * D);
+    L.q = take(T * Hd);
+    L.k = take(T * Kd);
+    L.v = take(T * Kd);
+    L.o = take(T * Hd);
+    L.h = take(T * D);
+    L.n2 = take(T * D);
+    L.a = take(T * static_cast<size_t>(d->intermediate));
+    L.tmp = take(T * D);
+    L.total = off;
+    return L;
+}
+
+// Records an event after each kernel launch of blk_forward_ex and the kind
+// of each launch (see blk_forward_ex in blk.h).
+struct StepLog {
+    void* const* events;
+    int n_events;
+    int32_t* kinds;
+    int* n_out;
+    cudaStream_t s;
+    int n = 0;
+    blk_status begin() {
+        if (events && n_events > 0) {
+            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[0]), s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        }
+        return BLK_OK;
+    }
+    blk_status step(int kind) {
+        if (kinds && n < 10 && n + 1 < (n_events > 0 ? n_events : 11)) kinds[n] = kind;
+        ++n;
+        if (events && n < n_events) {
+            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[n]), s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        }
+        return BLK_OK;
+    }
+    blk_status end() {
+        if (n_out) *n_out = n;
+        return BLK_OK;
+    }
+};
+
+// Launch the projection (+bias, +rotary when it can be fused) and, when a
+// qk-norm or a wider rotary span sits between the projection and attention,
+// the in-place qk-norm/rotary kernel.
+blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, const void* b_qkv,
+                   const void* q_norm_w, const void* k_norm_w, void* q, void* k, void* v,
+                   DType dt, cudaStream_t s, DevState* ds, StepLog* log = nullptr) {
+    const bool fuse_rope = d->qk_norm == BLK_QKNORM_NONE && d->rotary_span <= 32;
+    RopeParams rp = make_rope(fuse_rope ? d->rotary_span : 0, d->rope_base);
+    GemmArgs g{};
+    g.M = static_cast<int>(d->batch * d->seq);
+    g.N = static_cast<int>((d->n_heads + 2 * d->n_kv_heads) * d->head_dim);
+    g.K = static_cast<int>(d->hidden);
+    g.bias = b_qkv;
+    g.q = q;
+    g.k = k;
+    g.v = v;
+    g.S = static_cast<int>(d->seq);
+    g.H = static_cast<int>(d->n_heads);
+    g.Hk = static_cast<int>(d->n_kv_heads);
+    g.d = static_cast<int>(d->head_dim);
+    g.interleaved = d->qkv_layout == BLK_QKV_HEAD_INTERLEAVED;
+    g.err = ds->err;
+    cudaError_t e = launch_gemm(dt, EPI_QKV, x, w_qkv, nullptr, g, rp, ds->sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "qkv projection launch");
+    blk_status st;
+    if (log && (st = log->step(BLK_STEP_QKV)) != BLK_OK) return st;
+    if (!fuse_rope) {
+        QkNormRopeArgs a{};
+        a.q = q;
+        a.k = k;
+        a.q_w = q_norm_w;
+        a.k_w = k_norm_w;
+        a.B = g.M / g.S;
+        a.S = g.S;
+        a.H = g.H;
+        a.Hk = g.Hk;
+        a.d = g.d;
+        a.mode = d->qk_norm;
+        a.eps = d->qk_norm_eps;
+        e = launch_qk_norm_rope(dt, a, make_rope(d->rotary_span, d->rope_base), s);
+        if (e != cudaSuccess) return cuda_fail(e, "qk-norm/rotary launch");
+        if (log && (st = log->step(BLK_STEP_QK_NORM_ROPE)) != BLK_OK) return st;
+    }
+    return BLK_OK;
+}
+
+blk_status run_linear(DType dt, int epi, const void* x, const void* w, const void* w2,
+                      const void* bias, const void* r1, const void* r2, void* y, int64_t m,
+                      int64_t n, int64_t k, cudaStream_t s, DevState* ds) {
+    GemmArgs g{};
+    g.M = static_cast<int>(m);
+    g.N = static_cast<int>(n);
+    g.K = static_cast<int>(k);
+    g.out = y;
+    g.bias = bias;
+    g.res1 = r1;
+    g.res2 = r2;
+    g.err = ds->err;
+    const RopeParams rp = make_rope(0, 0.f);
+    cudaError_t e = launch_gemm(dt, epi, x, w, w2, g, rp, ds->sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return BLK_OK;
+}
+
+blk_status run_attn(const blk_attn_desc* d, const void* q, const void* k, const void* v,
+                    const float* slopes, void* o, DType dt, cudaStream_t s, DevState* ds) {
+    AttnArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.B = static_cast<int>(d->batch);
+    a.S = static_cast<int>(d->seq);
+    a.H = static_cast<int>(d->n_heads);
+    a.Hk = static_cast<int>(d->n_kv_heads);
+    a.d = static_cast<int>(d->head_dim);
+    a.scale = d->softmax_scale > 0.f ? d->softmax_scale
+                                     : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d->head_dim)));
+    a.alibi = d->alibi;
+    a.slopes = slopes;
+    a.err = ds->err;
+    cudaError_t e = launch_attention(dt, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    return BLK_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ ABI --
+extern "C" {
+
+const char* blk_status_string(blk_status s) {
+    switch (s) {
+        case BLK_OK: return "BLK_OK";
+        case BLK_EINVAL: return "BLK_EINVAL";
+        case BLK_EUNSUPPORTED: return "BLK_EUNSUPPORTED";
+        case BLK_ECUDA: return "BLK_ECUDA";
+        case BLK_ETIMEOUT: return "BLK_ETIMEOUT";
+        case BLK_EWORKSPACE: return "BLK_EWORKSPACE";
+    }
+    return "BLK_UNKNOWN";
+}
+
+const char* blk_last_error(void) { return t_last_error.c_str(); }
+
+int blk_version(void) { return (1 << 16) | 0; }
+
+blk_status blk_check_device_status(blk_stream_t s) {
+    DevState* ds = nullptr;
+    blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, ds->err, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+    if (word != DEV_ERR_NONE) {
+        const unsigned zero = 0;
+        cudaMemcpy(ds->err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        return fail(BLK_ETIMEOUT, "a bounded in-kernel wait gave up (device error code %u)", word);
+    }
+    return BLK_OK;
+}
+
+blk_status blk_layernorm_bias(const void* x, const void* residual, const void* gamma,
+                              const void* beta, void* y, int64_t rows, int64_t cols, float eps,
+                              blk_dtype dt, blk_stream_t s) {
+    blk_status st = validate_norm(x, residual, gamma, beta, y, rows, cols, eps, dt);
+    if (st != BLK_OK) return st;
+    cudaError_t e = launch_norm(to_dt(dt), false, x, residual, gamma, beta, y, rows,
+                                static_cast<int>(cols), eps, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "layernorm launch");
+}
+
+blk_status blk_rmsnorm(const void* x, const void* residual, const void* weight, void* y,
+                       int64_t rows, int64_t cols, float eps, blk_dtype dt, blk_stream_t s) {
+    blk_status st = validate_norm(x, residual, weight, nullptr, y, rows, cols, eps, dt);
+    if (st != BLK_OK) return st;
+    cudaError_t e = launch_norm(to_dt(dt), true, x, residual, weight, nullptr, y, rows,
+                                static_cast<int>(cols), eps, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "rmsnorm launch");
+}
+
+blk_status blk_qkv_bias_rope_partial(const blk_qkv_desc* d, const void* x, const void* w_qkv,
+                                     const void* b_qkv, const void* q_norm_w,
+                                     const void* k_norm_w, void* q, void* k, void* v,
+                                     blk_dtype dt, blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    blk_status st = validate_qkv_desc(d);
+    if (st != BLK_OK) return st;
+    const bool qkn = d->qk_norm != BLK_QKNORM_NONE;
+    BLK_CHECK_PTR(x, true);
+    BLK_CHECK_PTR(w_qkv, true);
+    BLK_CHECK_PTR(b_qkv, false);
+    BLK_CHECK_PTR(q_norm_w, qkn);
+    BLK_CHECK_PTR(k_norm_w, qkn);
+    BLK_REQUIRE(qkn || (!q_norm_w && !k_norm_w), "q_norm_w/k_norm_w must be NULL without qk_norm");
+    BLK_CHECK_PTR(q, true);
+    BLK_CHECK_PTR(k, true);
+    BLK_CHECK_PTR(v, true);
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+    return run_qkv(d, x, w_qkv, b_qkv, q_norm_w, k_norm_w, q, k, v, to_dt(dt),
+                   reinterpret_cast<cudaStream_t>(s), ds);
+}
+
+blk_status blk_rope_inplace(void* x, const void* bias, int64_t batch, int64_t n_heads,
+                            int64_t seq, int64_t head_dim, int32_t rotary_span, float rope_base,
+                            blk_dtype dt, blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    BLK_CHECK_PTR(x, true);
+    BLK_CHECK_PTR(bias, false);
+    BLK_REQUIRE(batch >= 1 && seq >= 1 && batch * seq <= kI32, "batch*seq out of range");
+    BLK_REQUIRE(n_heads >= 1 && head_dim >= 8 && head_dim % 8 == 0 && head_dim <= 256,
+                "head_dim must be a multiple of 8 in [8, 256]");
+    BLK_REQUIRE(n_heads * head_dim * 4 <= 200 * 1024, "n_heads * head_dim too large");
+    BLK_REQUIRE(rotary_span >= 0 && rotary_span % 2 == 0 && rotary_span <= head_dim &&
+                    rotary_span / 2 <= kMaxRotaryPairs,
+                "rotary_span must be even and in [0, head_dim]");
+    BLK_REQUIRE(rotary_span == 0 || (std::isfinite(rope_base) && rope_base > 1.f),
+                "rope_base must be > 1 when rotary is on");
+    QkNormRopeArgs a{};
+    a.q = x;
+    a.q_bias = bias;
+    a.B = static_cast<int>(batch);
+    a.S = static_cast<int>(seq);
+    a.H = static_cast<int>(n_heads);
+    a.Hk = 0;
+    a.d = static_cast<int>(head_dim);
+    a.mode = QKN_NONE;
+    cudaError_t e = launch_qk_norm_rope(to_dt(dt), a, make_rope(rotary_span, rope_base),
+                                        reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "rope launch");
+}
+
+blk_status blk_attn_prefill(const blk_attn_desc* d, const void* q, const void* k, const void* v,
+                            const float* alibi_slopes, void* o, blk_dtype dt, blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    blk_status st = validate_attn_desc(d);
+    if (st != BLK_OK) return st;
+    BLK_CHECK_PTR(q, true);
+    BLK_CHECK_PTR(k, true);
+    BLK_CHECK_PTR(v, true);
+    BLK_CHECK_PTR(o, true);
+    BLK_REQUIRE(d->alibi || !alibi_slopes, "alibi_slopes given with alibi = 0");
+    if (d->alibi && !alibi_slopes && !is_pow2(d->n_heads))
+        return fail(BLK_EUNSUPPORTED, "standard ALiBi slopes need a power-of-two head count");
+    BLK_REQUIRE(!alibi_slopes || (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u) == 0,
+                "alibi_slopes must be 4-byte aligned");
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+    return run_attn(d, q, k, v, alibi_slopes, o, to_dt(dt), reinterpret_cast<cudaStream_t>(s), ds);
+}
+
+blk_status blk_linear(const void* x, const void* w, const void* bias, const void* res1,
+                      const void* res2, void* y, int64_t m, int64_t n, int64_t k, blk_dtype dt,
+                      blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    BLK_REQUIRE(m >= 0 && m <= kI32, "m out of range");
+    BLK_REQUIRE(n >= 8 && n % 8 == 0 && n <= kI32, "n must be a positive multiple of 8");
+    BLK_REQUIRE(k >= 8 && k % 8 == 0 && k <= kI32, "k must be a positive multiple of 8");
+    BLK_CHECK_PTR(x, true);
+    BLK_CHECK_PTR(w, true);
+    BLK_CHECK_PTR(bias, false);
+    BLK_CHECK_PTR(res1, false);
+    BLK_CHECK_PTR(res2, false);
+    BLK_CHECK_PTR(y, true);
+    if (m == 0) return BLK_OK;
+    DevState* ds = nullptr;
+    blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
+    return run_linear(to_dt(dt), EPI_LINEAR, x, w, nullptr, bias, res1, res2, y, m, n, k,
+                      reinterpret_cast<cudaStream_t>(s), ds);
+}
+
+blk_status blk_mlp_workspace_size(const blk_mlp_desc* d, size_t* bytes) {
+    BLK_REQUIRE(d && bytes, "NULL argument");
+    BLK_REQUIRE(d->tokens >= 0 && d->intermediate >= 8, "bad sizes");
+    *bytes = align256(static_cast<size_t>(d->tokens) * d->intermediate * 2);
+    return BLK_OK;
+}
+
+blk_status blk_mlp(const blk_mlp_desc* d, const void* x, const void* w_gate, const void* w_up,
+                   const void* b_up, const void* w_down, const void* b_down, const void* res1,
+                   const void* res2, void* y, void* workspace, size_t ws_bytes, blk_dtype dt,
+                   blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    BLK_REQUIRE(d, "descriptor is NULL");
+    BLK_REQUIRE(d->act == BLK_ACT_SWIGLU || d->act == BLK_ACT_GELU_TANH, "unknown act");
+    BLK_REQUIRE(d->tokens >= 0 && d->tokens <= kI32, "tokens out of range");
+    BLK_REQUIRE(d->hidden >= 8 && d->hidden % 8 == 0 && d->hidden <= kI32, "hidden must be a positive multiple of 8");
+    BLK_REQUIRE(d->intermediate >= 8 && d->intermediate % 8 == 0 && d->intermediate <= kI32,
+                "intermediate must be a positive multiple of 8");
+    const bool swiglu = d->act == BLK_ACT_SWIGLU;
+    BLK_CHECK_PTR(x, true);
+    BLK_CHECK_PTR(w_gate, swiglu);
+    BLK_REQUIRE(swiglu || !w_gate, "w_gate must be NULL for GELU_TANH");
+    BLK_CHECK_PTR(w_up, true);
+    BLK_CHECK_PTR(b_up, false);
+    BLK_REQUIRE(!swiglu || !b_up, "b_up is not supported with SWIGLU (must be NULL)");
+    BLK_CHECK_PTR(w_down, true);
+    BLK_CHECK_PTR(b_down, false);
+    BLK_CHECK_PTR(res1, false);
+    BLK_CHECK_PTR(res2, false);
+    BLK_CHECK_PTR(y, true);
+    size_t need = 0;
+    blk_mlp_workspace_size(d, &need);
+    if (!workspace || ws_bytes < need || !aligned16(workspace))
+        return fail(BLK_EWORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
+    if (d->tokens == 0) return BLK_OK;
+    DevState* ds = nullptr;
+    blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
+    const DType t = to_dt(dt);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, x, swiglu ? w_gate : w_up,
+                    swiglu ? w_up : nullptr, b_up, nullptr, nullptr, workspace, d->tokens,
+                    d->intermediate, d->hidden, cs, ds);
+    if (st != BLK_OK) return st;
+    return run_linear(t, EPI_LINEAR, workspace, w_down, nullptr, b_down, res1, res2, y, d->tokens,
+                      d->hidden, d->intermediate, cs, ds);
+}
+
+blk_status blk_forward_workspace_size(const blk_block_desc* d, size_t* bytes) {
+    BLK_REQUIRE(d && bytes, "NULL argument");
+    blk_status st = validate_qkv_desc(&d->qkv);
+    if (st != BLK_OK) return st;
+    BLK_REQUIRE(d->intermediate >= 8 && d->intermediate % 8 == 0, "bad intermediate");
+    *bytes = forward_layout(d).total;
+    return BLK_OK;
+}
+
+blk_status blk_forward(const blk_block_desc* d, const blk_block_weights* w, const void* x,
+                       void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s) {
+    return blk_forward_ex(d, w, x, y, workspace, ws_bytes, dt, s, nullptr, 0, nullptr, nullptr);
+}
+
+blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, const void* x,
+                          void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s,
+                          void* const* events, int n_events, int32_t* step_kinds, int* n_launches) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    blk_status st = validate_block(d, w);
+    if (st != BLK_OK) return st;
+    BLK_CHECK_PTR(x, true);
+    BLK_CHECK_PTR(y, true);
+    BLK_REQUIRE(x != y, "y must not alias x");
+    const FwdLayout L = forward_layout(d);
+    if (!workspace || ws_bytes < L.total || !aligned16(workspace))
+        return fail(BLK_EWORKSPACE, "workspace needs %zu bytes, 16-byte aligned", L.total);
+    BLK_REQUIRE(n_events >= 0 && (events || n_events == 0), "events/n_events mismatch");
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+
+    const auto& q = d->qkv;
+    const DType t = to_dt(dt);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* n1 = ws + L.n1;
+    void* qb = ws + L.q;
+    void* kb = ws + L.k;
+    void* vb = ws + L.v;
+    void* ob = ws + L.o;
+    void* hb = ws + L.h;
+    void* n2 = ws + L.n2;
+    void* ab = ws + L.a;
+    void* tmp = ws + L.tmp;
+    const int64_t T = q.batch * q.seq, D = q.hidden, F = d->intermediate;
+    const bool rms = d->norm_kind == BLK_NORM_RMS;
+    const bool pre = d->norm_place == BLK_NORM_PRE;
+    const bool parallel = d->residual == BLK_RESIDUAL_PARALLEL;
+    const bool swiglu = d->act == BLK_ACT_SWIGLU;
+    cudaError_t e;
+    StepLog log{events, n_events, step_kinds, n_launches, cs};
+    if ((st = log.begin()) != BLK_OK) return st;
+#define BLK_STEP(kind)                                   \
+    do {                                                 \
+        if ((st = log.step(kind)) != BLK_OK) return st;  \
+    } while (0)
+
+    // 1. input norm (absent in the reordered post-norm block)
+    const void* attn_in = x;
+    if (pre) {
+        e = launch_norm(t, rms, x, nullptr, w->attn_norm_w, w->attn_norm_b, n1, T,
+                        static_cast<int>(D), d->eps, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "input norm launch");
+        BLK_STEP(BLK_STEP_INPUT_NORM);
+        attn_in = n1;
+    }
+    // 2. projection (+bias), qk-norm, rotary, head split
+    st = run_qkv(&q, attn_in, w->w_qkv, w->b_qkv, w->q_norm_w, w->k_norm_w, qb, kb, vb, t, cs, ds,
+                 &log);
+    if (st != BLK_OK) return st;
+    // 3. causal attention (+ALiBi)
+    blk_attn_desc ad{q.batch, q.seq, q.n_heads, q.n_kv_heads, q.head_dim, 0.f, 1, d->alibi};
+    st = run_attn(&ad, qb, kb, vb, w->alibi_slopes, ob, t, cs, ds);
+    if (st != BLK_OK) return st;
+    BLK_STEP(BLK_STEP_ATTENTION);
+    const int64_t Hd = q.n_heads * q.head_dim;
+    if (parallel) {
+        // 4p. attn_out = o W_o^T (+b_o); mlp on the same normed input; y = x + attn_out + mlp
+        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd, cs, ds);
+        if (st != BLK_OK) return st;
+        BLK_STEP(BLK_STEP_O_PROJ);
+        st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, attn_in, swiglu ? w->w_gate : w->w_up,
+                        swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds);
+        if (st != BLK_OK) return st;
+        BLK_STEP(BLK_STEP_MLP_UP);
+        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, x, tmp, y, T, D, F, cs, ds);
+        if (st != BLK_OK) return st;
+        BLK_STEP(BLK_STEP_MLP_DOWN);
+        return log.end();
+    }
+    const void* mlp_in;
+    if (pre) {
+        // 4. h = x + o W_o^T (+b_o);  5. n2 = norm(h)
+        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, x, nullptr, hb, T, D, Hd, cs, ds);
+        if (st != BLK_OK) return st;
+        BLK_STEP(BLK_STEP_O_PROJ);
+        e = launch_norm(t, rms, hb, nullptr, w->mlp_norm_w, w->mlp_norm_b, n2, T, static_cast<int>(D), d->eps, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "mlp norm launch");
+        BLK_STEP(BLK_STEP_MLP_NORM);
+        mlp_in = n2;
+    } else {
+        // 4. a = o W_o^T;  5. h = x + RMS(a) * w_post_attn
+        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd, cs, ds);
+        if (st != BLK_OK) return st;
+        BLK_STEP(BLK_STEP_O_PROJ);
+        e = launch_norm(t, true, tmp, x, w->post_attn_norm_w, nullptr, hb, T, static_cast<int>(D), d->eps, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "post-attention norm launch");
+        BLK_STEP(BLK_STEP_POST_ATTN_NORM);
+        mlp_in = hb;
+    }
+    // 6. MLP up (+activation)
+    st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, mlp_in, swiglu ? w->w_gate : w->w_up,
+                    swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds);
+    if (st != BLK_OK) return st;
+    BLK_STEP(BLK_STEP_MLP_UP);
+    if (pre) {
+        // 7. y = h + a W_d^T (+b_d)
+        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, hb, nullptr, y, T, D, F, cs, ds);
+        if (st != BLK_OK) return st;
+        BLK_STEP(BLK_STEP_MLP_DOWN);
+        return log.end();
+    }
+    // 7. m = a W_d^T;  8. y = h + RMS(m) * w_post_mlp
+    st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, nullptr, nullptr, tmp, T, D, F, cs, ds);
+    if (st != BLK_OK) return st;
+    BLK_STEP(BLK_STEP_MLP_DOWN);
+    e = launch_norm(t, true, tmp, hb, w->post_mlp_norm_w, nullptr, y, T, static_cast<int>(D), d->eps, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "post-mlp norm launch");
+    BLK_STEP(BLK_STEP_POST_MLP_NORM);
+    return log.end();
+#undef BLK_STEP
+}
+
+}  // extern "C"

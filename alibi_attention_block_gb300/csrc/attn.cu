@@ -1,0 +1,345 @@
+// K3: causal softmax attention, flash-style, on tcgen05 tensor cores.
+//
+// One CTA per (128-query tile, head, batch), heaviest (latest) query tiles
+// scheduled first. 6 warps:
+//   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into a
+//               STAGES-deep ring (128-byte swizzle, 64-column boxes)
+//   warp 1      TMEM allocator and single-thread MMA issuer:
+//                 S = Q K^T   (M=128, N=128, K=d; A and B K-major)  -> TMEM cols [0,128)
+//                 O += P V    (M=128, N=d,   K=128; P K-major from smem,
+//                              V MN-major from smem)                  -> TMEM cols [128,128+d)
+//               S_{j+1} is issued as soon as the softmax warps have read S_j,
+//               so the next QK^T overlaps the exponentials of this tile.
+//   warps 2..5  softmax, one thread per query row: tcgen05.ld of the row of
+//               S, scale (and the ALiBi bias -slope*(i-j), "Bloom in a sovereign
+//               engine", Contribution), causal mask on the diagonal tile,
+//               online max/sum in the exp2 domain, P rounded to the storage
+//               type into 128-byte-swizzled smem; O is rescaled in TMEM only
+//               when the running max grows by more than 2^8, so most tiles
+//               skip the rescale. Finally O / l is written as [B, S, H, d].
+// Query scale head_dim^-0.5 and GQA (kv head = h / (H/Hk)) follow nnterp
+// "stablelm" 03 Notes.
+#include "internal.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int kAttnThreads = 192;
+constexpr int kBQ = 128;
+constexpr int kBKV = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest unnormalised p
+
+template <int D>
+struct AttnCfg {
+    static constexpr int kSub = (D + 63) / 64;          // 64-column boxes per row
+    static constexpr int kTileBytes = kSub * kBQ * 128;  // 128 rows x kSub x 128 B
+    static constexpr int kStages = D > 128 ? 1 : 2;
+    static constexpr int kPBytes = 2 * kBQ * 128;        // 128 x 128 keys, 2 boxes
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmem = kTileBytes * (1 + 2 * kStages) + kPBytes + 1024 + kBarBytes;
+    static constexpr uint32_t kTmemCols = (kBKV + D) <= 256 ? 256 : 512;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+    using Cfg = AttnCfg<D>;
+    constexpr int kStages = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sKV = sQ + Cfg::kTileBytes;  // stage i: K at +2i, V at +2i+1 tiles
+    const uint32_t sP = sKV + 2 * kStages * Cfg::kTileBytes;
+    uint8_t* pP = smem + (sP - sQ);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(pP + Cfg::kPBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 3 * kStages);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t q_full = bar0;
+    const uint32_t s_full = bar0 + 8;
+    const uint32_t s_free = bar0 + 16;
+    const uint32_t p_full = bar0 + 24;
+    const uint32_t o_done = bar0 + 32;
+    auto k_full = [&](int i) { return bar0 + 64u + 8u * i; };
+    auto v_full = [&](int i) { return bar0 + 64u + 8u * (kStages + i); };
+    auto kv_empty = [&](int i) { return bar0 + 64u + 8u * (2 * kStages + i); };
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+
+    // tile decode: heaviest query tiles first
+    const int nq = (a.S + kBQ - 1) / kBQ;
+    const int bh_count = a.B * a.H;
+    const int qt = nq - 1 - static_cast<int>(blockIdx.x) / bh_count;
+    const int bh = static_cast<int>(blockIdx.x) % bh_count;
+    const int b = bh / a.H;
+    const int h = bh - b * a.H;
+    const int g = h / (a.H / a.Hk);
+    const int nkv = qt + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(kv_empty(i), 1);
+        }
+        fence_barrier_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tS = tmem_base;
+    const uint32_t tO = tmem_base + kBKV;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_expect_tx(q_full, Cfg::kTileBytes);
+#pragma unroll
+            for (int sub = 0; sub < Cfg::kSub; ++sub)
+                tma_load_3d(sQ + sub * kBQ * 128, &tmQ, q_full, sub * 64, qt * kBQ, b * a.H + h);
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j % kStages;
+                const uint32_t ph = (j / kStages) & 1;
+                if (!mbar_wait(kv_empty(st), ph ^ 1u, a.err)) break;
+                const uint32_t sK = sKV + (2 * st) * Cfg::kTileBytes;
+                const uint32_t sV = sK + Cfg::kTileBytes;
+                mbar_expect_tx(k_full(st), Cfg::kTileBytes);
+#pragma unroll
+                for (int sub = 0; sub < Cfg::kSub; ++sub)
+                    tma_load_3d(sK + sub * kBKV * 128, &tmK, k_full(st), sub * 64, j * kBKV,
+                                b * a.Hk + g);
+                mbar_expect_tx(v_full(st), Cfg::kTileBytes);
+#pragma unroll
+                for (int sub = 0; sub < Cfg::kSub; ++sub)
+                    tma_load_3d(sV + sub * kBKV * 128, &tmV, v_full(st), sub * 64, j * kBKV,
+                                b * a.Hk + g);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t fmt = dt_traits<T>::mma_fmt;
+            constexpr uint32_t idesc_s = make_idesc_f16(fmt, kBQ, kBKV, false);
+            constexpr uint32_t idesc_o = make_idesc_f16(fmt, kBQ, D, true);
+            bool ok = mbar_wait(q_full, 0, a.err);
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % kStages;
+                if (!mbar_wait(k_full(st), (j / kStages) & 1, a.err)) return false;
+                tc_fence_after();
+                const uint32_t sK = sKV + (2 * st) * Cfg::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * (kBQ * 128) + (ks % 4) * 32;
+                    tc_mma_ss(tS, make_sdesc_sw128(sQ + off, 16, 1024),
+                              make_sdesc_sw128(sK + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(s_full);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int st = j % kStages;
+                if (j + 1 < nkv) {
+                    if (!mbar_wait(s_free, j & 1, a.err)) break;
+                    tc_fence_after();
+                    if (!issue_s(j + 1)) break;
+                }
+                if (!mbar_wait(p_full, j & 1, a.err)) break;
+                if (!mbar_wait(v_full(st), (j / kStages) & 1, a.err)) break;
+                tc_fence_after();
+                const uint32_t sV = sKV + (2 * st + 1) * Cfg::kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < kBKV / 16; ++ks) {
+                    const uint32_t pa = sP + (ks / 4) * (kBQ * 128) + (ks % 4) * 32;
+                    const uint32_t vb = sV + ks * 16 * 128;
+                    tc_mma_ss(tO, make_sdesc_sw128(pa, 16, 1024),
+                              make_sdesc_sw128(vb, kBKV * 128, 1024), idesc_o,
+                              (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(o_done);
+                tc_commit(kv_empty(st));
+            }
+        }
+    } else {
+        // softmax warps: thread owns query row `row` of the tile
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int qpos = qt * kBQ + row;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const float scale_l2 = a.scale * kLog2e;
+        float slope_l2 = 0.f;
+        if (a.alibi) {
+            const float slope = a.slopes ? a.slopes[h]
+                                         : exp2f(-8.0f * static_cast<float>(h + 1) /
+                                                 static_cast<float>(a.H));
+            slope_l2 = slope * kLog2e;
+        }
+        float m_used = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            if (!mbar_wait(s_full, j & 1, a.err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[kBKV];
+#pragma unroll
+            for (int c = 0; c < kBKV / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tS + lane_off + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+
+            const int kbase = j * kBKV;
+            const bool need_mask = (j == qt) || (kbase + kBKV > a.S);
+            const float bias0 = slope_l2 * static_cast<float>(kbase - qpos);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kBKV; ++i) {
+                float x = fmaf(s[i], scale_l2, fmaf(slope_l2, static_cast<float>(i), bias0));
+                if (need_mask && (kbase + i > qpos || kbase + i >= a.S)) x = -INFINITY;
+                s[i] = x;
+                mx = fmaxf(mx, x);
+            }
+            float corr = 1.f;
+            const float m_new = fmaxf(m_used, mx);
+            if (m_new > m_used + kRescaleThreshold) {
+                corr = ex2_approx(m_used - m_new);
+                m_used = m_new;
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < kBKV; ++i) {
+                s[i] = ex2_approx(s[i] - m_used);
+                sum += s[i];
+            }
+            l = l * corr + sum;
+
+            if (j > 0) {
+                if (!mbar_wait(o_done, (j - 1) & 1, a.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + lane_off + c * 32, r);
+                        uint32_t lo[16], hi[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            lo[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                            hi[i] = __float_as_uint(__uint_as_float(r[16 + i]) * corr);
+                        }
+                        tmem_st16(tO + lane_off + c * 32, lo);
+                        tmem_st16(tO + lane_off + c * 32 + 16, hi);
+                    }
+                }
+            }
+            // P row -> smem, K-major, 128-byte swizzle (16-byte chunk c of a
+            // 128-byte row r lives at chunk c ^ (r & 7))
+#pragma unroll
+            for (int ch = 0; ch < kBKV / 8; ++ch) {
+                uint4 u;
+                u.x = dt_traits<T>::pack2(s[ch * 8 + 0], s[ch * 8 + 1]);
+                u.y = dt_traits<T>::pack2(s[ch * 8 + 2], s[ch * 8 + 3]);
+                u.z = dt_traits<T>::pack2(s[ch * 8 + 4], s[ch * 8 + 5]);
+                u.w = dt_traits<T>::pack2(s[ch * 8 + 6], s[ch * 8 + 7]);
+                const int sub = ch / 8, c16 = ch % 8;
+                uint8_t* dst = pP + sub * (kBQ * 128) + row * 128 + ((c16 ^ (row & 7)) * 16);
+                *reinterpret_cast<uint4*>(dst) = u;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && mbar_wait(o_done, (nkv - 1) & 1, a.err)) {
+            tc_fence_after();
+            const float inv_l = 1.0f / l;
+            T* dst = static_cast<T*>(a.o) +
+                     ((static_cast<int64_t>(b) * a.S + qpos) * a.H + h) * static_cast<int64_t>(D);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tO + lane_off + c * 32, r);
+                if (qpos < a.S) {
+                    float o[8];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(r[v * 8 + e]) * inv_l;
+                        store8(dst + c * 32 + v * 8, o);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_d(DType dt, const AttnArgs& a, cudaStream_t s) {
+    using Cfg = AttnCfg<D>;
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_3d(&tq, dt, a.q, static_cast<uint64_t>(a.B) * a.H, a.S, D, kBQ) ||
+        !make_tmap_3d(&tk, dt, a.k, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kBKV) ||
+        !make_tmap_3d(&tv, dt, a.v, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kBKV))
+        return cudaErrorInvalidValue;
+    auto kern = attn_kernel<T, D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int64_t grid = static_cast<int64_t>((a.S + kBQ - 1) / kBQ) * a.B * a.H;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    kern<<<static_cast<unsigned>(grid), kAttnThreads, Cfg::kSmem, s>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(DType dt, const AttnArgs& a, cudaStream_t s) {
+    switch (a.d) {
+        case 64: return launch_d<T, 64>(dt, a, s);
+        case 128: return launch_d<T, 128>(dt, a, s);
+        case 160: return launch_d<T, 160>(dt, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s) {
+    if (a.B == 0 || a.S == 0) return cudaSuccess;
+    if (dt == DType::F16) return launch_t<__half>(dt, a, s);
+    return launch_t<__nv_bfloat16>(dt, a, s);
+}
+
+}  // namespace blk

@@ -1,0 +1,284 @@
+// Device-side primitives shared by the sm_103a kernels: mbarriers with
+// bounded waits, TMA tensor loads, tcgen05 (TMEM allocation, MMA, commit,
+// TMEM loads/stores) and the shared-memory matrix descriptors they read.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace blk {
+
+// ---------------------------------------------------------------- errors --
+// Device error word codes (first failure wins; the host reads and clears it).
+enum : unsigned { DEV_ERR_NONE = 0u, DEV_ERR_TIMEOUT = 1u };
+
+// Upper bound on any single wait inside a kernel. Legitimate waits in these
+// kernels last microseconds; a wait this long means a lost arrival.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void report_error(unsigned* err, unsigned code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+// ------------------------------------------------------------ dtype ------
+template <typename T> struct dt_traits;
+template <> struct dt_traits<__half> {
+    static constexpr uint32_t mma_fmt = 0;  // kind::f16 operand format: f16
+    static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ float2 unpack2(uint32_t u) {
+        __half2 h = *reinterpret_cast<__half2*>(&u);
+        return __half22float2(h);
+    }
+};
+template <> struct dt_traits<__nv_bfloat16> {
+    static constexpr uint32_t mma_fmt = 1;  // kind::f16 operand format: bf16
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ float2 unpack2(uint32_t u) {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+        return __bfloat1622float2(h);
+    }
+};
+
+// 8 storage elements <-> 8 floats through one 16-byte access.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&f)[8]) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = dt_traits<T>::unpack2(w[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const float (&f)[8]) {
+    uint4 u;
+    u.x = dt_traits<T>::pack2(f[0], f[1]);
+    u.y = dt_traits<T>::pack2(f[2], f[3]);
+    u.z = dt_traits<T>::pack2(f[4], f[5]);
+    u.w = dt_traits<T>::pack2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+
+// ------------------------------------------------------------ rotary -----
+// Rotary angles p * theta_j reduced to about [-pi, pi] in fp32 with ~1e-6 rad
+// absolute error up to p = 2^20. theta_j = theta_hi + theta_lo (split on the
+// host from the double value); the product's rounding error is recovered with
+// an fma; the reduction by 2*pi = c1 + c2 + c3 follows Cody and Waite
+// (c1 has few significant bits so k * c1 is exact).
+constexpr int kMaxRotaryPairs = 128;
+struct RopeParams {
+    int span;  // rotary span r (even); 0 = off
+    float c1, c2, c3, inv_2pi;
+    float theta_hi[kMaxRotaryPairs];
+    float theta_lo[kMaxRotaryPairs];
+};
+
+__device__ __forceinline__ void rope_cos_sin(const RopeParams& rp, int pos, int j, float& c,
+                                             float& s) {
+    const float p = static_cast<float>(pos);
+    const float hi = rp.theta_hi[j];
+    const float a = p * hi;
+    float e = fmaf(p, hi, -a);
+    e = fmaf(p, rp.theta_lo[j], e);
+    const float k = rintf(a * rp.inv_2pi);
+    float r = fmaf(-k, rp.c1, a);
+    r = fmaf(-k, rp.c2, r);
+    r = fmaf(-k, rp.c3, r);
+    r += e;
+    sincosf(r, &s, &c);
+}
+
+// ---------------------------------------------------------- smem/mbar ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (TMA, tensor cores).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity to complete. Gives up after
+// kWaitLimitNs: sets the error word and returns false.
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
+            report_error(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- TMA ---
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// ------------------------------------------------------------- tcgen05 ---
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     slot_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive (once) on `bar` when every tcgen05 op this thread issued so far completes.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction of shape given by idesc.
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::f16 with fp32 accumulation.
+// Bits: [4,6) D format (1 = f32); [7,10) A format; [10,13) B format
+// (0 = f16, 1 = bf16); 15 A major (0 = K); 16 B major (0 = K, 1 = MN);
+// [17,23) N >> 3; [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t fmt, int m, int n,
+                                                      bool b_mn_major) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((static_cast<uint32_t>(n) >> 3) << 17) | ((static_cast<uint32_t>(m) >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle. [0,14) start >> 4;
+// [16,30) leading byte offset >> 4; [32,46) stride byte offset >> 4;
+// [46,48) = 1 (descriptor version); [61,64) = 2 (128B swizzle).
+// K-major tiles: rows of 128 bytes, 8-row groups SBO = 1024 bytes apart
+// (LBO unused). MN-major tiles: 64-element MN atoms LBO bytes apart, 8-row
+// K groups SBO = 1024 bytes apart.
+__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// 32 lanes x 32 consecutive 32-bit TMEM columns per warp; thread t gets lane
+// (taddr.lane + t). The wait is inside the same asm so the results are ready.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+// 32 lanes x 16 columns store, then wait for it.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Round a dynamic shared-memory pointer up so its shared-window offset is a
+// multiple of 1024 bytes (the 128B-swizzle atom); callers reserve 1 KB slack.
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+    const uint32_t pad = (1024u - (smem_u32(p) & 1023u)) & 1023u;
+    return p + pad;
+}
+
+}  // namespace blk

@@ -1,0 +1,352 @@
+// K2: C = A B^T on tcgen05 tensor cores, with the block's epilogues fused.
+//
+// A [M, K] (activations) and B [N, K] (a torch-convention weight W[out, in])
+// are both K-major. Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0      TMA producer: 128x64 A tile and BNx64 B tile per stage
+//               (128-byte swizzle) into a STAGES-deep shared-memory ring
+//   warp 1      TMEM allocator and single-thread MMA issuer:
+//               tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16 per
+//               instruction, fp32 accumulators in TMEM, double-buffered so
+//               the epilogue of tile i overlaps the mainloop of tile i+1
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per load (one
+//               thread per output row), fused op, 16-byte global stores
+// Epilogues (the block's steps after each projection):
+//   EPI_LINEAR  + bias, + up to two residuals (o_proj and down_proj residual adds)
+//   EPI_SWIGLU  B tile = [gate rows | up rows]; out = silu(gate) * up
+//               (nnterp "stablelm" 02 support(): mlp_neurons = act(gate)*up)
+//   EPI_GELU    gelu_tanh(acc + bias) (Bloom's MLP)
+//   EPI_QKV     + bias, optional partial NeoX rotary on q/k heads (span <= 32),
+//               scatter of the [M, (H+2Hk)d] projection into head-split q, k, v
+//               for stacked or per-head interleaved ([head][q,k,v][d]) rows
+//               ("Bloom in a sovereign engine", Contribution: de-interleave).
+#include "internal.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kGemmThreads = 192;
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kABytes = kBM * kBK * 2;
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmem = kStages * kStageBytes + 1024 + kBarBytes;
+    static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+};
+
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, const float (&o)[32], int valid) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if (v * 8 < valid) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = o[v * 8 + e];
+            store8(dst + v * 8, f);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void add_row32(const T* src, float (&o)[32], int valid) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if (v * 8 < valid) {
+            float f[8];
+            load8(src + v * 8, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[v * 8 + e] += f[e];
+        }
+    }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ float gelu_tanh_f(float z) {
+    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+    return 0.5f * z * (1.0f + tanhf(k0 * (z + 0.044715f * z * z * z)));
+}
+
+template <typename T, int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParams& rp,
+                                              uint32_t tbase, int m, int nt) {
+    const bool row_ok = m < g.M;
+    if constexpr (EPI == EPI_SWIGLU) {
+        constexpr int kHalf = BN / 2;
+#pragma unroll 1
+        for (int c = 0; c < kHalf / 32; ++c) {
+            uint32_t gr[32], ur[32];
+            tmem_ld32(tbase + c * 32, gr);
+            tmem_ld32(tbase + kHalf + c * 32, ur);
+            const int n0 = nt * kHalf + c * 32;
+            if (!row_ok || n0 >= g.N) continue;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                o[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+            store_row32(static_cast<T*>(g.out) + static_cast<int64_t>(m) * g.N + n0, o, g.N - n0);
+        }
+    } else if constexpr (EPI == EPI_QKV) {
+        const int d = g.d;
+        const int b = m / g.S;
+        const int s = m - b * g.S;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            const int n0 = nt * BN + c * 32;
+            if (!row_ok || n0 >= g.N) continue;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, 32);
+            int which, head, dd0;
+            if (g.interleaved) {
+                head = n0 / (3 * d);
+                const int w = n0 - head * 3 * d;
+                which = w / d;
+                dd0 = w - which * d;
+            } else {
+                const int hd = g.H * d, kd = g.Hk * d;
+                which = n0 < hd ? 0 : (n0 < hd + kd ? 1 : 2);
+                const int off = which == 0 ? 0 : (which == 1 ? hd : hd + kd);
+                head = (n0 - off) / d;
+                dd0 = n0 - off - head * d;
+            }
+            if (which < 2 && rp.span > 0 && dd0 == 0) {
+                const int half = rp.span / 2;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (j < half) {
+                        float cs, sn;
+                        rope_cos_sin(rp, s, j, cs, sn);
+                        const float x1 = o[j], x2 = o[j + half];
+                        o[j] = x1 * cs - x2 * sn;
+                        o[j + half] = x2 * cs + x1 * sn;
+                    }
+                }
+            }
+            T* base = static_cast<T*>(which == 0 ? g.q : (which == 1 ? g.k : g.v));
+            const int nheads = which == 0 ? g.H : g.Hk;
+            T* dst = base + ((static_cast<int64_t>(b) * nheads + head) * g.S + s) * d + dd0;
+            store_row32(dst, o, 32);
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            const int n0 = nt * BN + c * 32;
+            if (!row_ok || n0 >= g.N) continue;
+            const int valid = g.N - n0;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
+            if constexpr (EPI == EPI_GELU) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
+            }
+            const int64_t off = static_cast<int64_t>(m) * g.N + n0;
+            if (g.res1) add_row32(static_cast<const T*>(g.res1) + off, o, valid);
+            if (g.res2) add_row32(static_cast<const T*>(g.res2) + off, o, valid);
+            store_row32(static_cast<T*>(g.out) + off, o, valid);
+        }
+    }
+}
+
+template <typename T, int BN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmB2, const GemmArgs g,
+                const __grid_constant__ RopeParams rp) {
+    using Cfg = GemmCfg<BN>;
+    constexpr int kStages = Cfg::kStages;
+    constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int i) { return bar0 + 8u * i; };
+    auto empty = [&](int i) { return bar0 + 8u * (kStages + i); };
+    auto tfull = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
+    auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 + i); };
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full(i), 1);
+            mbar_init(empty(i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull(i), 1);
+            mbar_init(tempty(i), 4);
+        }
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmB2);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int m_tiles = (g.M + kBM - 1) / kBM;
+    const int n_tiles = (g.N + kBNOut - 1) / kBNOut;
+    const int num_tiles = m_tiles * n_tiles;
+    const int kb_count = (g.K + kBK - 1) / kBK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const int mt = t % m_tiles, nt = t / m_tiles;
+                for (int kb = 0; kb < kb_count; ++kb) {
+                    if (!mbar_wait(empty(stage), phase ^ 1u, g.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + stage * Cfg::kStageBytes;
+                    const uint32_t sb = sa + Cfg::kABytes;
+                    mbar_expect_tx(full(stage), Cfg::kStageBytes);
+                    tma_load_2d(sa, &tmA, full(stage), kb * kBK, mt * kBM);
+                    if constexpr (EPI == EPI_SWIGLU) {
+                        tma_load_2d(sb, &tmB, full(stage), kb * kBK, nt * kBNOut);
+                        tma_load_2d(sb + (BN / 2) * 128, &tmB2, full(stage), kb * kBK, nt * kBNOut);
+                    } else {
+                        tma_load_2d(sb, &tmB, full(stage), kb * kBK, nt * BN);
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc_f16(dt_traits<T>::mma_fmt, kBM, BN, false);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait(tempty(acc), acc_phase ^ 1u, g.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < kb_count; ++kb) {
+                    if (!mbar_wait(full(stage), phase, g.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * Cfg::kStageBytes;
+                    const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        const uint64_t ad = make_sdesc_sw128(sa + k * 32, 16, 1024);
+                        const uint64_t bd = make_sdesc_sw128(sb + k * 32, 16, 1024);
+                        tc_mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit(tfull(acc));
+            }
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        int it = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!mbar_wait(tfull(acc), acc_phase, g.err)) break;
+            tc_fence_after();
+            const int mt = t % m_tiles, nt = t / m_tiles;
+            const uint32_t tbase =
+                tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+            epilogue_tile<T, BN, EPI>(g, rp, tbase, mt * kBM + row, nt);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(acc));
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+template <typename T, int BN, int EPI>
+cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                       const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
+    using Cfg = GemmCfg<BN>;
+    constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
+    auto kern = gemm_kernel<T, BN, EPI>;
+    static bool attr_set = false;  // per template instance
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int64_t tiles = static_cast<int64_t>((g.M + kBM - 1) / kBM) * ((g.N + kBNOut - 1) / kBNOut);
+    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+    kern<<<grid, kGemmThreads, Cfg::kSmem, s>>>(ta, tb, tb2, g, rp);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(DType dt, int epi, const void* a, const void* b, const void* b2,
+                     const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
+    constexpr int BN = 256;
+    CUtensorMap ta, tb, tb2;
+    const uint32_t b_box = epi == EPI_SWIGLU ? BN / 2 : BN;
+    if (!make_tmap_2d(&ta, dt, a, g.M, g.K, kBM)) return cudaErrorInvalidValue;
+    if (!make_tmap_2d(&tb, dt, b, g.N, g.K, b_box)) return cudaErrorInvalidValue;
+    tb2 = tb;
+    if (epi == EPI_SWIGLU && !make_tmap_2d(&tb2, dt, b2, g.N, g.K, b_box))
+        return cudaErrorInvalidValue;
+    switch (epi) {
+        case EPI_LINEAR: return launch_cfg<T, BN, EPI_LINEAR>(ta, tb, tb2, g, rp, num_sms, s);
+        case EPI_SWIGLU: return launch_cfg<T, BN, EPI_SWIGLU>(ta, tb, tb2, g, rp, num_sms, s);
+        case EPI_GELU: return launch_cfg<T, BN, EPI_GELU>(ta, tb, tb2, g, rp, num_sms, s);
+        case EPI_QKV: return launch_cfg<T, BN, EPI_QKV>(ta, tb, tb2, g, rp, num_sms, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const void* b2,
+                        const GemmArgs& args, const RopeParams& rp, int num_sms, cudaStream_t s) {
+    if (args.M == 0 || args.N == 0) return cudaSuccess;
+    if (dt == DType::F16) return launch_t<__half>(dt, epi, a, b, b2, args, rp, num_sms, s);
+    return launch_t<__nv_bfloat16>(dt, epi, a, b, b2, args, rp, num_sms, s);
+}
+
+}  // namespace blk

@@ -1,0 +1,77 @@
+// Host-side launch interface between the C-ABI layer (api.cu) and the
+// kernel translation units. Launchers assume validated arguments.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace blk {
+
+enum class DType { F16 = 0, BF16 = 1 };
+
+// ---- K1: row norms (norm.cu)
+cudaError_t launch_norm(DType dt, bool rms, const void* x, const void* res, const void* gamma,
+                        const void* beta, void* y, int64_t rows, int cols, float eps,
+                        cudaStream_t s);
+
+// ---- K4/K5: qk-norm + rotary on head-split q/k, in place (rope.cu)
+enum QkNormMode { QKN_NONE = 0, QKN_RMS_FULL = 1, QKN_LN_PER_HEAD = 2 };
+struct QkNormRopeArgs {
+    void* q;            // [B, H, S, d]
+    void* k;            // [B, Hk, S, d] or nullptr (then Hk must be 0)
+    const void* q_w;    // norm weights (mode-dependent layout) or nullptr
+    const void* k_w;
+    const void* q_bias; // [H*d] or nullptr (added first)
+    const void* k_bias; // [Hk*d] or nullptr
+    int B, S, H, Hk, d;
+    int mode;           // QkNormMode
+    float eps;
+};
+cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopeParams& rp,
+                                cudaStream_t s);
+
+// ---- K2: tcgen05 GEMM with fused epilogues (gemm.cu)
+enum GemmEpi { EPI_LINEAR = 0, EPI_SWIGLU = 1, EPI_GELU = 2, EPI_QKV = 3 };
+struct GemmArgs {
+    int M, N, K;          // out is [M, N]; for SWIGLU N = intermediate (gate/up rows each)
+    void* out;            // LINEAR / SWIGLU / GELU output, row stride N
+    const void* bias;     // [N] or nullptr
+    const void* res1;     // [M, N] or nullptr
+    const void* res2;
+    // EPI_QKV: scatter of [M, (H+2Hk)d] into head-split q/k/v
+    void* q;
+    void* k;
+    void* v;
+    int S, H, Hk, d, interleaved;
+    unsigned* err;
+};
+// a: [M, K]; b: [N(or N rows of gate), K]; b2: up weights for SWIGLU.
+cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const void* b2,
+                        const GemmArgs& args, const RopeParams& rp, int num_sms, cudaStream_t s);
+
+// ---- K3: tcgen05 flash attention (attn.cu)
+struct AttnArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    int B, S, H, Hk, d;
+    float scale;
+    int alibi;
+    const float* slopes;  // device [H] or nullptr (standard slopes)
+    unsigned* err;
+};
+cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s);
+
+// ---- tensor maps (api.cu)
+// 2D row-major [rows, cols] map with a {64, box_rows} box and 128B swizzle.
+bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows);
+// 3D [planes, rows, cols] map with a {64, box_rows, 1} box and 128B swizzle.
+bool make_tmap_3d(CUtensorMap* m, DType dt, const void* base, uint64_t planes, uint64_t rows,
+                  uint64_t cols, uint32_t box_rows);
+
+}  // namespace blk

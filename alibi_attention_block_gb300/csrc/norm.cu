@@ -1,0 +1,155 @@
+// K1: row norms. LayerNorm with bias ("StableLM-2: partial RoPE and a first
+// LayerNorm-with-bias path", section 1) and RMSNorm ("OLMo-2: reordered (post)
+// normalization", section 1), with an optional residual added after the norm
+// (the OLMo-2 post-norm add).
+//
+// HBM-bound: each row is read once into registers with 16-byte loads (a group
+// of TPR threads per row, VPT 8-element vectors per thread), reduced with warp
+// shuffles (plus shared memory when a row spans several warps), normalised
+// from registers (two-pass mean/variance, fp32) and written once.
+#include "internal.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int kNormThreads = 256;
+
+template <int TPR>
+__device__ __forceinline__ float row_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if constexpr (TPR > 32) {
+        constexpr int kWarpsPerRow = TPR / 32;
+        const int warp = threadIdx.x / 32;
+        const int first = (warp / kWarpsPerRow) * kWarpsPerRow;
+        __syncthreads();
+        if ((threadIdx.x & 31) == 0) red[warp] = v;
+        __syncthreads();
+        v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarpsPerRow; ++w) v += red[first + w];
+    }
+    return v;
+}
+
+template <typename T, int TPR, int VPT, bool RMS>
+__global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict__ x,
+                                                            const T* __restrict__ res,
+                                                            const T* __restrict__ gamma,
+                                                            const T* __restrict__ beta,
+                                                            T* __restrict__ y, int64_t rows,
+                                                            int cols, float eps) {
+    __shared__ float red[kNormThreads / 32];
+    constexpr int kRowsPerBlock = kNormThreads / TPR;
+    const int sub = threadIdx.x % TPR;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + threadIdx.x / TPR;
+    const bool active = row < rows;
+    const int nvec = cols / 8;
+    const T* xr = x + (active ? row : 0) * cols;
+
+    float v[VPT][8];
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int vi = sub + i * TPR;
+        if (active && vi < nvec) {
+            load8(xr + vi * 8, v[i]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[i][e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum += v[i][e];
+    }
+    float mean = 0.f;
+    if constexpr (!RMS) mean = row_sum<TPR>(sum, red) / static_cast<float>(cols);
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int vi = sub + i * TPR;
+        if (vi < nvec) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float c = v[i][e] - mean;
+                sq += c * c;
+            }
+        }
+    }
+    const float rstd = rsqrtf(row_sum<TPR>(sq, red) / static_cast<float>(cols) + eps);
+    if (!active) return;
+    T* yr = y + row * cols;
+    const T* rr = res ? res + row * cols : nullptr;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        const int vi = sub + i * TPR;
+        if (vi >= nvec) continue;
+        float g[8], o[8];
+        load8(gamma + vi * 8, g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (v[i][e] - mean) * rstd * g[e];
+        if (!RMS && beta) {
+            float b[8];
+            load8(beta + vi * 8, b);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] += b[e];
+        }
+        if (rr) {
+            float r[8];
+            load8(rr + vi * 8, r);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] += r[e];
+        }
+        store8(yr + vi * 8, o);
+    }
+}
+
+template <typename T, int TPR, int VPT>
+cudaError_t launch_tv(bool rms, const void* x, const void* res, const void* g, const void* b,
+                      void* y, int64_t rows, int cols, float eps, cudaStream_t s) {
+    constexpr int kRowsPerBlock = kNormThreads / TPR;
+    const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    auto args = [&](auto kern) {
+        kern<<<static_cast<unsigned>(blocks), kNormThreads, 0, s>>>(
+            static_cast<const T*>(x), static_cast<const T*>(res), static_cast<const T*>(g),
+            static_cast<const T*>(b), static_cast<T*>(y), rows, cols, eps);
+    };
+    if (rms)
+        args(norm_kernel<T, TPR, VPT, true>);
+    else
+        args(norm_kernel<T, TPR, VPT, false>);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(bool rms, const void* x, const void* res, const void* g, const void* b,
+                     void* y, int64_t rows, int cols, float eps, cudaStream_t s) {
+    const int nvec = cols / 8;
+    // One warp per row while a lane holds at most 8 vectors (cols <= 2048);
+    // wider rows spread over 2..8 warps.
+#define BLK_NORM_CASE(TPR, VPT) \
+    if (nvec <= (TPR) * (VPT)) return launch_tv<T, TPR, VPT>(rms, x, res, g, b, y, rows, cols, eps, s)
+    BLK_NORM_CASE(32, 1);
+    BLK_NORM_CASE(32, 2);
+    BLK_NORM_CASE(32, 4);
+    BLK_NORM_CASE(32, 8);
+    BLK_NORM_CASE(64, 8);
+    BLK_NORM_CASE(128, 8);
+    BLK_NORM_CASE(256, 8);
+#undef BLK_NORM_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_norm(DType dt, bool rms, const void* x, const void* res, const void* gamma,
+                        const void* beta, void* y, int64_t rows, int cols, float eps,
+                        cudaStream_t s) {
+    if (rows == 0) return cudaSuccess;
+    if (dt == DType::F16)
+        return launch_t<__half>(rms, x, res, gamma, beta, y, rows, cols, eps, s);
+    return launch_t<__nv_bfloat16>(rms, x, res, gamma, beta, y, rows, cols, eps, s);
+}
+
+}  // namespace blk

@@ -1,0 +1,163 @@
+// K4/K5: in-place qk-norm and partial NeoX split-half rotary on head-split
+// q [B, H, S, d] and k [B, Hk, S, d].
+//
+// Per token (b, s) one CTA stages the token's q heads and k heads in shared
+// memory as fp32 (16-byte loads per head row), then:
+//   1. adds the q/k bias (the projection bias comes before the rotary:
+//      nnterp "stablelm" 03 Notes, "Biased queries, keys and values"),
+//   2. QKN_RMS_FULL: one RMSNorm over the whole H*d (and Hk*d) row ("OLMo-2:
+//      reordered (post) normalization", section 1: full-width, not per head);
+//      QKN_LN_PER_HEAD: one bias-free LayerNorm per head (nnterp "stablelm"
+//      03 Notes, "Per-head LayerNorms on queries and keys on 12B"),
+//   3. rotates pairs (j, j + r/2), j < r/2, of each head by p * theta_j
+//      ("StableLM-2: partial RoPE ...", section 1); dims >= r pass through,
+//   4. writes the rows back with 16-byte stores.
+// HBM-bound: every element of q and k is read and written once.
+#include "internal.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int kRopeThreads = 128;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRopeThreads / 32; ++w) t += red[w];
+    return t;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRopeThreads) qk_norm_rope_kernel(QkNormRopeArgs a,
+                                                                    RopeParams rp) {
+    extern __shared__ float buf[];  // (H + Hk) * d floats
+    __shared__ float red[kRopeThreads / 32];
+    const int token = blockIdx.x;
+    const int b = token / a.S;
+    const int s = token % a.S;
+    const int d = a.d;
+    const int nh = a.H + a.Hk;
+    const int nvec = nh * d / 8;
+    const int vpr = d / 8;  // vectors per head row
+
+    auto row_ptr = [&](int head) -> T* {
+        if (head < a.H)
+            return static_cast<T*>(a.q) + ((static_cast<int64_t>(b) * a.H + head) * a.S + s) * d;
+        return static_cast<T*>(a.k) +
+               ((static_cast<int64_t>(b) * a.Hk + (head - a.H)) * a.S + s) * d;
+    };
+
+    // 1. load (+ bias)
+    for (int i = threadIdx.x; i < nvec; i += kRopeThreads) {
+        const int head = i / vpr;
+        const int c = (i % vpr) * 8;
+        float f[8];
+        load8(row_ptr(head) + c, f);
+        const T* bias = head < a.H ? static_cast<const T*>(a.q_bias) : static_cast<const T*>(a.k_bias);
+        if (bias) {
+            float bb[8];
+            load8(bias + (head < a.H ? head : head - a.H) * d + c, bb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] += bb[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) buf[head * d + c + e] = f[e];
+    }
+    __syncthreads();
+
+    // 2. qk-norm
+    if (a.mode == QKN_RMS_FULL) {
+        for (int part = 0; part < 2; ++part) {
+            const int h0 = part == 0 ? 0 : a.H;
+            const int n = (part == 0 ? a.H : a.Hk) * d;
+            if (n == 0) continue;
+            float sq = 0.f;
+            for (int i = threadIdx.x; i < n; i += kRopeThreads) {
+                const float t = buf[h0 * d + i];
+                sq += t * t;
+            }
+            const float rstd = rsqrtf(block_sum(sq, red) / static_cast<float>(n) + a.eps);
+            const T* w = static_cast<const T*>(part == 0 ? a.q_w : a.k_w);
+            for (int i = threadIdx.x; i < n; i += kRopeThreads)
+                buf[h0 * d + i] *= rstd * dt_traits<T>::to_f(w[i]);
+        }
+        __syncthreads();
+    } else if (a.mode == QKN_LN_PER_HEAD) {
+        const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+        for (int head = warp; head < nh; head += kRopeThreads / 32) {
+            float* r = buf + head * d;
+            float sum = 0.f;
+            for (int i = lane; i < d; i += 32) sum += r[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float mean = sum / static_cast<float>(d);
+            float sq = 0.f;
+            for (int i = lane; i < d; i += 32) {
+                const float c = r[i] - mean;
+                sq += c * c;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            const float rstd = rsqrtf(sq / static_cast<float>(d) + a.eps);
+            const T* g = head < a.H ? static_cast<const T*>(a.q_w) + head * d
+                                    : static_cast<const T*>(a.k_w) + (head - a.H) * d;
+            for (int i = lane; i < d; i += 32) r[i] = (r[i] - mean) * rstd * dt_traits<T>::to_f(g[i]);
+        }
+        __syncthreads();
+    }
+
+    // 3. rotary over the first rp.span dims of every q and k head
+    const int half = rp.span / 2;
+    if (half > 0) {
+        for (int i = threadIdx.x; i < nh * half; i += kRopeThreads) {
+            const int head = i / half;
+            const int j = i % half;
+            float c, sn;
+            rope_cos_sin(rp, s, j, c, sn);
+            float* r = buf + head * d;
+            const float x1 = r[j], x2 = r[j + half];
+            r[j] = x1 * c - x2 * sn;
+            r[j + half] = x2 * c + x1 * sn;
+        }
+        __syncthreads();
+    }
+
+    // 4. store
+    for (int i = threadIdx.x; i < nvec; i += kRopeThreads) {
+        const int head = i / vpr;
+        const int c = (i % vpr) * 8;
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = buf[head * d + c + e];
+        store8(row_ptr(head) + c, f);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopeParams& rp,
+                                cudaStream_t s) {
+    const int64_t tokens = static_cast<int64_t>(a.B) * a.S;
+    if (tokens == 0) return cudaSuccess;
+    const size_t smem = static_cast<size_t>(a.H + a.Hk) * a.d * sizeof(float);
+    if (dt == DType::F16) {
+        auto k = qk_norm_rope_kernel<__half>;
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        k<<<static_cast<unsigned>(tokens), kRopeThreads, smem, s>>>(a, rp);
+    } else {
+        auto k = qk_norm_rope_kernel<__nv_bfloat16>;
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        k<<<static_cast<unsigned>(tokens), kRopeThreads, smem, s>>>(a, rp);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace blk

@@ -1,0 +1,364 @@
+"""Prefill tokens/s of one decoder block on GB300, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = one blk_forward of the whole block (input norm, QKV projection with
+bias and partial rotary, causal flash attention, output projection with the
+residual add, MLP norm, gate/up SwiGLU, down projection with the residual add)
+over one batch of synthetic input already resident in HBM. L2 is flushed
+(a 512 MiB write) before every step, outside the step's own events.
+
+N > 1 (torchrun): every rank runs its own replica of the workload on its own
+GPU (the block has no cross-GPU exchange); value = all ranks' tokens / the
+slowest rank's time ("scaling": "weak").
+
+--impl reference times the fp64 CPU oracle (the correctness reference) on the
+host cores, one sequence of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "prefill tokens/s per block and attention TFLOP/s (% of GB300 FP16 peak) at 1 GPU"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return None, 0, 1, 0
+
+
+# --------------------------------------------------------------- work model --
+def step_work(cfg):
+    """Algorithmic flops (and bytes) of each launch kind for one forward."""
+    T, D, F = cfg.tokens, cfg.hidden, cfg.intermediate
+    H, Hk, d, S, B = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.seq, cfg.batch
+    e = 2  # bytes per element
+    n_up = 2 * F if cfg.act == "swiglu" else F
+    return {
+        "input_norm": dict(flops=0, bytes=2 * T * D * e),
+        "qkv": dict(flops=2 * T * D * (H + 2 * Hk) * d, bytes=(T * D + (H + 2 * Hk) * d * (D + T)) * e),
+        "qk_norm_rope": dict(flops=0, bytes=2 * T * (H + Hk) * d * e),
+        # causal: only the S(S+1)/2 unmasked scores, QK^T and PV
+        "attention": dict(flops=4 * B * H * d * S * (S + 1) // 2, bytes=(2 * T * H * d + 2 * T * Hk * d) * e),
+        "o_proj": dict(flops=2 * T * H * d * D, bytes=(T * H * d + D * H * d + 2 * T * D) * e),
+        "post_attn_norm": dict(flops=0, bytes=3 * T * D * e),
+        "mlp_norm": dict(flops=0, bytes=2 * T * D * e),
+        "mlp_up": dict(flops=2 * T * D * n_up, bytes=(T * D + n_up * D + T * F) * e),
+        "mlp_down": dict(flops=2 * T * F * D, bytes=(T * F + D * F + 2 * T * D) * e),
+        "post_mlp_norm": dict(flops=0, bytes=3 * T * D * e),
+    }
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:
+            sel = ["-i", str(device_index)]
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "100", *sel]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        rows = []
+        for line in open(self.out.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+                except ValueError:
+                    pass
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- oracle --
+def time_oracle(cfg, budget_s: float = 20.0, max_seqs: int | None = None):
+    """The fp64 oracle on host cores, one sequence of the workload at a time
+    until the budget is spent. Returns (tokens/s, tokens, seconds, sample)."""
+    import oracle
+    x, w = workloads.block_inputs(cfg)
+    done, t0 = 0, time.perf_counter()
+    n = cfg.batch if max_seqs is None else min(max_seqs, cfg.batch)
+    for b in range(n):
+        one = workloads.scaled(cfg, batch=1)
+        oracle.block_forward(one, x[b:b + 1], w)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done * cfg.seq / dt, done * cfg.seq, dt, f"{done} of {cfg.batch} sequences x {cfg.seq} tokens"
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return
+    cores = os.cpu_count()
+    for _ in range(args.warmup):
+        time_oracle(cfg, budget_s=0.0, max_seqs=1)
+    times = []
+    for _ in range(args.steps):
+        _, _, dt, _ = time_oracle(cfg, budget_s=0.0, max_seqs=1)
+        times.append(dt)
+    total = sum(times)
+    value = args.steps * cfg.seq / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(cfg, "none (CPU)"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one sequence of {cfg.seq} tokens (batch element 0) per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(cfg, l2):
+    return {"workload": f"{cfg.name} block prefill", "global_batch": cfg.batch, "seq_len": cfg.seq,
+            "hidden": cfg.hidden, "heads": cfg.n_heads, "kv_heads": cfg.n_kv_heads,
+            "head_dim": cfg.head_dim, "intermediate": cfg.intermediate,
+            "rotary_span": cfg.rotary_span, "alibi": cfg.alibi, "storage": cfg.dtype,
+            "parallelism": "replicas", "l2": l2}
+
+
+# -------------------------------------------------------------------- ours --
+def run_ours(args, cfg, rank, world, local_rank, dist):
+    import ctypes as C
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import alibi_attention_block_gb300 as blk
+    from alibi_attention_block_gb300 import _abi
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = _abi.load()
+    x_cpu, w_cpu = workloads.block_inputs(cfg)
+    x = x_cpu.to(dev)
+    wd = {k: t.to(dev) for k, t in w_cpu.items()}
+    y = torch.empty_like(x)
+    ws_bytes = blk.forward_workspace_size(cfg, cfg.batch, cfg.seq)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    desc = blk.block_desc(cfg, cfg.batch, cfg.seq)
+    wstruct = _abi.BlockWeights(*[(wd[n].data_ptr() if n in wd else None) for n in _abi.WEIGHT_SLOTS])
+    dt = _abi.BLK_F16 if cfg.dtype == "fp16" else _abi.BLK_BF16
+    stream = torch.cuda.current_stream()
+    max_ev = 11
+    kinds = (C.c_int32 * 10)()
+    nl = C.c_int(0)
+
+    def one_step(events):
+        arr = (C.c_void_p * max_ev)(*[e.cuda_event for e in events]) if events else None
+        _abi.check(lib.blk_forward_ex(C.byref(desc), C.byref(wstruct), C.c_void_p(x.data_ptr()),
+                                      C.c_void_p(y.data_ptr()), C.c_void_p(ws.data_ptr()), ws_bytes,
+                                      dt, C.c_void_p(stream.cuda_stream), arr,
+                                      max_ev if events else 0, kinds, C.byref(nl)),
+                   "blk_forward_ex")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        one_step(None)
+    torch.cuda.synchronize()
+    blk.check_device_status()
+    n_launch = nl.value
+    step_names = [_abi.STEP_NAMES[kinds[i]] for i in range(n_launch)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(max_ev)] for _ in range(args.steps)]
+
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            one_step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    blk.check_device_status()
+    clocks = clk.summary()
+
+    step_ms = [e[0].elapsed_time(e[n_launch]) for e in evs]
+    per_kind = {}
+    for e in evs:
+        for j, name in enumerate(step_names):
+            per_kind.setdefault(name, []).append(e[j].elapsed_time(e[j + 1]))
+    kernel_ms = {k: float(np.mean(v)) for k, v in per_kind.items()}
+    total_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * cfg.tokens * args.steps / (total_ms / 1e3)
+
+    # e2e through the public Python API: pinned host x -> device -> forward -> pinned host y
+    x_host = x_cpu.pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x_e2e = torch.empty_like(x)
+    for _ in range(2):
+        x_e2e.copy_(x_host, non_blocking=True)
+        blk.forward(cfg, wd, x_e2e, workspace=ws, out=y)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 50))
+    e0.record()
+    for _ in range(e2e_steps):
+        x_e2e.copy_(x_host, non_blocking=True)
+        blk.forward(cfg, wd, x_e2e, workspace=ws, out=y)
+        y_host.copy_(y, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    work = step_work(cfg)
+    dom = max(kernel_ms, key=kernel_ms.get)
+    dw = work[dom]
+    if dw["flops"]:
+        achieved = dw["flops"] / (kernel_ms[dom] / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_source": peaks["source"] + " sustained bf16"}
+    else:
+        achieved = dw["bytes"] / (kernel_ms[dom] / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"] + " copy"}
+    kernels = {}
+    for k, ms in kernel_ms.items():
+        w_ = work[k]
+        ent = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4)}
+        if w_["flops"]:
+            ent["tflops"] = round(w_["flops"] / (ms / 1e3) / 1e12, 1)
+        else:
+            ent["gbs"] = round(w_["bytes"] / (ms / 1e3) / 1e9, 1)
+        kernels[k] = ent
+    attn = None
+    if "attention" in kernel_ms:
+        at = work["attention"]["flops"] / (kernel_ms["attention"] / 1e3) / 1e12
+        attn = {"tflops": at, "frac_of_measured_bf16_peak": at / peaks["bf16_tflops"],
+                "frac_of_nominal_2250": at / 2250.0}
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, n_tok, secs, sample = time_oracle(cfg, budget_s=args.cpu_budget)
+        cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{sample} ({secs:.1f} s, fp64 NumPy)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights)",
+        "config": _config(cfg, "flushed before every step (512 MiB write)"),
+        "block_tflops": sum(work[k]["flops"] for k in kernel_ms) / (ms_per_step / 1e3) / 1e12,
+        "attention": attn,
+        "kernels": kernels,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * cfg.tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": y.numel() * y.element_size()},
+        "gpu_launches": n_launch * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="stablelm2_1p6b", choices=sorted(workloads.BLOCK_CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = workloads.BLOCK_CONFIGS[args.config]
+    dist, rank, world, local_rank = _dist()
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+    else:
+        run_ours(args, cfg, rank, world, local_rank, dist)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,242 @@
+/*
+ * blk.h - C ABI of the GB300 (sm_103a) prefill forward of one decoder block.
+ *
+ * The block, as the pages state it:
+ *   - sequential pre-norm (nnterp encyclopedia "stablelm", 03 Notes, "The
+ *     block is sequential on 1.6B and 3B"): h = x + attn(LN1(x)); y = h + mlp(LN2(h))
+ *   - parallel (same section, 12B): n = LN(x); y = x + attn(n) + mlp(n)
+ *   - reordered post-norm ("OLMo-2: reordered (post) normalization", section 1):
+ *     no input norm; h = x + RMS(attn(x)); y = h + RMS(mlp(h))
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are DEVICE pointers owned by the caller. The library
+ *     allocates no device memory, frees nothing and never synchronises a
+ *     stream (blk_check_device_status is the one call that does, by design).
+ *   - Work is enqueued on the caller's stream `s` (a cudaStream_t; NULL is the
+ *     legacy default stream) and runs asynchronously.
+ *   - Row-major, contiguous, 16-byte-aligned tensors. Linear weights follow the
+ *     torch convention W[out, in], y = x W^T + b (nnterp "stablelm" Printout).
+ *   - Storage dtype `dt` is fp16 or bf16 for every tensor of a call, except
+ *     ALiBi slopes (fp32). All accumulation and statistics are fp32. K/V are
+ *     read at the stated dtype: nothing is silently converted.
+ *   - Every call validates its arguments before any launch and returns a
+ *     blk_status; a rejected call has no side effects. blk_last_error() gives a
+ *     thread-local message for the last failure.
+ *   - Every wait inside a kernel is bounded (about 2 s); on timeout the kernel
+ *     sets a device error word and exits. blk_check_device_status() reports it.
+ */
+#ifndef BLK_H
+#define BLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* blk_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    BLK_OK = 0,
+    BLK_EINVAL = 1,        /* bad argument: null pointer, bad size, misalignment */
+    BLK_EUNSUPPORTED = 2,  /* valid request outside what the kernels implement */
+    BLK_ECUDA = 3,         /* a CUDA runtime/driver call failed */
+    BLK_ETIMEOUT = 4,      /* a bounded in-kernel wait gave up (device error word) */
+    BLK_EWORKSPACE = 5     /* workspace pointer null or smaller than required */
+} blk_status;
+
+typedef enum { BLK_F16 = 0, BLK_BF16 = 1 } blk_dtype;
+
+typedef enum { BLK_QKV_STACKED = 0, BLK_QKV_HEAD_INTERLEAVED = 1 } blk_qkv_layout;
+typedef enum { BLK_QKNORM_NONE = 0, BLK_QKNORM_RMS_FULL = 1, BLK_QKNORM_LN_PER_HEAD = 2 } blk_qk_norm;
+typedef enum { BLK_NORM_LAYERNORM = 0, BLK_NORM_RMS = 1 } blk_norm_kind;
+typedef enum { BLK_NORM_PRE = 0, BLK_NORM_POST = 1 } blk_norm_place;
+typedef enum { BLK_RESIDUAL_SEQUENTIAL = 0, BLK_RESIDUAL_PARALLEL = 1 } blk_residual;
+typedef enum { BLK_ACT_SWIGLU = 0, BLK_ACT_GELU_TANH = 1 } blk_act;
+
+/* ---- status ---------------------------------------------------------- */
+
+const char* blk_status_string(blk_status s);
+/* Message for the last failed call on this host thread ("" if none). */
+const char* blk_last_error(void);
+/* ABI version: (major << 16) | minor. */
+int blk_version(void);
+/* Synchronises `s`, then reads and clears the device error word of the
+ * current device. BLK_ETIMEOUT if an in-kernel bounded wait gave up since the
+ * last check; BLK_ECUDA on a CUDA error. */
+blk_status blk_check_device_status(blk_stream_t s);
+
+/* ---- norms ------------------------------------------------------------ */
+
+/* LayerNorm with bias ("StableLM-2: partial RoPE and a first
+ * LayerNorm-with-bias path", section 1; nnterp "stablelm" Printout):
+ *   y[r,:] = (x[r,:] - mean) / sqrt(var + eps) * gamma + beta  [+ residual[r,:]]
+ * population variance over `cols`. x, residual, y: [rows, cols]; gamma,
+ * beta: [cols]. beta NULL = bias-free LayerNorm. residual NULL = no add (the
+ * add, when given, comes after the norm). y may alias x. cols % 8 == 0,
+ * cols <= 16384. */
+blk_status blk_layernorm_bias(const void* x, const void* residual, const void* gamma,
+                              const void* beta, void* y, int64_t rows, int64_t cols, float eps,
+                              blk_dtype dt, blk_stream_t s);
+
+/* RMSNorm ("OLMo-2: reordered (post) normalization", section 1):
+ *   y[r,:] = x[r,:] / sqrt(mean(x[r,:]^2) + eps) * weight  [+ residual[r,:]]
+ * Same layout and rules as blk_layernorm_bias. With a residual this is the
+ * OLMo-2 post-norm add: h = residual + RMS(sublayer_out). */
+blk_status blk_rmsnorm(const void* x, const void* residual, const void* weight, void* y,
+                       int64_t rows, int64_t cols, float eps, blk_dtype dt, blk_stream_t s);
+
+/* ---- projection, rotary, qk-norm -------------------------------------- */
+
+typedef struct {
+    int64_t batch, seq, hidden, n_heads, n_kv_heads, head_dim;
+    int32_t qkv_layout;  /* blk_qkv_layout; HEAD_INTERLEAVED needs n_heads == n_kv_heads */
+    int32_t qk_norm;     /* blk_qk_norm */
+    float qk_norm_eps;
+    int32_t rotary_span; /* 0..head_dim, even; 0 = rotary off (no trig evaluated) */
+    float rope_base;     /* theta_j = rope_base^(-2j/rotary_span), positions 0..seq-1 */
+} blk_qkv_desc;
+
+/* QKV projection with bias, de-interleave/head split, optional qk-norm and
+ * partial NeoX split-half rotary ("StableLM-2: partial RoPE ...", section 1;
+ * nnterp "stablelm" 03 Notes: bias added before the rotary, first
+ * rotary_span dims of each q/k head rotate as two halves, the rest pass
+ * through; "Bloom in a sovereign engine", Contribution: fused QKV
+ * de-interleave; "OLMo-2 ...", section 1: full-width QK RMSNorm; nnterp
+ * 03 Notes "Per-head LayerNorms on queries and keys on 12B").
+ *   x      [batch*seq, hidden]
+ *   w_qkv  [(H + 2*Hk)*d, hidden]: STACKED rows [Wq; Wk; Wv], or
+ *          HEAD_INTERLEAVED rows [head][q,k,v][d]
+ *   b_qkv  [(H + 2*Hk)*d] in the same row order, or NULL
+ *   q_norm_w / k_norm_w: RMS_FULL -> [H*d] / [Hk*d]; LN_PER_HEAD -> [H, d] /
+ *          [Hk, d] (bias-free LayerNorm per head, before the rotary); NONE -> NULL
+ *   q [batch, H, seq, d], k and v [batch, Hk, seq, d] (outputs).
+ * hidden % 8 == 0; head_dim a multiple of 32, at most 256. */
+blk_status blk_qkv_bias_rope_partial(const blk_qkv_desc* d, const void* x, const void* w_qkv,
+                                     const void* b_qkv, const void* q_norm_w,
+                                     const void* k_norm_w, void* q, void* k, void* v,
+                                     blk_dtype dt, blk_stream_t s);
+
+/* In-place optional bias add then partial NeoX rotary on a head-split tensor
+ * x [batch, n_heads, seq, head_dim] (positions 0..seq-1). bias: [n_heads*head_dim]
+ * or NULL. rotary_span 0 = bias only. Same rotary as blk_qkv_bias_rope_partial. */
+blk_status blk_rope_inplace(void* x, const void* bias, int64_t batch, int64_t n_heads,
+                            int64_t seq, int64_t head_dim, int32_t rotary_span, float rope_base,
+                            blk_dtype dt, blk_stream_t s);
+
+/* ---- attention -------------------------------------------------------- */
+
+typedef struct {
+    int64_t batch, seq, n_heads, n_kv_heads, head_dim;
+    float softmax_scale; /* <= 0 -> head_dim^-0.5 (nnterp "stablelm" 03 Notes) */
+    int32_t causal;      /* must be 1: prefill is causal */
+    int32_t alibi;       /* 0 off; 1: score -= slope_h * (query_pos - key_pos) */
+} blk_attn_desc;
+
+/* Causal softmax attention, flash-style on tcgen05 tensor cores, with
+ * optional ALiBi ("Bloom in a sovereign engine", Contribution: per-head
+ * geometric slope, linear pre-softmax bias; the bias is added after the
+ * score scale and is not scaled itself). GQA: kv head = h / (H / Hk).
+ *   q [batch, H, seq, d]; k, v [batch, Hk, seq, d]
+ *   alibi_slopes: device fp32 [H], or NULL with alibi=1 for the standard
+ *     slopes 2^(-8(h+1)/H) (H a power of two)
+ *   o [batch, seq, H, d] (= [batch*seq, H*d], what o_proj reads)
+ * head_dim in {64, 128, 160}. Rotary and ALiBi are exclusive at the block
+ * level: blk_forward rejects rotary_span > 0 together with alibi. */
+blk_status blk_attn_prefill(const blk_attn_desc* d, const void* q, const void* k, const void* v,
+                            const float* alibi_slopes, void* o, blk_dtype dt, blk_stream_t s);
+
+/* ---- linear and MLP --------------------------------------------------- */
+
+/* y = x W^T [+ bias] [+ res1] [+ res2] on tcgen05 tensor cores.
+ * x [m, k], w [n, k], bias [n], res1/res2/y [m, n]. k % 8 == 0, n % 8 == 0. */
+blk_status blk_linear(const void* x, const void* w, const void* bias, const void* res1,
+                      const void* res2, void* y, int64_t m, int64_t n, int64_t k, blk_dtype dt,
+                      blk_stream_t s);
+
+typedef struct {
+    int64_t tokens, hidden, intermediate;
+    int32_t act; /* blk_act */
+} blk_mlp_desc;
+
+/* Workspace bytes blk_mlp needs (the [tokens, intermediate] activation). */
+blk_status blk_mlp_workspace_size(const blk_mlp_desc* d, size_t* bytes);
+
+/* The MLP (nnterp "stablelm" Printout and 02 support(): mlp_neurons =
+ * act(gate)*up on a gated MLP):
+ *   SWIGLU:    a = silu(x Wg^T) * (x Wu^T)               (w_gate required, b_up NULL)
+ *   GELU_TANH: a = gelu_tanh(x Wu^T + b_up)              (w_gate NULL)
+ *   y = a Wd^T [+ b_down] [+ res1] [+ res2]
+ * x [tokens, hidden]; w_gate, w_up [intermediate, hidden]; w_down
+ * [hidden, intermediate]; res1, res2, y [tokens, hidden]. workspace holds a. */
+blk_status blk_mlp(const blk_mlp_desc* d, const void* x, const void* w_gate, const void* w_up,
+                   const void* b_up, const void* w_down, const void* b_down, const void* res1,
+                   const void* res2, void* y, void* workspace, size_t ws_bytes, blk_dtype dt,
+                   blk_stream_t s);
+
+/* ---- the block -------------------------------------------------------- */
+
+typedef struct {
+    blk_qkv_desc qkv;     /* shapes, QKV layout, qk-norm, rotary */
+    int32_t norm_kind;    /* blk_norm_kind, for the block norms */
+    int32_t norm_place;   /* blk_norm_place: PRE (input norm) or POST (OLMo-2 reordered) */
+    int32_t residual;     /* blk_residual */
+    float eps;            /* block norm eps */
+    int32_t alibi;        /* 1: ALiBi with standard slopes (or w->alibi_slopes); needs rotary_span 0 */
+    int64_t intermediate; /* MLP width */
+    int32_t act;          /* blk_act */
+} blk_block_desc;
+
+/* Named weight slots. Each norm has its own slot; no slot is read in place of
+ * another ("OLMo-2 ...", section 1: the loader-clobber root cause). Unused
+ * slots must be NULL. */
+typedef struct {
+    const void *attn_norm_w, *attn_norm_b;       /* PRE: input norm (LayerNorm bias nullable) */
+    const void *mlp_norm_w, *mlp_norm_b;         /* PRE + SEQUENTIAL: MLP norm */
+    const void *post_attn_norm_w, *post_mlp_norm_w; /* POST: RMSNorms on sublayer outputs */
+    const void *w_qkv, *b_qkv, *q_norm_w, *k_norm_w;
+    const void *w_o, *b_o;
+    const void *w_gate, *w_up, *b_up, *w_down, *b_down;
+    const float* alibi_slopes;                   /* optional device fp32 [H] */
+} blk_block_weights;
+
+/* Workspace bytes blk_forward needs for this descriptor. */
+blk_status blk_forward_workspace_size(const blk_block_desc* d, size_t* bytes);
+
+/* The prefill forward of one decoder block: x [batch, seq, hidden] ->
+ * y [batch, seq, hidden]. y must not alias x. Every step runs in this
+ * library's kernels on stream s; workspace (caller-owned device memory of at
+ * least blk_forward_workspace_size bytes) holds the intermediates. */
+blk_status blk_forward(const blk_block_desc* d, const blk_block_weights* w, const void* x,
+                       void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s);
+
+/* Kinds of the kernel launches blk_forward enqueues, in the order they run. */
+typedef enum {
+    BLK_STEP_INPUT_NORM = 0,   /* input LayerNorm/RMSNorm (pre-norm blocks) */
+    BLK_STEP_QKV = 1,          /* projection + bias (+ fused rotary) + head split */
+    BLK_STEP_QK_NORM_ROPE = 2, /* qk-norm and/or rotary wider than the fused span */
+    BLK_STEP_ATTENTION = 3,    /* causal flash attention (+ALiBi) */
+    BLK_STEP_O_PROJ = 4,       /* output projection (+bias, +residual) */
+    BLK_STEP_POST_ATTN_NORM = 5, /* OLMo-2: h = x + RMS(attn_out) */
+    BLK_STEP_MLP_NORM = 6,     /* LN/RMS of h (sequential pre-norm) */
+    BLK_STEP_MLP_UP = 7,       /* gate/up GEMM + SwiGLU, or up GEMM + bias + GELU */
+    BLK_STEP_MLP_DOWN = 8,     /* down GEMM (+bias, +residuals) */
+    BLK_STEP_POST_MLP_NORM = 9 /* OLMo-2: y = h + RMS(mlp_out) */
+} blk_step_kind;
+
+/* blk_forward, also reporting its kernel launches. If `events` is non-NULL
+ * it points to n_events cudaEvent_t handles (created by the caller): events[0]
+ * is recorded on s before the first launch and events[i] right after launch
+ * i, for i < n_events; the time between events[i-1] and events[i] is launch
+ * i's duration on the stream. If step_kinds is non-NULL it receives the
+ * blk_step_kind of each launch (room for n_events - 1 entries, at most 10 are
+ * written). *n_launches (nullable) receives the number of launches. */
+blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, const void* x,
+                          void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s,
+                          void* const* events, int n_events, int32_t* step_kinds, int* n_launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLK_H */

@@ -1,0 +1,175 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+include/blk.h declares, rejects bad arguments before any CUDA call, and links
+no vendor BLAS/DNN library (the pages' linkage audit: "StableLM-2: partial
+RoPE ..." section 6, "Bloom in a sovereign engine" Methods, "OLMo-2 ..."
+section 6)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+from alibi_attention_block_gb300 import _abi, build
+
+FAKE = 0x100000  # 16-byte-aligned stand-in address; validation rejects before any access
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _abi.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = _abi.header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_abi._PROTOS), "binding and header disagree"
+    nm = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], capture_output=True,
+                        text=True).stdout
+    exported = set(re.findall(r"\sT\s(blk_\w+)", nm))
+    assert set(names) <= exported
+
+
+def test_links_no_vendor_math_library(lib):
+    out = subprocess.run(["ldd", _abi.LIB_PATH], capture_output=True, text=True).stdout
+    for bad in ("cublas", "cudnn", "cutlass", "cusparse", "nccl"):
+        assert bad not in out.lower(), out
+
+
+def test_sources_use_no_cluster_multicast():
+    csrc = os.path.join(os.path.dirname(_abi.HERE), "alibi_attention_block_gb300", "csrc")
+    for f in os.listdir(csrc):
+        text = open(os.path.join(csrc, f)).read()
+        assert "multicast::cluster" not in text, f
+        assert "wgmma" not in text and "mma.sync" not in text, f
+
+
+def test_status_strings_and_version(lib):
+    assert lib.blk_status_string(_abi.BLK_EINVAL) == b"BLK_EINVAL"
+    assert lib.blk_status_string(_abi.BLK_ETIMEOUT) == b"BLK_ETIMEOUT"
+    assert lib.blk_version() >> 16 == 1
+
+
+def _err(lib):
+    return lib.blk_last_error().decode()
+
+
+def test_norm_validation(lib):
+    st = lib.blk_layernorm_bias(None, None, FAKE, None, FAKE, 4, 64, 1e-5, 0, None)
+    assert st == _abi.BLK_EINVAL and "x is NULL" in _err(lib)
+    st = lib.blk_rmsnorm(FAKE, None, FAKE, FAKE, 4, 60, 1e-5, 1, None)
+    assert st == _abi.BLK_EINVAL and "multiple of 8" in _err(lib)
+    st = lib.blk_rmsnorm(FAKE + 4, None, FAKE, FAKE, 4, 64, 1e-5, 1, None)
+    assert st == _abi.BLK_EINVAL and "aligned" in _err(lib)
+    st = lib.blk_layernorm_bias(FAKE, None, FAKE, None, FAKE, 4, 64, 1e-5, 7, None)
+    assert st == _abi.BLK_EINVAL and "dtype" in _err(lib)
+
+
+def test_attention_validation(lib):
+    d = _abi.AttnDesc(1, 128, 4, 4, 96, -1.0, 1, 0)
+    assert lib.blk_attn_prefill(C.byref(d), FAKE, FAKE, FAKE, None, FAKE, 1, None) == _abi.BLK_EUNSUPPORTED
+    d = _abi.AttnDesc(1, 128, 4, 4, 64, -1.0, 0, 0)
+    assert lib.blk_attn_prefill(C.byref(d), FAKE, FAKE, FAKE, None, FAKE, 1, None) == _abi.BLK_EUNSUPPORTED
+    assert "causal" in _err(lib)
+    d = _abi.AttnDesc(1, 128, 6, 4, 64, -1.0, 1, 0)
+    assert lib.blk_attn_prefill(C.byref(d), FAKE, FAKE, FAKE, None, FAKE, 1, None) == _abi.BLK_EINVAL
+    d = _abi.AttnDesc(1, 128, 12, 12, 64, -1.0, 1, 1)   # standard slopes need 2^k heads
+    assert lib.blk_attn_prefill(C.byref(d), FAKE, FAKE, FAKE, None, FAKE, 1, None) == _abi.BLK_EUNSUPPORTED
+    d = _abi.AttnDesc(1, 128, 4, 4, 64, -1.0, 1, 0)     # slopes with alibi off
+    assert lib.blk_attn_prefill(C.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, 1, None) == _abi.BLK_EINVAL
+
+
+def test_qkv_validation(lib):
+    d = _abi.QkvDesc(1, 16, 256, 4, 4, 64, _abi.BLK_QKV_STACKED, 0, 1e-5, 15, 1e4)
+    assert lib.blk_qkv_bias_rope_partial(C.byref(d), FAKE, FAKE, None, None, None, FAKE, FAKE,
+                                         FAKE, 1, None) == _abi.BLK_EINVAL     # odd span
+    d = _abi.QkvDesc(1, 16, 256, 4, 2, 64, _abi.BLK_QKV_HEAD_INTERLEAVED, 0, 1e-5, 0, 1e4)
+    assert lib.blk_qkv_bias_rope_partial(C.byref(d), FAKE, FAKE, None, None, None, FAKE, FAKE,
+                                         FAKE, 1, None) == _abi.BLK_EINVAL     # interleaved GQA
+    d = _abi.QkvDesc(1, 16, 256, 4, 4, 64, _abi.BLK_QKV_STACKED, 1, 1e-6, 0, 1e4)
+    assert lib.blk_qkv_bias_rope_partial(C.byref(d), FAKE, FAKE, None, None, None, FAKE, FAKE,
+                                         FAKE, 1, None) == _abi.BLK_EINVAL     # missing q_norm_w
+    assert "q_norm_w" in _err(lib)
+
+
+def _block(**kw):
+    q = _abi.QkvDesc(1, 128, 256, 4, 4, 64, 0, 0, 1e-5, 16, 1e4)
+    for k, v in kw.pop("qkv", {}).items():
+        setattr(q, k, v)
+    d = _abi.BlockDesc(q, _abi.BLK_NORM_LAYERNORM, _abi.BLK_NORM_PRE,
+                       _abi.BLK_RESIDUAL_SEQUENTIAL, 1e-5, 0, 688, _abi.BLK_ACT_SWIGLU)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def _weights(**kw):
+    base = dict(attn_norm_w=FAKE, mlp_norm_w=FAKE, w_qkv=FAKE, w_o=FAKE, w_gate=FAKE, w_up=FAKE,
+                w_down=FAKE)
+    base.update(kw)
+    return _abi.BlockWeights(*[base.get(n) for n in _abi.WEIGHT_SLOTS])
+
+
+def _fwd(lib, d, w, ws_bytes=1 << 40):
+    return lib.blk_forward(C.byref(d), C.byref(w), FAKE, FAKE + 4096, FAKE, ws_bytes, 1, None)
+
+
+def test_forward_rejects_rotary_with_alibi(lib):
+    assert _fwd(lib, _block(alibi=1), _weights()) == _abi.BLK_EUNSUPPORTED
+    assert "exclusive" in _err(lib)
+
+
+def test_forward_slot_rules(lib):
+    """A weight in a slot the block does not read is an error, never ignored;
+    a required slot left empty is an error (the loader-clobber lesson,
+    "OLMo-2 ..." section 1 and section 6)."""
+    post = dict(norm_kind=_abi.BLK_NORM_RMS, norm_place=_abi.BLK_NORM_POST)
+    w_post = dict(attn_norm_w=None, mlp_norm_w=None, post_attn_norm_w=FAKE, post_mlp_norm_w=FAKE)
+    # post-norm block handed a pre-norm slot
+    assert _fwd(lib, _block(**post), _weights(**dict(w_post, mlp_norm_w=FAKE))) == _abi.BLK_EINVAL
+    assert "mlp_norm_w" in _err(lib)
+    # post-norm block missing its MLP norm
+    assert _fwd(lib, _block(**post), _weights(**dict(w_post, post_mlp_norm_w=None))) == _abi.BLK_EINVAL
+    assert "post_mlp_norm_w" in _err(lib)
+    # parallel block has no MLP norm
+    par = dict(residual=_abi.BLK_RESIDUAL_PARALLEL)
+    assert _fwd(lib, _block(**par), _weights()) == _abi.BLK_EINVAL
+    # GELU block must not get a gate weight
+    assert _fwd(lib, _block(act=_abi.BLK_ACT_GELU_TANH), _weights()) == _abi.BLK_EINVAL
+    assert "w_gate" in _err(lib)
+
+
+def test_forward_workspace_check(lib):
+    assert _fwd(lib, _block(), _weights(), ws_bytes=16) == _abi.BLK_EWORKSPACE
+    need = C.c_size_t(0)
+    assert lib.blk_forward_workspace_size(C.byref(_block()), C.byref(need)) == _abi.BLK_OK
+    # n1, q, k, v, o, h, n2, a, tmp for T = 128 tokens, all 256-byte aligned
+    T, D, F = 128, 256, 688
+    assert need.value == 2 * T * (D * 4 + 256 * 4 + F)
+
+
+def test_mlp_validation(lib):
+    d = _abi.MlpDesc(128, 256, 688, _abi.BLK_ACT_SWIGLU)
+    st = lib.blk_mlp(C.byref(d), FAKE, None, FAKE, None, FAKE, None, None, None, FAKE, FAKE,
+                     1 << 30, 1, None)
+    assert st == _abi.BLK_EINVAL and "w_gate" in _err(lib)
+    st = lib.blk_mlp(C.byref(d), FAKE, FAKE, FAKE, None, FAKE, None, None, None, FAKE, FAKE, 8,
+                     1, None)
+    assert st == _abi.BLK_EWORKSPACE
+
+
+def test_linear_validation(lib):
+    assert lib.blk_linear(FAKE, FAKE, None, None, None, FAKE, 128, 100, 256, 1, None) == _abi.BLK_EINVAL
+    assert lib.blk_linear(FAKE, FAKE, None, None, None, FAKE, 0, 128, 256, 1, None) == _abi.BLK_OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+
+    import alibi_attention_block_gb300 as blk
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        blk.rmsnorm(x, torch.ones(64, dtype=torch.bfloat16))

@@ -1,0 +1,91 @@
+"""GPU parity of blk_forward (the whole block) against the fp64 oracle.
+
+Small configs of every variant are compared on every output element; the
+full-size workloads (StableLM-2-1.6B, Bloom-560m, OLMo-2-1B shapes, launched
+exactly as bench.py times them) on a seeded sample of token rows that the
+oracle evaluates one by one."""
+import numpy as np
+import pytest
+import torch
+
+import alibi_attention_block_gb300 as blk
+import oracle
+import workloads
+from tests.parity import check, f64, to_dev
+from workloads import BLOCK_CONFIGS, scaled
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny_stablelm2": BLOCK_CONFIGS["tiny_stablelm2"],
+    "stablelm2_ragged_bf16": scaled(BLOCK_CONFIGS["stablelm2_1p6b"], batch=2, seq=200, hidden=256,
+                                    n_heads=4, n_kv_heads=4, intermediate=688),
+    "bloom_small": scaled(BLOCK_CONFIGS["bloom_560m"], batch=2, seq=256, hidden=256, n_heads=4,
+                          n_kv_heads=4, intermediate=1024),
+    "olmo2_small": scaled(BLOCK_CONFIGS["olmo2_1b"], batch=2, seq=300, hidden=256, n_heads=2,
+                          n_kv_heads=2, intermediate=512),
+    "stablelm2_12b_small": scaled(BLOCK_CONFIGS["stablelm2_12b"], batch=1, seq=260, hidden=320,
+                                  n_heads=8, n_kv_heads=2, intermediate=512),
+}
+
+
+def _gpu_forward(cfg, x, w):
+    wd = {k: to_dev(t) for k, t in w.items()}
+    y = blk.forward(cfg, wd, to_dev(x))
+    blk.check_device_status()
+    return y
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from alibi_attention_block_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_block_small(name):
+    cfg = SMALL[name]
+    x, w = workloads.block_inputs(cfg)
+    y = _gpu_forward(cfg, x, w)
+    ref = oracle.block_forward(cfg, x, w)["y"]
+    check(y, ref, name, unit_scale=True)
+
+
+def test_block_deterministic():
+    cfg = SMALL["stablelm2_ragged_bf16"]
+    x, w = workloads.block_inputs(cfg)
+    assert torch.equal(_gpu_forward(cfg, x, w), _gpu_forward(cfg, x, w))
+
+
+def test_block_alibi_explicit_slopes_match_standard():
+    cfg = SMALL["bloom_small"]
+    x, w = workloads.block_inputs(cfg)
+    y_std = _gpu_forward(cfg, x, w)
+    slopes = torch.tensor(oracle.alibi_slopes(cfg.n_heads), dtype=torch.float32)
+    y_exp = _gpu_forward(cfg, x, dict(w, alibi_slopes=slopes))
+    check(y_exp, f64(y_std), "explicit vs standard slopes", unit_scale=True, abs_tol=1e-2)
+
+
+def test_block_negative_control_full_rotary_diverges():
+    """Rotating the whole head changes the output (the full-RoPE control of
+    "StableLM-2: partial RoPE ...", section 4); the GPU sees it as the oracle does."""
+    cfg = SMALL["stablelm2_ragged_bf16"]
+    x, w = workloads.block_inputs(cfg)
+    w = dict(w, w_qkv=w["w_qkv"] * 8)
+    y16 = f64(_gpu_forward(cfg, x, w))
+    y64 = f64(_gpu_forward(scaled(cfg, rotary_span=64), x, w))
+    assert np.abs(y16 - y64).max() > 0.05
+    check(y64, oracle.block_forward(scaled(cfg, rotary_span=64), x, w)["y"], "full rotary",
+          unit_scale=True)
+
+
+@pytest.mark.parametrize("name", ["stablelm2_1p6b", "bloom_560m", "olmo2_1b"])
+def test_block_full_size_sampled_rows(name):
+    cfg = BLOCK_CONFIGS[name]
+    x, w = workloads.block_inputs(cfg)
+    y = _gpu_forward(cfg, x, w)
+    rows = workloads.sample_rows(cfg.tokens, 48, seed=cfg.seed)
+    ref = oracle.block_forward(cfg, x, w, rows=rows)["y"]
+    got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
+    check(got, ref, f"{name} sampled rows", unit_scale=True)
+    assert torch.isfinite(y).all()

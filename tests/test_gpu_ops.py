@@ -1,0 +1,232 @@
+"""GPU parity of each C-ABI call against the fp64 oracle (element by element).
+
+Sizes span several tiles with ragged tails (rows, tokens, columns and
+sequence lengths that are not multiples of the 128-row tiles)."""
+import numpy as np
+import pytest
+import torch
+
+import alibi_attention_block_gb300 as blk
+import oracle
+import workloads
+from tests.parity import check, f64, to_dev
+from workloads import draw
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["fp16", "bf16"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from alibi_attention_block_gb300 import build
+    build.build()
+    yield
+    blk.check_device_status()
+
+
+# ------------------------------------------------------------------ norms --
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("rows,cols", [(1, 256), (77, 1024), (1000, 2048), (33, 5120), (5, 16384)])
+@pytest.mark.parametrize("kind", ["layernorm", "layernorm_nobias", "rmsnorm"])
+def test_norm(dt, rows, cols, kind):
+    seed = rows * 7 + cols
+    x = draw((rows, cols), dt, seed, scale=2.0)
+    g = draw((cols,), dt, seed + 1, "g")
+    b = draw((cols,), dt, seed + 2, "b")
+    res = draw((rows, cols), dt, seed + 3) if rows % 2 else None
+    eps = 1e-5
+    if kind == "rmsnorm":
+        out = blk.rmsnorm(to_dev(x), to_dev(g), residual=to_dev(res), eps=eps)
+        ref = oracle.rms_norm(f64(x), f64(g), eps)
+    else:
+        beta = b if kind == "layernorm" else None
+        out = blk.layernorm_bias(to_dev(x), to_dev(g), to_dev(beta), residual=to_dev(res), eps=eps)
+        ref = oracle.layer_norm(f64(x), f64(g), None if beta is None else f64(beta), eps)
+    if res is not None:
+        ref = ref + f64(res)
+    check(out, ref, f"{kind} {rows}x{cols}", unit_scale=True)
+
+
+def test_norm_in_place():
+    x = to_dev(draw((64, 2048), "bf16", 5))
+    g = to_dev(draw((2048,), "bf16", 6, "g"))
+    ref = oracle.rms_norm(f64(x), f64(g), 1e-6)
+    blk.rmsnorm(x, g, eps=1e-6, out=x)
+    check(x, ref, "rmsnorm in place", unit_scale=True)
+
+
+# ----------------------------------------------------------------- linear --
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("m,n,k", [(128, 256, 256), (200, 264, 688), (1000, 2048, 2048),
+                                   (37, 8, 8), (300, 768, 5632), (513, 1024, 64)])
+def test_linear(dt, m, n, k):
+    seed = m + n + k
+    x = draw((m, k), dt, seed)
+    w = draw((n, k), dt, seed + 1, "w")
+    bias = draw((n,), dt, seed + 2, "b") if m % 2 else None
+    r1 = draw((m, n), dt, seed + 3) if n % 3 else None
+    r2 = draw((m, n), dt, seed + 4) if k > 1000 else None
+    y = blk.linear(to_dev(x), to_dev(w), to_dev(bias), to_dev(r1), to_dev(r2))
+    ref = oracle.linear(f64(x), f64(w), None if bias is None else f64(bias))
+    for r in (r1, r2):
+        if r is not None:
+            ref = ref + f64(r)
+    check(y, ref, f"linear {m}x{n}x{k}")
+
+
+def test_linear_persistent_multi_wave():
+    """More output tiles than SMs: every CTA loops over several tiles and
+    both TMEM accumulators."""
+    x = draw((4096, 1024), "bf16", 11)
+    w = draw((4096, 1024), "bf16", 12, "w")
+    y = blk.linear(to_dev(x), to_dev(w))
+    rows = workloads.sample_rows(4096, 64)
+    ref = f64(x)[rows] @ f64(w).T
+    check(y[torch.as_tensor(rows, device="cuda")], ref, "linear multi-wave")
+
+
+# -------------------------------------------------------------------- MLP --
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("act,T,D,F", [("swiglu", 128, 256, 688), ("swiglu", 300, 512, 1024),
+                                       ("gelu_tanh", 200, 256, 1024), ("gelu_tanh", 64, 1024, 4096)])
+def test_mlp(dt, act, T, D, F):
+    seed = T + D + F
+    x = draw((T, D), dt, seed)
+    w_up = draw((F, D), dt, seed + 1, "w")
+    w_down = draw((D, F), dt, seed + 2, "w")
+    w = {"w_up": f64(w_up), "w_down": f64(w_down)}
+    kw = {}
+    if act == "swiglu":
+        w_gate = draw((F, D), dt, seed + 3, "w")
+        w["w_gate"] = f64(w_gate)
+        kw["w_gate"] = to_dev(w_gate)
+    else:
+        b_up = draw((F,), dt, seed + 4, "b")
+        b_down = draw((D,), dt, seed + 5, "b")
+        w["b_up"], w["b_down"] = f64(b_up), f64(b_down)
+        kw["b_up"], kw["b_down"] = to_dev(b_up), to_dev(b_down)
+    res = draw((T, D), dt, seed + 6)
+    y = blk.mlp(to_dev(x), to_dev(w_up), to_dev(w_down), res1=to_dev(res), act=act, **kw)
+    _, m = oracle.mlp(f64(x), w, act)
+    check(y, m + f64(res), f"mlp {act}")
+
+
+# -------------------------------------------------------------------- QKV --
+QKV_CASES = {
+    # name: (B, S, D, H, Hk, d, layout, qk_norm, r, base, bias)
+    "stablelm_fused_rope": (2, 200, 256, 4, 4, 64, "stacked", "none", 16, 1e4, True),
+    "bloom_interleaved": (2, 130, 256, 4, 4, 64, "head_interleaved", "none", 0, 1e4, True),
+    "olmo_rms_full_r128": (2, 150, 256, 2, 2, 128, "stacked", "rms_full", 128, 5e5, False),
+    "gqa_ln_per_head_r40": (1, 140, 320, 8, 2, 160, "stacked", "ln_per_head", 40, 1e4, False),
+    "full_span_r64": (1, 128, 256, 4, 4, 64, "stacked", "none", 64, 1e4, True),
+}
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("name", sorted(QKV_CASES))
+def test_qkv_bias_rope_partial(dt, name):
+    B, S, D, H, Hk, d, layout, qkn, r, base, bias = QKV_CASES[name]
+    seed = 100 * sorted(QKV_CASES).index(name) + 7
+    n_out = (H + 2 * Hk) * d
+    x = draw((B, S, D), dt, seed)
+    w = draw((n_out, D), dt, seed + 1, "w")
+    b = draw((n_out,), dt, seed + 2, "b") if bias else None
+    qnw = knw = None
+    if qkn == "rms_full":
+        qnw, knw = draw((H * d,), dt, seed + 3, "g"), draw((Hk * d,), dt, seed + 4, "g")
+    elif qkn == "ln_per_head":
+        qnw, knw = draw((H, d), dt, seed + 3, "g"), draw((Hk, d), dt, seed + 4, "g")
+    q, k, v = blk.qkv_bias_rope_partial(to_dev(x), to_dev(w), to_dev(b), n_heads=H, n_kv_heads=Hk,
+                                        head_dim=d, layout=layout, qk_norm=qkn, qk_norm_eps=1e-5,
+                                        rotary_span=r, rope_base=base, q_norm_w=to_dev(qnw),
+                                        k_norm_w=to_dev(knw))
+    qf, kf, vf = oracle.split_qkv(oracle.linear(f64(x), f64(w), None if b is None else f64(b)),
+                                  H, Hk, d, layout)
+    if qkn == "rms_full":
+        qf = oracle.qk_norm_full_rms(qf, f64(qnw), 1e-5)
+        kf = oracle.qk_norm_full_rms(kf, f64(knw), 1e-5)
+    qh, kh, vh = oracle.split_heads(qf, H, d), oracle.split_heads(kf, Hk, d), oracle.split_heads(vf, Hk, d)
+    if qkn == "ln_per_head":
+        qh = oracle.qk_norm_per_head_ln(qh, f64(qnw), 1e-5)
+        kh = oracle.qk_norm_per_head_ln(kh, f64(knw), 1e-5)
+    pos = np.arange(S)
+    check(q, oracle.rope(qh, pos, r, base), f"{name} q")
+    check(k, oracle.rope(kh, pos, r, base), f"{name} k")
+    check(v, vh, f"{name} v")
+    if qkn == "none" and 0 < r < d:
+        # past the span the queries are the projection output unchanged: bit-equal
+        # to the same projection with the rotary off
+        q0, k0, _ = blk.qkv_bias_rope_partial(to_dev(x), to_dev(w), to_dev(b), n_heads=H,
+                                              n_kv_heads=Hk, head_dim=d, layout=layout,
+                                              rotary_span=0)
+        assert torch.equal(q[..., r:], q0[..., r:]) and torch.equal(k[..., r:], k0[..., r:])
+        assert not torch.equal(q[..., 1:, :r], q0[..., 1:, :r])
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("r,bias", [(16, True), (0, True), (64, False)])
+def test_rope_inplace(dt, r, bias):
+    x = draw((2, 4, 100, 64), dt, 21 + r)
+    b = draw((4 * 64,), dt, 22, "b") if bias else None
+    xd = to_dev(x)
+    blk.rope_inplace(xd, to_dev(b), rotary_span=r, rope_base=1e4)
+    ref = f64(x)
+    if bias:
+        ref = ref + f64(b).reshape(4, 64)[None, :, None, :]
+    check(xd, oracle.rope(ref, np.arange(100), r, 1e4), f"rope r={r}")
+
+
+# -------------------------------------------------------------- attention --
+ATTN_CASES = [
+    # (B, H, Hk, S, d, alibi)
+    (1, 2, 2, 128, 64, False),
+    (2, 4, 4, 200, 64, False),
+    (1, 4, 2, 1000, 64, False),
+    (2, 4, 4, 384, 64, True),
+    (1, 2, 2, 333, 128, False),
+    (1, 4, 4, 256, 128, True),
+    (1, 4, 1, 300, 160, False),
+    (2, 2, 2, 129, 160, False),
+]
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: "B{}H{}Hk{}S{}d{}{}".format(*c[:5], "_alibi" if c[5] else ""))
+def test_attention(dt, case):
+    B, H, Hk, S, d, alibi = case
+    seed = B * 1000 + H * 100 + S + d
+    q = draw((B, H, S, d), dt, seed)
+    k = draw((B, Hk, S, d), dt, seed + 1)
+    v = draw((B, Hk, S, d), dt, seed + 2)
+    o = blk.attn_prefill(to_dev(q), to_dev(k), to_dev(v), alibi=alibi)
+    ref = oracle.attention(f64(q), f64(k), f64(v), slopes=oracle.alibi_slopes(H) if alibi else None)
+    check(o, ref.transpose(0, 2, 1, 3), f"attention {case}")
+
+
+def test_attention_explicit_slopes_and_scale():
+    B, H, S, d = 1, 4, 256, 64
+    q, k, v = (draw((B, H, S, d), "bf16", 40 + i) for i in range(3))
+    slopes = torch.tensor([0.5, 0.1, 0.0, 1.5], dtype=torch.float32)
+    o = blk.attn_prefill(to_dev(q), to_dev(k), to_dev(v), alibi=True, slopes=slopes.cuda(),
+                         scale=0.2)
+    ref = oracle.attention(f64(q), f64(k), f64(v), scale=0.2, slopes=slopes.double().numpy())
+    check(o, ref.transpose(0, 2, 1, 3), "attention explicit slopes")
+
+
+def test_attention_large_scores_stay_finite():
+    """Sharp softmax (scores of order 100) exercises the rescale path."""
+    B, H, S, d = 1, 2, 512, 64
+    q = draw((B, H, S, d), "bf16", 50, scale=6.0)
+    k = draw((B, H, S, d), "bf16", 51, scale=6.0)
+    v = draw((B, H, S, d), "bf16", 52)
+    o = blk.attn_prefill(to_dev(q), to_dev(k), to_dev(v))
+    ref = oracle.attention(f64(q), f64(k), f64(v))
+    check(o, ref.transpose(0, 2, 1, 3), "attention sharp")
+
+
+def test_attention_deterministic():
+    q, k, v = (to_dev(draw((2, 4, 700, 64), "bf16", 60 + i)) for i in range(3))
+    o1 = blk.attn_prefill(q, k, v)
+    o2 = blk.attn_prefill(q, k, v)
+    assert torch.equal(o1, o2)

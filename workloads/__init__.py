@@ -29,7 +29,8 @@ import torch
 
 __all__ = [
     "BlockConfig", "AttnConfig", "BLOCK_CONFIGS", "ATTN_CONFIGS",
-    "block_inputs", "attn_inputs", "weight_shapes", "storage_dtype", "scaled",
+    "block_inputs", "attn_inputs", "weight_shapes", "storage_dtype", "scaled", "draw",
+    "sample_rows",
 ]
 
 
@@ -246,3 +247,13 @@ def sample_rows(n_tokens: int, n: int, seed: int = 7) -> np.ndarray:
         return np.arange(n_tokens)
     pick = rng.choice(np.arange(1, n_tokens - 1), size=n - 2, replace=False)
     return np.sort(np.concatenate([[0, n_tokens - 1], pick]))
+
+
+def draw(shape, dtype: str, seed: int, kind: str = "x", scale: float = 1.0) -> torch.Tensor:
+    """One seeded tensor in a storage dtype: kind "x" ~ N(0, scale^2), "w"/"b"
+    ~ N(0, 0.02^2), "g" ~ 1 + N(0, 0.02^2)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = _draw(rng, tuple(shape), kind)
+    if kind == "x" and scale != 1.0:
+        a = a * scale
+    return _to_storage(a, dtype)
