@@ -295,7 +295,7 @@ blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w) {
 }
 
 struct FwdLayout {
-    size_t n1, q, k, v, o, h, n2, a, tmp, total;
+    size_t n1, q, k, v, o, h, n2, a, h16, tmp, total;
 };
 
 FwdLayout forward_layout(const blk_block_desc* d) {
@@ -314,10 +314,11 @@ FwdLayout forward_layout(const blk_block_desc* d) {
     L.k = take(T * Kd);
     L.v = take(T * Kd);
     L.o = take(T * Hd);
-    L.h = take(T * D);
+    L.h = take(2 * T * D);    // fp32 mid-block residual stream
     L.n2 = take(T * D);
     L.a = take(T * static_cast<size_t>(d->intermediate));
-    L.tmp = take(T * D);
+    L.h16 = take(T * D);      // storage-dtype copy of h (post-norm MLP input)
+    L.tmp = take(2 * T * D);  // fp32 sublayer output (parallel residual, post-norm input)
     L.total = off;
     return L;
 }
@@ -399,10 +400,15 @@ blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, cons
     return BLK_OK;
 }
 
+enum : int { F32_OUT = 1, F32_RES1 = 2, F32_RES2 = 4 };
+
 blk_status run_linear(DType dt, int epi, const void* x, const void* w, const void* w2,
                       const void* bias, const void* r1, const void* r2, void* y, int64_t m,
-                      int64_t n, int64_t k, cudaStream_t s, DevState* ds) {
+                      int64_t n, int64_t k, cudaStream_t s, DevState* ds, int f32 = 0) {
     GemmArgs g{};
+    g.out_f32 = (f32 & F32_OUT) != 0;
+    g.res1_f32 = (f32 & F32_RES1) != 0;
+    g.res2_f32 = (f32 & F32_RES2) != 0;
     g.M = static_cast<int>(m);
     g.N = static_cast<int>(n);
     g.K = static_cast<int>(k);
@@ -482,8 +488,9 @@ blk_status blk_layernorm_bias(const void* x, const void* residual, const void* g
                               blk_dtype dt, blk_stream_t s) {
     blk_status st = validate_norm(x, residual, gamma, beta, y, rows, cols, eps, dt);
     if (st != BLK_OK) return st;
-    cudaError_t e = launch_norm(to_dt(dt), false, x, residual, gamma, beta, y, rows,
-                                static_cast<int>(cols), eps, reinterpret_cast<cudaStream_t>(s));
+    const NormIO io{x, false, residual, false, y, nullptr};
+    cudaError_t e = launch_norm(to_dt(dt), false, io, gamma, beta, rows, static_cast<int>(cols),
+                                eps, reinterpret_cast<cudaStream_t>(s));
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "layernorm launch");
 }
 
@@ -491,8 +498,9 @@ blk_status blk_rmsnorm(const void* x, const void* residual, const void* weight, 
                        int64_t rows, int64_t cols, float eps, blk_dtype dt, blk_stream_t s) {
     blk_status st = validate_norm(x, residual, weight, nullptr, y, rows, cols, eps, dt);
     if (st != BLK_OK) return st;
-    cudaError_t e = launch_norm(to_dt(dt), true, x, residual, weight, nullptr, y, rows,
-                                static_cast<int>(cols), eps, reinterpret_cast<cudaStream_t>(s));
+    const NormIO io{x, false, residual, false, y, nullptr};
+    cudaError_t e = launch_norm(to_dt(dt), true, io, weight, nullptr, rows, static_cast<int>(cols),
+                                eps, reinterpret_cast<cudaStream_t>(s));
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "rmsnorm launch");
 }
 
@@ -679,6 +687,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     void* n2 = ws + L.n2;
     void* ab = ws + L.a;
     void* tmp = ws + L.tmp;
+    void* h16 = ws + L.h16;
     const int64_t T = q.batch * q.seq, D = q.hidden, F = d->intermediate;
     const bool rms = d->norm_kind == BLK_NORM_RMS;
     const bool pre = d->norm_place == BLK_NORM_PRE;
@@ -695,8 +704,8 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     // 1. input norm (absent in the reordered post-norm block)
     const void* attn_in = x;
     if (pre) {
-        e = launch_norm(t, rms, x, nullptr, w->attn_norm_w, w->attn_norm_b, n1, T,
-                        static_cast<int>(D), d->eps, cs);
+        e = launch_norm(t, rms, NormIO{x, false, nullptr, false, n1, nullptr}, w->attn_norm_w,
+                        w->attn_norm_b, T, static_cast<int>(D), d->eps, cs);
         if (e != cudaSuccess) return cuda_fail(e, "input norm launch");
         BLK_STEP(BLK_STEP_INPUT_NORM);
         attn_in = n1;
@@ -712,38 +721,47 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     BLK_STEP(BLK_STEP_ATTENTION);
     const int64_t Hd = q.n_heads * q.head_dim;
     if (parallel) {
-        // 4p. attn_out = o W_o^T (+b_o); mlp on the same normed input; y = x + attn_out + mlp
-        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd, cs, ds);
+        // 4p. attn_out = o W_o^T (+b_o) kept in fp32; mlp on the same normed
+        // input; y = x + attn_out + mlp
+        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
+                        cs, ds, F32_OUT);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
         st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, attn_in, swiglu ? w->w_gate : w->w_up,
                         swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_UP);
-        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, x, tmp, y, T, D, F, cs, ds);
+        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, x, tmp, y, T, D, F, cs,
+                        ds, F32_RES2);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
         return log.end();
     }
     const void* mlp_in;
     if (pre) {
-        // 4. h = x + o W_o^T (+b_o);  5. n2 = norm(h)
-        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, x, nullptr, hb, T, D, Hd, cs, ds);
+        // 4. h = x + o W_o^T (+b_o), fp32;  5. n2 = norm(h)
+        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, x, nullptr, hb, T, D, Hd, cs, ds,
+                        F32_OUT);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
-        e = launch_norm(t, rms, hb, nullptr, w->mlp_norm_w, w->mlp_norm_b, n2, T, static_cast<int>(D), d->eps, cs);
+        e = launch_norm(t, rms, NormIO{hb, true, nullptr, false, n2, nullptr}, w->mlp_norm_w,
+                        w->mlp_norm_b, T, static_cast<int>(D), d->eps, cs);
         if (e != cudaSuccess) return cuda_fail(e, "mlp norm launch");
         BLK_STEP(BLK_STEP_MLP_NORM);
         mlp_in = n2;
     } else {
-        // 4. a = o W_o^T;  5. h = x + RMS(a) * w_post_attn
-        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd, cs, ds);
+        // 4. a = o W_o^T (fp32: the RMS norm rescales it to unit size, so its
+        // rounding would be magnified);  5. h = x + RMS(a) * w_post_attn
+        // (fp32, and a storage copy for the MLP)
+        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
+                        cs, ds, F32_OUT);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
-        e = launch_norm(t, true, tmp, x, w->post_attn_norm_w, nullptr, hb, T, static_cast<int>(D), d->eps, cs);
+        e = launch_norm(t, true, NormIO{tmp, true, x, false, h16, static_cast<float*>(hb)},
+                        w->post_attn_norm_w, nullptr, T, static_cast<int>(D), d->eps, cs);
         if (e != cudaSuccess) return cuda_fail(e, "post-attention norm launch");
         BLK_STEP(BLK_STEP_POST_ATTN_NORM);
-        mlp_in = hb;
+        mlp_in = h16;
     }
     // 6. MLP up (+activation)
     st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, mlp_in, swiglu ? w->w_gate : w->w_up,
@@ -752,16 +770,19 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     BLK_STEP(BLK_STEP_MLP_UP);
     if (pre) {
         // 7. y = h + a W_d^T (+b_d)
-        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, hb, nullptr, y, T, D, F, cs, ds);
+        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, hb, nullptr, y, T, D, F, cs,
+                        ds, F32_RES1);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
         return log.end();
     }
     // 7. m = a W_d^T;  8. y = h + RMS(m) * w_post_mlp
-    st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, nullptr, nullptr, tmp, T, D, F, cs, ds);
+    st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, nullptr, nullptr, tmp, T, D, F,
+                    cs, ds, F32_OUT);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_DOWN);
-    e = launch_norm(t, true, tmp, hb, w->post_mlp_norm_w, nullptr, y, T, static_cast<int>(D), d->eps, cs);
+    e = launch_norm(t, true, NormIO{tmp, true, hb, true, y, nullptr}, w->post_mlp_norm_w, nullptr,
+                    T, static_cast<int>(D), d->eps, cs);
     if (e != cudaSuccess) return cuda_fail(e, "post-mlp norm launch");
     BLK_STEP(BLK_STEP_POST_MLP_NORM);
     return log.end();

@@ -3,7 +3,9 @@
 // One CTA per (128-query tile, head, batch), heaviest (latest) query tiles
 // scheduled first. 6 warps:
 //   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into a
-//               STAGES-deep ring (128-byte swizzle, 64-column boxes)
+//               STAGES-deep ring (128-byte swizzle, 64-column boxes). A K
+//               slot is refilled once its QK^T has completed and a V slot once
+//               its PV has, so S_{j+1} never waits on PV_j (even with one stage).
 //   warp 1      TMEM allocator and single-thread MMA issuer:
 //                 S = Q K^T   (M=128, N=128, K=d; A and B K-major)  -> TMEM cols [0,128)
 //                 O += P V    (M=128, N=d,   K=128; P K-major from smem,
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t sP = sKV + 2 * kStages * Cfg::kTileBytes;
     uint8_t* pP = smem + (sP - sQ);
     uint64_t* bars = reinterpret_cast<uint64_t*>(pP + Cfg::kPBytes);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 3 * kStages);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 4 * kStages);
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t q_full = bar0;
     const uint32_t s_full = bar0 + 8;
@@ -64,7 +66,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t o_done = bar0 + 32;
     auto k_full = [&](int i) { return bar0 + 64u + 8u * i; };
     auto v_full = [&](int i) { return bar0 + 64u + 8u * (kStages + i); };
-    auto kv_empty = [&](int i) { return bar0 + 64u + 8u * (2 * kStages + i); };
+    auto k_empty = [&](int i) { return bar0 + 64u + 8u * (2 * kStages + i); };
+    auto v_empty = [&](int i) { return bar0 + 64u + 8u * (3 * kStages + i); };
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -88,7 +91,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int i = 0; i < kStages; ++i) {
             mbar_init(k_full(i), 1);
             mbar_init(v_full(i), 1);
-            mbar_init(kv_empty(i), 1);
+            mbar_init(k_empty(i), 1);
+            mbar_init(v_empty(i), 1);
         }
         fence_barrier_init();
         tma_prefetch_desc(&tmQ);
@@ -115,14 +119,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int j = 0; j < nkv; ++j) {
                 const int st = j % kStages;
                 const uint32_t ph = (j / kStages) & 1;
-                if (!mbar_wait(kv_empty(st), ph ^ 1u, a.err)) break;
                 const uint32_t sK = sKV + (2 * st) * Cfg::kTileBytes;
                 const uint32_t sV = sK + Cfg::kTileBytes;
+                if (!mbar_wait(k_empty(st), ph ^ 1u, a.err)) break;
                 mbar_expect_tx(k_full(st), Cfg::kTileBytes);
 #pragma unroll
                 for (int sub = 0; sub < Cfg::kSub; ++sub)
                     tma_load_3d(sK + sub * kBKV * 128, &tmK, k_full(st), sub * 64, j * kBKV,
                                 b * a.Hk + g);
+                if (!mbar_wait(v_empty(st), ph ^ 1u, a.err)) break;
                 mbar_expect_tx(v_full(st), Cfg::kTileBytes);
 #pragma unroll
                 for (int sub = 0; sub < Cfg::kSub; ++sub)
@@ -148,6 +153,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                               make_sdesc_sw128(sK + off, 16, 1024), idesc_s, ks > 0 ? 1u : 0u);
                 }
                 tc_commit(s_full);
+                tc_commit(k_empty(st));
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                               (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 tc_commit(o_done);
-                tc_commit(kv_empty(st));
+                tc_commit(v_empty(st));
             }
         }
     } else {

@@ -78,6 +78,17 @@ __device__ __forceinline__ void store8(T* p, const float (&f)[8]) {
     *reinterpret_cast<uint4*>(p) = u;
 }
 
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
 // ------------------------------------------------------------ rotary -----
 // Rotary angles p * theta_j reduced to about [-pi, pi] in fp32 with ~1e-6 rad
 // absolute error up to p = 2^20. theta_j = theta_hi + theta_lo (split on the

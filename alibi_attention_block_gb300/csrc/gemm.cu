@@ -11,7 +11,9 @@
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per load (one
 //               thread per output row), fused op, 16-byte global stores
 // Epilogues (the block's steps after each projection):
-//   EPI_LINEAR  + bias, + up to two residuals (o_proj and down_proj residual adds)
+//   EPI_LINEAR  + bias, + up to two residuals (o_proj and down_proj residual
+//               adds); residuals and output may be fp32 (the block keeps its
+//               mid-block residual stream in fp32)
 //   EPI_SWIGLU  B tile = [gate rows | up rows]; out = silu(gate) * up
 //               (nnterp "stablelm" 02 support(): mlp_neurons = act(gate)*up)
 //   EPI_GELU    gelu_tanh(acc + bias) (Bloom's MLP)
@@ -154,9 +156,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
             }
             const int64_t off = static_cast<int64_t>(m) * g.N + n0;
-            if (g.res1) add_row32(static_cast<const T*>(g.res1) + off, o, valid);
-            if (g.res2) add_row32(static_cast<const T*>(g.res2) + off, o, valid);
-            store_row32(static_cast<T*>(g.out) + off, o, valid);
+            if (g.res1) {
+                if (g.res1_f32) add_row32(static_cast<const float*>(g.res1) + off, o, valid);
+                else add_row32(static_cast<const T*>(g.res1) + off, o, valid);
+            }
+            if (g.res2) {
+                if (g.res2_f32) add_row32(static_cast<const float*>(g.res2) + off, o, valid);
+                else add_row32(static_cast<const T*>(g.res2) + off, o, valid);
+            }
+            if (g.out_f32) store_row32(static_cast<float*>(g.out) + off, o, valid);
+            else store_row32(static_cast<T*>(g.out) + off, o, valid);
         }
     }
 }

@@ -13,9 +13,19 @@ namespace blk {
 enum class DType { F16 = 0, BF16 = 1 };
 
 // ---- K1: row norms (norm.cu)
-cudaError_t launch_norm(DType dt, bool rms, const void* x, const void* res, const void* gamma,
-                        const void* beta, void* y, int64_t rows, int cols, float eps,
-                        cudaStream_t s);
+// x, res and y are in the storage dtype unless the matching *_f32 flag is set
+// (fp32 row-major); y32 (nullable) receives an fp32 copy of y. Supported
+// combinations: any of x and res in fp32.
+struct NormIO {
+    const void* x;
+    bool x_f32;
+    const void* res;
+    bool res_f32;
+    void* y;
+    float* y32;
+};
+cudaError_t launch_norm(DType dt, bool rms, const NormIO& io, const void* gamma, const void* beta,
+                        int64_t rows, int cols, float eps, cudaStream_t s);
 
 // ---- K4/K5: qk-norm + rotary on head-split q/k, in place (rope.cu)
 enum QkNormMode { QKN_NONE = 0, QKN_RMS_FULL = 1, QKN_LN_PER_HEAD = 2 };
@@ -41,6 +51,9 @@ struct GemmArgs {
     const void* bias;     // [N] or nullptr
     const void* res1;     // [M, N] or nullptr
     const void* res2;
+    int out_f32;          // LINEAR: out is fp32
+    int res1_f32;         // LINEAR: res1 / res2 are fp32
+    int res2_f32;
     // EPI_QKV: scatter of [M, (H+2Hk)d] into head-split q/k/v
     void* q;
     void* k;

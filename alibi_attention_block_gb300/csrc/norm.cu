@@ -1,7 +1,9 @@
 // K1: row norms. LayerNorm with bias ("StableLM-2: partial RoPE and a first
 // LayerNorm-with-bias path", section 1) and RMSNorm ("OLMo-2: reordered (post)
 // normalization", section 1), with an optional residual added after the norm
-// (the OLMo-2 post-norm add).
+// (the OLMo-2 post-norm add). Inside the block the input or the residual may
+// be the fp32 mid-block residual stream, and an fp32 copy of the output can be
+// written alongside the storage-dtype one.
 //
 // HBM-bound: each row is read once into registers with 16-byte loads (a group
 // of TPR threads per row, VPT 8-element vectors per thread), reduced with warp
@@ -33,12 +35,15 @@ __device__ __forceinline__ float row_sum(float v, float* red) {
     return v;
 }
 
-template <typename T, int TPR, int VPT, bool RMS>
-__global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict__ x,
-                                                            const T* __restrict__ res,
+// T: gains/shifts; TX: input rows; TR: residual rows; y is T, y32 an
+// optional fp32 copy of y.
+template <typename T, typename TX, typename TR, int TPR, int VPT, bool RMS>
+__global__ void __launch_bounds__(kNormThreads) norm_kernel(const TX* x,
+                                                            const TR* __restrict__ res,
                                                             const T* __restrict__ gamma,
                                                             const T* __restrict__ beta,
-                                                            T* __restrict__ y, int64_t rows,
+                                                            T* y,
+                                                            float* __restrict__ y32, int64_t rows,
                                                             int cols, float eps) {
     __shared__ float red[kNormThreads / 32];
     constexpr int kRowsPerBlock = kNormThreads / TPR;
@@ -46,7 +51,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict_
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + threadIdx.x / TPR;
     const bool active = row < rows;
     const int nvec = cols / 8;
-    const T* xr = x + (active ? row : 0) * cols;
+    const TX* xr = x + (active ? row : 0) * cols;
 
     float v[VPT][8];
     float sum = 0.f;
@@ -79,7 +84,8 @@ __global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict_
     const float rstd = rsqrtf(row_sum<TPR>(sq, red) / static_cast<float>(cols) + eps);
     if (!active) return;
     T* yr = y + row * cols;
-    const T* rr = res ? res + row * cols : nullptr;
+    float* y32r = y32 ? y32 + row * cols : nullptr;
+    const TR* rr = res ? res + row * cols : nullptr;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int vi = sub + i * TPR;
@@ -101,35 +107,36 @@ __global__ void __launch_bounds__(kNormThreads) norm_kernel(const T* __restrict_
             for (int e = 0; e < 8; ++e) o[e] += r[e];
         }
         store8(yr + vi * 8, o);
+        if (y32r) store8(y32r + vi * 8, o);
     }
 }
 
-template <typename T, int TPR, int VPT>
-cudaError_t launch_tv(bool rms, const void* x, const void* res, const void* g, const void* b,
-                      void* y, int64_t rows, int cols, float eps, cudaStream_t s) {
+template <typename T, typename TX, typename TR, int TPR, int VPT>
+cudaError_t launch_tv(bool rms, const NormIO& io, const void* g, const void* b, int64_t rows,
+                      int cols, float eps, cudaStream_t s) {
     constexpr int kRowsPerBlock = kNormThreads / TPR;
     const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-    auto args = [&](auto kern) {
+    auto go = [&](auto kern) {
         kern<<<static_cast<unsigned>(blocks), kNormThreads, 0, s>>>(
-            static_cast<const T*>(x), static_cast<const T*>(res), static_cast<const T*>(g),
-            static_cast<const T*>(b), static_cast<T*>(y), rows, cols, eps);
+            static_cast<const TX*>(io.x), static_cast<const TR*>(io.res), static_cast<const T*>(g),
+            static_cast<const T*>(b), static_cast<T*>(io.y), io.y32, rows, cols, eps);
     };
     if (rms)
-        args(norm_kernel<T, TPR, VPT, true>);
+        go(norm_kernel<T, TX, TR, TPR, VPT, true>);
     else
-        args(norm_kernel<T, TPR, VPT, false>);
+        go(norm_kernel<T, TX, TR, TPR, VPT, false>);
     return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_t(bool rms, const void* x, const void* res, const void* g, const void* b,
-                     void* y, int64_t rows, int cols, float eps, cudaStream_t s) {
+template <typename T, typename TX, typename TR>
+cudaError_t launch_t(bool rms, const NormIO& io, const void* g, const void* b, int64_t rows,
+                     int cols, float eps, cudaStream_t s) {
     const int nvec = cols / 8;
     // One warp per row while a lane holds at most 8 vectors (cols <= 2048);
     // wider rows spread over 2..8 warps.
 #define BLK_NORM_CASE(TPR, VPT) \
-    if (nvec <= (TPR) * (VPT)) return launch_tv<T, TPR, VPT>(rms, x, res, g, b, y, rows, cols, eps, s)
+    if (nvec <= (TPR) * (VPT)) return launch_tv<T, TX, TR, TPR, VPT>(rms, io, g, b, rows, cols, eps, s)
     BLK_NORM_CASE(32, 1);
     BLK_NORM_CASE(32, 2);
     BLK_NORM_CASE(32, 4);
@@ -141,15 +148,22 @@ cudaError_t launch_t(bool rms, const void* x, const void* res, const void* g, co
     return cudaErrorInvalidValue;
 }
 
+template <typename T>
+cudaError_t launch_io(bool rms, const NormIO& io, const void* g, const void* b, int64_t rows,
+                      int cols, float eps, cudaStream_t s) {
+    if (io.x_f32 && io.res_f32) return launch_t<T, float, float>(rms, io, g, b, rows, cols, eps, s);
+    if (io.x_f32) return launch_t<T, float, T>(rms, io, g, b, rows, cols, eps, s);
+    if (io.res_f32) return launch_t<T, T, float>(rms, io, g, b, rows, cols, eps, s);
+    return launch_t<T, T, T>(rms, io, g, b, rows, cols, eps, s);
+}
+
 }  // namespace
 
-cudaError_t launch_norm(DType dt, bool rms, const void* x, const void* res, const void* gamma,
-                        const void* beta, void* y, int64_t rows, int cols, float eps,
-                        cudaStream_t s) {
+cudaError_t launch_norm(DType dt, bool rms, const NormIO& io, const void* gamma, const void* beta,
+                        int64_t rows, int cols, float eps, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    if (dt == DType::F16)
-        return launch_t<__half>(rms, x, res, gamma, beta, y, rows, cols, eps, s);
-    return launch_t<__nv_bfloat16>(rms, x, res, gamma, beta, y, rows, cols, eps, s);
+    if (dt == DType::F16) return launch_io<__half>(rms, io, gamma, beta, rows, cols, eps, s);
+    return launch_io<__nv_bfloat16>(rms, io, gamma, beta, rows, cols, eps, s);
 }
 
 }  // namespace blk

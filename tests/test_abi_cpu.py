@@ -146,9 +146,9 @@ def test_forward_workspace_check(lib):
     assert _fwd(lib, _block(), _weights(), ws_bytes=16) == _abi.BLK_EWORKSPACE
     need = C.c_size_t(0)
     assert lib.blk_forward_workspace_size(C.byref(_block()), C.byref(need)) == _abi.BLK_OK
-    # n1, q, k, v, o, h, n2, a, tmp for T = 128 tokens, all 256-byte aligned
+    # n1, q, k, v, o, h (fp32), n2, a, h16, tmp (fp32) for T = 128 tokens
     T, D, F = 128, 256, 688
-    assert need.value == 2 * T * (D * 4 + 256 * 4 + F)
+    assert need.value == 2 * T * (7 * D + 4 * 256 + F)
 
 
 def test_mlp_validation(lib):
