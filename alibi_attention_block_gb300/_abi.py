@@ -72,6 +72,8 @@ _PROTOS = {
     "blk_mlp_workspace_size": (C.c_int, [C.POINTER(MlpDesc), C.POINTER(C.c_size_t)]),
     "blk_mlp": (C.c_int, [C.POINTER(MlpDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_size_t,
                           C.c_int, vp]),
+    "blk_mlp_noalloc": (C.c_int, [C.POINTER(MlpDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_int,
+                                  vp]),
     "blk_forward_workspace_size": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(C.c_size_t)]),
     "blk_forward": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp,
                               C.c_size_t, C.c_int, vp]),

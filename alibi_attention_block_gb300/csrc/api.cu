@@ -118,6 +118,25 @@ constexpr int64_t kI32 = 0x7fffffff;
 
 }  // namespace
 
+blk_status current_device_info(int* sms, unsigned** err) {
+    DevState* ds = nullptr;
+    const blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
+    *sms = ds->sms;
+    *err = ds->err;
+    return BLK_OK;
+}
+
+blk_status report_error_status(blk_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
 bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uint64_t cols,
                   uint32_t box_rows) {
     auto fn = encode_fn();

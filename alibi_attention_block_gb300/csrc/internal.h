@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/blk.h"
 #include "common.cuh"
 
 namespace blk {
@@ -78,6 +79,12 @@ struct AttnArgs {
     unsigned* err;
 };
 cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s);
+
+// ---- per-device state and error reporting shared with other entry points (api.cu)
+// SM count and device error word of the current device (set up on first use).
+blk_status current_device_info(int* sms, unsigned** err);
+// Record a printf-style message for blk_last_error() and return `st`.
+blk_status report_error_status(blk_status st, const char* fmt, ...);
 
 // ---- tensor maps (api.cu)
 // 2D row-major [rows, cols] map with a {64, box_rows} box and 128B swizzle.

@@ -175,6 +175,32 @@ blk_status blk_mlp(const blk_mlp_desc* d, const void* x, const void* w_gate, con
                    const void* res2, void* y, void* workspace, size_t ws_bytes, blk_dtype dt,
                    blk_stream_t s);
 
+/* Size of the device scratch array blk_mlp_noalloc keeps for its activation. */
+#define BLK_MLP_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* blk_mlp without a workspace argument, for callers that cannot allocate
+ * device memory: code running inside an engine or plugin host that owns all
+ * device memory and forbids allocation once it has started, and latency-bound
+ * callers that cannot take cudaMalloc's implicit device synchronisation.
+ * The pages have no counterpart of this call; it only changes where the
+ * [tokens, intermediate] activation lives.
+ *
+ * That activation goes to one fixed array of BLK_MLP_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) in the library's device memory, which every GPU that loads the
+ * library keeps until the process exits. tokens * intermediate * 2 bytes must
+ * fit in it; larger requests return BLK_EWORKSPACE and launch nothing. The
+ * call allocates and frees nothing. Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress), so make that first call
+ * before any stream capture. All calls share the one array: calls whose
+ * kernels overlap on the GPU (other streams, other host threads) race on it.
+ * Every element the MLP reads from it is written first in the same call, so
+ * nothing has to be cleared between calls. Arguments, results and errors are
+ * otherwise those of blk_mlp. */
+blk_status blk_mlp_noalloc(const blk_mlp_desc* d, const void* x, const void* w_gate,
+                           const void* w_up, const void* b_up, const void* w_down,
+                           const void* b_down, const void* res1, const void* res2, void* y,
+                           blk_dtype dt, blk_stream_t s);
+
 /* ---- the block -------------------------------------------------------- */
 
 typedef struct {
