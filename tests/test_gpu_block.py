@@ -11,7 +11,8 @@ import torch
 import alibi_attention_block_gb300 as blk
 import oracle
 import workloads
-from tests.parity import check, f64, to_dev
+from tests.parity import ABS_TOL, check, f64, to_dev
+from tests.test_storage_budget import POST_NORM_ABS_TOL
 from workloads import BLOCK_CONFIGS, scaled
 
 pytestmark = pytest.mark.gpu
@@ -27,6 +28,12 @@ SMALL = {
     "stablelm2_12b_small": scaled(BLOCK_CONFIGS["stablelm2_12b"], batch=1, seq=260, hidden=320,
                                   n_heads=8, n_kv_heads=2, intermediate=512),
 }
+
+
+def _abs_tol(cfg):
+    """2e-2 on unit-scale outputs; the post-norm block's bf16-storage floor is
+    above that (tests/test_storage_budget.py), so it is gated at 5e-2."""
+    return POST_NORM_ABS_TOL if cfg.norm_place == "post" else ABS_TOL
 
 
 def _gpu_forward(cfg, x, w):
@@ -48,7 +55,7 @@ def test_block_small(name):
     x, w = workloads.block_inputs(cfg)
     y = _gpu_forward(cfg, x, w)
     ref = oracle.block_forward(cfg, x, w)["y"]
-    check(y, ref, name, unit_scale=True)
+    check(y, ref, name, unit_scale=True, abs_tol=_abs_tol(cfg))
 
 
 def test_block_deterministic():
@@ -89,5 +96,5 @@ def test_block_full_size_sampled_rows(name):
     rows = workloads.sample_rows(cfg.tokens, 48, seed=cfg.seed)
     ref = oracle.block_forward(cfg, x, w, rows=rows)["y"]
     got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
-    check(got, ref, f"{name} sampled rows", unit_scale=True)
+    check(got, ref, f"{name} sampled rows", unit_scale=True, abs_tol=_abs_tol(cfg))
     assert torch.isfinite(y).all()
