@@ -379,7 +379,11 @@ struct StepLog {
 blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, const void* b_qkv,
                    const void* q_norm_w, const void* k_norm_w, void* q, void* k, void* v,
                    DType dt, cudaStream_t s, DevState* ds, StepLog* log = nullptr) {
-    const bool fuse_rope = d->qk_norm == BLK_QKNORM_NONE && d->rotary_span <= 32;
+    // the GEMM epilogue rotates spans of 16 or 32 dims in registers; other
+    // spans, and any qk-norm (which must precede the rotary), run in the
+    // qk-norm/rotary kernel after the projection
+    const bool fuse_rope = d->qk_norm == BLK_QKNORM_NONE &&
+                           (d->rotary_span == 0 || d->rotary_span == 16 || d->rotary_span == 32);
     RopeParams rp = make_rope(fuse_rope ? d->rotary_span : 0, d->rope_base);
     GemmArgs g{};
     g.M = static_cast<int>(d->batch * d->seq);

@@ -1,24 +1,30 @@
 // K3: causal softmax attention, flash-style, on tcgen05 tensor cores.
 //
 // One CTA per (128-query tile, head, batch), heaviest (latest) query tiles
-// scheduled first. 6 warps:
+// scheduled first; at head_dim 64 two CTAs share an SM, so one CTA's MMAs
+// run while the other's softmax warps compute. 6 warps:
 //   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into a
 //               STAGES-deep ring (128-byte swizzle, 64-column boxes). A K
 //               slot is refilled once its QK^T has completed and a V slot once
 //               its PV has, so S_{j+1} never waits on PV_j (even with one stage).
 //   warp 1      TMEM allocator and single-thread MMA issuer:
-//                 S = Q K^T   (M=128, N=128, K=d; A and B K-major)  -> TMEM cols [0,128)
-//                 O += P V    (M=128, N=d,   K=128; P K-major from smem,
-//                              V MN-major from smem)                  -> TMEM cols [128,128+d)
+//                 S  = Q K^T  (M=128, N=128, K=d; Q and K K-major in smem)  -> TMEM S
+//                 O += P V    (M=128, N=d, K=128; P read from TMEM,
+//                              V MN-major in smem)                          -> TMEM O
 //               S_{j+1} is issued as soon as the softmax warps have read S_j,
 //               so the next QK^T overlaps the exponentials of this tile.
-//   warps 2..5  softmax, one thread per query row: tcgen05.ld of the row of
-//               S, scale (and the ALiBi bias -slope*(i-j), "Bloom in a sovereign
-//               engine", Contribution), causal mask on the diagonal tile,
-//               online max/sum in the exp2 domain, P rounded to the storage
-//               type into 128-byte-swizzled smem; O is rescaled in TMEM only
-//               when the running max grows by more than 2^8, so most tiles
-//               skip the rescale. Finally O / l is written as [B, S, H, d].
+//   warps 2..5  softmax, one thread per query row: one tcgen05.ld of the
+//               row's 128 scores, the causal mask on the diagonal (and ragged
+//               last) tile only, the row max on the raw scores, one FFMA per
+//               score into ex2 (scale log2(e)/sqrt(d) folded in; for ALiBi the
+//               bias -slope*(i-j), "Bloom in a sovereign engine",
+//               Contribution, enters as +slope*j, the -slope*i part being
+//               constant along the row), P rounded to the storage type and
+//               written to TMEM as the A operand of PV. O is rescaled in TMEM
+//               only when the running max grows by more than 2^8. Finally
+//               O / l is written as [B, S, H, d].
+// TMEM columns: S [0, 128), P [128, 192) (two 16-bit values per column),
+// O [192, 192 + d).
 // Query scale head_dim^-0.5 and GQA (kv head = h / (H/Hk)) follow nnterp
 // "stablelm" 03 Notes.
 #include "internal.h"
@@ -32,20 +38,21 @@ constexpr int kBQ = 128;
 constexpr int kBKV = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest unnormalised p
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 
 template <int D>
 struct AttnCfg {
     static constexpr int kSub = (D + 63) / 64;          // 64-column boxes per row
     static constexpr int kTileBytes = kSub * kBQ * 128;  // 128 rows x kSub x 128 B
     static constexpr int kStages = D > 128 ? 1 : 2;
-    static constexpr int kPBytes = 2 * kBQ * 128;        // 128 x 128 keys, 2 boxes
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmem = kTileBytes * (1 + 2 * kStages) + kPBytes + 1024 + kBarBytes;
-    static constexpr uint32_t kTmemCols = (kBKV + D) <= 256 ? 256 : 512;
+    static constexpr int kSmem = kTileBytes * (1 + 2 * kStages) + 1024 + kBarBytes;
+    static constexpr uint32_t kTmemCols = (kColO + D) <= 256 ? 256 : 512;
+    static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
 };
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+template <typename T, int D, bool ALIBI>
+__global__ void __launch_bounds__(kAttnThreads, AttnCfg<D>::kMinBlocks)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
     using Cfg = AttnCfg<D>;
@@ -54,9 +61,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* smem = align_1024(smem_raw);
     const uint32_t sQ = smem_u32(smem);
     const uint32_t sKV = sQ + Cfg::kTileBytes;  // stage i: K at +2i, V at +2i+1 tiles
-    const uint32_t sP = sKV + 2 * kStages * Cfg::kTileBytes;
-    uint8_t* pP = smem + (sP - sQ);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(pP + Cfg::kPBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (1 + 2 * kStages) * Cfg::kTileBytes);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 4 * kStages);
     const uint32_t bar0 = smem_u32(bars);
     const uint32_t q_full = bar0;
@@ -107,8 +112,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tS = tmem_base;
-    const uint32_t tO = tmem_base + kBKV;
+    const uint32_t tS = tmem_base + kColS;
+    const uint32_t tP = tmem_base + kColP;
+    const uint32_t tO = tmem_base + kColO;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -170,11 +176,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t sV = sKV + (2 * st + 1) * Cfg::kTileBytes;
 #pragma unroll
                 for (int ks = 0; ks < kBKV / 16; ++ks) {
-                    const uint32_t pa = sP + (ks / 4) * (kBQ * 128) + (ks % 4) * 32;
-                    const uint32_t vb = sV + ks * 16 * 128;
-                    tc_mma_ss(tO, make_sdesc_sw128(pa, 16, 1024),
-                              make_sdesc_sw128(vb, kBKV * 128, 1024), idesc_o,
-                              (j > 0 || ks > 0) ? 1u : 0u);
+                    tc_mma_ts(tO, tP + ks * 8, make_sdesc_sw128(sV + ks * 16 * 128, kBKV * 128, 1024),
+                              idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 tc_commit(o_done);
                 tc_commit(v_empty(st));
@@ -188,13 +191,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const float scale_l2 = a.scale * kLog2e;
         float slope_l2 = 0.f;
-        if (a.alibi) {
+        if constexpr (ALIBI) {
             const float slope = a.slopes ? a.slopes[h]
                                          : exp2f(-8.0f * static_cast<float>(h + 1) /
                                                  static_cast<float>(a.H));
             slope_l2 = slope * kLog2e;
         }
-        float m_used = -INFINITY;
+        float m_used = -INFINITY;  // running max, log2 domain (scores * scale * log2 e)
         float l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
@@ -203,42 +206,61 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             }
             tc_fence_after();
-            float s[kBKV];
-#pragma unroll
-            for (int c = 0; c < kBKV / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tS + lane_off + c * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-            }
+            uint32_t r[kBKV];
+            tmem_ld128(tS + lane_off, r);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
 
             const int kbase = j * kBKV;
-            const bool need_mask = (j == qt) || (kbase + kBKV > a.S);
-            const float bias0 = slope_l2 * static_cast<float>(kbase - qpos);
-            float mx = -INFINITY;
+            if constexpr (ALIBI) {
+                // t_j = s_j * scale + slope * key_pos (the -slope * query_pos part
+                // is constant along the row and cancels in the softmax)
+                const float sk = slope_l2 * static_cast<float>(kbase);
 #pragma unroll
-            for (int i = 0; i < kBKV; ++i) {
-                float x = fmaf(s[i], scale_l2, fmaf(slope_l2, static_cast<float>(i), bias0));
-                if (need_mask && (kbase + i > qpos || kbase + i >= a.S)) x = -INFINITY;
-                s[i] = x;
-                mx = fmaxf(mx, x);
+                for (int i = 0; i < kBKV; ++i)
+                    r[i] = __float_as_uint(fmaf(__uint_as_float(r[i]), scale_l2,
+                                                fmaf(slope_l2, static_cast<float>(i), sk)));
             }
+            if (j == qt || kbase + kBKV > a.S) {
+                const int lim = min(qpos, a.S - 1) - kbase;  // keys <= lim are visible
+#pragma unroll
+                for (int i = 0; i < kBKV; ++i)
+                    if (i > lim) r[i] = __float_as_uint(-INFINITY);
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kBKV; i += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(r[i]));
+                mx1 = fmaxf(mx1, __uint_as_float(r[i + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(r[i + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(r[i + 3]));
+            }
+            float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            if constexpr (!ALIBI) mx *= scale_l2;  // scale > 0: max commutes with it
             float corr = 1.f;
-            const float m_new = fmaxf(m_used, mx);
-            if (m_new > m_used + kRescaleThreshold) {
-                corr = ex2_approx(m_used - m_new);
-                m_used = m_new;
+            if (mx > m_used + kRescaleThreshold) {
+                corr = ex2_approx(m_used - mx);
+                m_used = mx;
             }
-            float sum = 0.f;
+            const float neg = -m_used;
+            uint32_t pk[kBKV / 2];
+            float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < kBKV; ++i) {
-                s[i] = ex2_approx(s[i] - m_used);
-                sum += s[i];
+            for (int i = 0; i < kBKV; i += 2) {
+                float p0, p1;
+                if constexpr (ALIBI) {
+                    p0 = ex2_approx(__uint_as_float(r[i]) + neg);
+                    p1 = ex2_approx(__uint_as_float(r[i + 1]) + neg);
+                } else {
+                    p0 = ex2_approx(fmaf(__uint_as_float(r[i]), scale_l2, neg));
+                    p1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), scale_l2, neg));
+                }
+                sum0 += p0;
+                sum1 += p1;
+                pk[i / 2] = dt_traits<T>::pack2(p0, p1);
             }
-            l = l * corr + sum;
+            l = l * corr + (sum0 + sum1);
 
             if (j > 0) {
                 if (!mbar_wait(o_done, (j - 1) & 1, a.err)) {
@@ -249,33 +271,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (__any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + lane_off + c * 32, r);
-                        uint32_t lo[16], hi[16];
+                        uint32_t o[32];
+                        tmem_ld32(tO + lane_off + c * 32, o);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            lo[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-                            hi[i] = __float_as_uint(__uint_as_float(r[16 + i]) * corr);
-                        }
-                        tmem_st16(tO + lane_off + c * 32, lo);
-                        tmem_st16(tO + lane_off + c * 32 + 16, hi);
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        tmem_st32_nowait(tO + lane_off + c * 32, o);
                     }
                 }
             }
-            // P row -> smem, K-major, 128-byte swizzle (16-byte chunk c of a
-            // 128-byte row r lives at chunk c ^ (r & 7))
-#pragma unroll
-            for (int ch = 0; ch < kBKV / 8; ++ch) {
-                uint4 u;
-                u.x = dt_traits<T>::pack2(s[ch * 8 + 0], s[ch * 8 + 1]);
-                u.y = dt_traits<T>::pack2(s[ch * 8 + 2], s[ch * 8 + 3]);
-                u.z = dt_traits<T>::pack2(s[ch * 8 + 4], s[ch * 8 + 5]);
-                u.w = dt_traits<T>::pack2(s[ch * 8 + 6], s[ch * 8 + 7]);
-                const int sub = ch / 8, c16 = ch % 8;
-                uint8_t* dst = pP + sub * (kBQ * 128) + row * 128 + ((c16 ^ (row & 7)) * 16);
-                *reinterpret_cast<uint4*>(dst) = u;
-            }
-            fence_proxy_async_smem();
+            uint32_t (&pk0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
+            uint32_t (&pk1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
+            tmem_st32_nowait(tP + lane_off, pk0);
+            tmem_st32_nowait(tP + lane_off + 32, pk1);
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
@@ -308,7 +317,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool ALIBI>
 cudaError_t launch_d(DType dt, const AttnArgs& a, cudaStream_t s) {
     using Cfg = AttnCfg<D>;
     CUtensorMap tq, tk, tv;
@@ -316,7 +325,7 @@ cudaError_t launch_d(DType dt, const AttnArgs& a, cudaStream_t s) {
         !make_tmap_3d(&tk, dt, a.k, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kBKV) ||
         !make_tmap_3d(&tv, dt, a.v, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kBKV))
         return cudaErrorInvalidValue;
-    auto kern = attn_kernel<T, D>;
+    auto kern = attn_kernel<T, D, ALIBI>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e =
@@ -330,12 +339,17 @@ cudaError_t launch_d(DType dt, const AttnArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename T, int D>
+cudaError_t launch_a(DType dt, const AttnArgs& a, cudaStream_t s) {
+    return a.alibi ? launch_d<T, D, true>(dt, a, s) : launch_d<T, D, false>(dt, a, s);
+}
+
 template <typename T>
 cudaError_t launch_t(DType dt, const AttnArgs& a, cudaStream_t s) {
     switch (a.d) {
-        case 64: return launch_d<T, 64>(dt, a, s);
-        case 128: return launch_d<T, 128>(dt, a, s);
-        case 160: return launch_d<T, 160>(dt, a, s);
+        case 64: return launch_a<T, 64>(dt, a, s);
+        case 128: return launch_a<T, 128>(dt, a, s);
+        case 160: return launch_a<T, 160>(dt, a, s);
         default: return cudaErrorInvalidValue;
     }
 }

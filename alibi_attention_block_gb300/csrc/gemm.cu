@@ -17,7 +17,7 @@
 //   EPI_SWIGLU  B tile = [gate rows | up rows]; out = silu(gate) * up
 //               (nnterp "stablelm" 02 support(): mlp_neurons = act(gate)*up)
 //   EPI_GELU    gelu_tanh(acc + bias) (Bloom's MLP)
-//   EPI_QKV     + bias, optional partial NeoX rotary on q/k heads (span <= 32),
+//   EPI_QKV     + bias, optional partial NeoX rotary on q/k heads (span 16 or 32),
 //               scatter of the [M, (H+2Hk)d] projection into head-split q, k, v
 //               for stacked or per-head interleaved ([head][q,k,v][d]) rows
 //               ("Bloom in a sovereign engine", Contribution: de-interleave).
@@ -75,7 +75,7 @@ __device__ __forceinline__ float gelu_tanh_f(float z) {
     return 0.5f * z * (1.0f + tanhf(k0 * (z + 0.044715f * z * z * z)));
 }
 
-template <typename T, int BN, int EPI>
+template <typename T, int BN, int EPI, int ROT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParams& rp,
                                               uint32_t tbase, int m, int nt) {
     const bool row_ok = m < g.M;
@@ -121,16 +121,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 head = (n0 - off) / d;
                 dd0 = n0 - off - head * d;
             }
-            if (which < 2 && rp.span > 0 && dd0 == 0) {
-                const int half = rp.span / 2;
+            if constexpr (ROT > 0) {
+                // the span is a compile-time constant so o[] stays in registers
+                if (which < 2 && dd0 == 0) {
+                    constexpr int kHalf = ROT / 2;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (j < half) {
+                    for (int j = 0; j < kHalf; ++j) {
                         float cs, sn;
                         rope_cos_sin(rp, s, j, cs, sn);
-                        const float x1 = o[j], x2 = o[j + half];
+                        const float x1 = o[j], x2 = o[j + kHalf];
                         o[j] = x1 * cs - x2 * sn;
-                        o[j + half] = x2 * cs + x1 * sn;
+                        o[j + kHalf] = x2 * cs + x1 * sn;
                     }
                 }
             }
@@ -170,7 +171,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
     }
 }
 
-template <typename T, int BN, int EPI>
+template <typename T, int BN, int EPI, int ROT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const GemmArgs g,
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int mt = t % m_tiles, nt = t / m_tiles;
             const uint32_t tbase =
                 tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            epilogue_tile<T, BN, EPI>(g, rp, tbase, mt * kBM + row, nt);
+            epilogue_tile<T, BN, EPI, ROT>(g, rp, tbase, mt * kBM + row, nt);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(acc));
@@ -310,12 +311,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <typename T, int BN, int EPI>
+template <typename T, int BN, int EPI, int ROT = 0>
 cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
                        const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
     using Cfg = GemmCfg<BN>;
     constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
-    auto kern = gemm_kernel<T, BN, EPI>;
+    auto kern = gemm_kernel<T, BN, EPI, ROT>;
     static bool attr_set = false;  // per template instance
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -344,7 +345,13 @@ cudaError_t launch_t(DType dt, int epi, const void* a, const void* b, const void
         case EPI_LINEAR: return launch_cfg<T, BN, EPI_LINEAR>(ta, tb, tb2, g, rp, num_sms, s);
         case EPI_SWIGLU: return launch_cfg<T, BN, EPI_SWIGLU>(ta, tb, tb2, g, rp, num_sms, s);
         case EPI_GELU: return launch_cfg<T, BN, EPI_GELU>(ta, tb, tb2, g, rp, num_sms, s);
-        case EPI_QKV: return launch_cfg<T, BN, EPI_QKV>(ta, tb, tb2, g, rp, num_sms, s);
+        case EPI_QKV:
+            switch (rp.span) {
+                case 0: return launch_cfg<T, BN, EPI_QKV, 0>(ta, tb, tb2, g, rp, num_sms, s);
+                case 16: return launch_cfg<T, BN, EPI_QKV, 16>(ta, tb, tb2, g, rp, num_sms, s);
+                case 32: return launch_cfg<T, BN, EPI_QKV, 32>(ta, tb, tb2, g, rp, num_sms, s);
+                default: return cudaErrorInvalidValue;
+            }
         default: return cudaErrorInvalidValue;
     }
 }
