@@ -14,13 +14,15 @@
 //               S_{j+1} is issued as soon as the softmax warps have read S_j,
 //               so the next QK^T overlaps the exponentials of this tile.
 //   warps 2..5  softmax, one thread per query row: one tcgen05.ld of the
-//               row's 128 scores, the causal mask on the diagonal (and ragged
-//               last) tile only, the row max on the raw scores, one FFMA per
-//               score into ex2 (scale log2(e)/sqrt(d) folded in; for ALiBi the
+//               row's 128 scores (S is released at once), the causal
+//               mask on the diagonal (and ragged last) tile only, the row max
+//               on the raw scores (3-input max), one paired (f32x2) FMA per two
+//               scores into ex2 (scale log2(e)/sqrt(d) folded in; for ALiBi the
 //               bias -slope*(i-j), "Bloom in a sovereign engine",
 //               Contribution, enters as +slope*j, the -slope*i part being
 //               constant along the row), P rounded to the storage type and
-//               written to TMEM as the A operand of PV. O is rescaled in TMEM
+//               written to TMEM (32 keys at a time) as the A operand of PV,
+//               after PV_{j-1} has finished reading the previous P. O is rescaled in TMEM
 //               only when the running max grows by more than 2^8. Finally
 //               O / l is written as [B, S, H, d].
 // TMEM columns: S [0, 128), P [128, 192) (two 16-bit values per column),
@@ -206,62 +208,52 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<D>::kMinBlocks)
                 break;
             }
             tc_fence_after();
+            const int kbase = j * kBKV;
+            const bool masked = j == qt || kbase + kBKV > a.S;
+            const int lim = min(qpos, a.S - 1) - kbase;  // keys <= lim are visible
+            const float sk = slope_l2 * static_cast<float>(kbase);
+            // scores in the log2 domain before the max subtraction: s*scale for
+            // plain attention (applied after the max, which commutes with a
+            // positive scale), s*scale + slope*key_pos for ALiBi (the
+            // -slope*query_pos part is constant along the row and cancels)
+            auto logit = [&](uint32_t raw, int i) -> float {
+                const float v = __uint_as_float(raw);
+                if constexpr (ALIBI)
+                    return fmaf(v, scale_l2, fmaf(slope_l2, static_cast<float>(i), sk));
+                else
+                    return v;
+            };
+            // the whole row of S in registers, so S can be overwritten by the
+            // next QK^T while this tile's exponentials run
             uint32_t r[kBKV];
             tmem_ld128(tS + lane_off, r);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free);
-
-            const int kbase = j * kBKV;
             if constexpr (ALIBI) {
-                // t_j = s_j * scale + slope * key_pos (the -slope * query_pos part
-                // is constant along the row and cancels in the softmax)
-                const float sk = slope_l2 * static_cast<float>(kbase);
 #pragma unroll
-                for (int i = 0; i < kBKV; ++i)
-                    r[i] = __float_as_uint(fmaf(__uint_as_float(r[i]), scale_l2,
-                                                fmaf(slope_l2, static_cast<float>(i), sk)));
+                for (int i = 0; i < kBKV; ++i) r[i] = __float_as_uint(logit(r[i], i));
             }
-            if (j == qt || kbase + kBKV > a.S) {
-                const int lim = min(qpos, a.S - 1) - kbase;  // keys <= lim are visible
+            if (masked) {
 #pragma unroll
                 for (int i = 0; i < kBKV; ++i)
                     if (i > lim) r[i] = __float_as_uint(-INFINITY);
             }
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+            float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
             for (int i = 0; i < kBKV; i += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(r[i]));
-                mx1 = fmaxf(mx1, __uint_as_float(r[i + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(r[i + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(r[i + 3]));
+                m0 = fmax3f(m0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                m1 = fmax3f(m1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
             }
-            float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            float mx = fmaxf(m0, m1);
             if constexpr (!ALIBI) mx *= scale_l2;  // scale > 0: max commutes with it
             float corr = 1.f;
             if (mx > m_used + kRescaleThreshold) {
                 corr = ex2_approx(m_used - mx);
                 m_used = mx;
             }
-            const float neg = -m_used;
-            uint32_t pk[kBKV / 2];
-            float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < kBKV; i += 2) {
-                float p0, p1;
-                if constexpr (ALIBI) {
-                    p0 = ex2_approx(__uint_as_float(r[i]) + neg);
-                    p1 = ex2_approx(__uint_as_float(r[i + 1]) + neg);
-                } else {
-                    p0 = ex2_approx(fmaf(__uint_as_float(r[i]), scale_l2, neg));
-                    p1 = ex2_approx(fmaf(__uint_as_float(r[i + 1]), scale_l2, neg));
-                }
-                sum0 += p0;
-                sum1 += p1;
-                pk[i / 2] = dt_traits<T>::pack2(p0, p1);
-            }
-            l = l * corr + (sum0 + sum1);
-
+            // PV_{j-1} must be done before O is rescaled and before P_j
+            // overwrites P_{j-1}, which it reads
             if (j > 0) {
                 if (!mbar_wait(o_done, (j - 1) & 1, a.err)) {
                     ok = false;
@@ -280,14 +272,31 @@ __global__ void __launch_bounds__(kAttnThreads, AttnCfg<D>::kMinBlocks)
                     }
                 }
             }
-            uint32_t (&pk0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[0]);
-            uint32_t (&pk1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&pk[32]);
-            tmem_st32_nowait(tP + lane_off, pk0);
-            tmem_st32_nowait(tP + lane_off + 32, pk1);
+            // p = 2^(logit - m), row sum, P (storage type) into TMEM 32 keys at a time
+            const uint64_t mul2 = f2_pack(ALIBI ? 1.f : scale_l2, ALIBI ? 1.f : scale_l2);
+            const uint64_t neg2 = f2_pack(-m_used, -m_used);
+            uint64_t acc2 = f2_pack(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < kBKV / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float e0, e1;
+                    ffma2(__uint_as_float(r[c * 32 + i]), __uint_as_float(r[c * 32 + i + 1]),
+                          mul2, neg2, e0, e1);
+                    const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+                    fadd2_acc(acc2, p0, p1);
+                    pk[i / 2] = dt_traits<T>::pack2(p0, p1);
+                }
+                tmem_st16_nowait(tP + lane_off + c * 16, pk);
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
+            float sum0, sum1;
+            f2_unpack(acc2, sum0, sum1);
+            l = l * corr + (sum0 + sum1);
         }
         if (ok && mbar_wait(o_done, (nkv - 1) & 1, a.err)) {
             tc_fence_after();
