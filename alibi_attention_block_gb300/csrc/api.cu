@@ -10,7 +10,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/blk.h"
+#include "blk.h"
 #include "internal.h"
 
 namespace blk {
@@ -463,6 +463,7 @@ blk_status run_attn(const blk_attn_desc* d, const void* q, const void* k, const 
     a.alibi = d->alibi;
     a.slopes = slopes;
     a.err = ds->err;
+    a.num_sms = ds->sms;
     cudaError_t e = launch_attention(dt, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     return BLK_OK;

@@ -253,6 +253,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc_f16(dt_traits<T>::mma_fmt, kBM, BN, false);
+            const uint64_t da0 = make_sdesc_sw128(sbase, 16, 1024);
+            const uint64_t db0 = make_sdesc_sw128(sbase + Cfg::kABytes, 16, 1024);
+            constexpr uint64_t kStageStep = Cfg::kStageBytes >> 4;
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -269,14 +272,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = sbase + stage * Cfg::kStageBytes;
-                    const uint32_t sb = sa + Cfg::kABytes;
+                    const uint64_t ad = da0 + stage * kStageStep;
+                    const uint64_t bd = db0 + stage * kStageStep;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        const uint64_t ad = make_sdesc_sw128(sa + k * 32, 16, 1024);
-                        const uint64_t bd = make_sdesc_sw128(sb + k * 32, 16, 1024);
-                        tc_mma_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc_mma_ss(d_tmem, ad + k * 2, bd + k * 2, idesc, (kb | k) != 0 ? 1u : 0u);
                     tc_commit(empty(stage));
                     if (++stage == kStages) {
                         stage = 0;

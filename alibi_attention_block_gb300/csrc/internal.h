@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/blk.h"
+#include "blk.h"
 #include "common.cuh"
 
 namespace blk {
@@ -77,6 +77,7 @@ struct AttnArgs {
     int alibi;
     const float* slopes;  // device [H] or nullptr (standard slopes)
     unsigned* err;
+    int num_sms;          // persistent grid size
 };
 cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s);
 
