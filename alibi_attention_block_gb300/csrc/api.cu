@@ -512,7 +512,9 @@ blk_status blk_layernorm_bias(const void* x, const void* residual, const void* g
                               blk_dtype dt, blk_stream_t s) {
     blk_status st = validate_norm(x, residual, gamma, beta, y, rows, cols, eps, dt);
     if (st != BLK_OK) return st;
-    const NormIO io{x, false, residual, false, y, nullptr};
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+    const NormIO io{x, false, residual, false, y, nullptr, ds->err, ds->sms};
     cudaError_t e = launch_norm(to_dt(dt), false, io, gamma, beta, rows, static_cast<int>(cols),
                                 eps, reinterpret_cast<cudaStream_t>(s));
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "layernorm launch");
@@ -522,7 +524,9 @@ blk_status blk_rmsnorm(const void* x, const void* residual, const void* weight, 
                        int64_t rows, int64_t cols, float eps, blk_dtype dt, blk_stream_t s) {
     blk_status st = validate_norm(x, residual, weight, nullptr, y, rows, cols, eps, dt);
     if (st != BLK_OK) return st;
-    const NormIO io{x, false, residual, false, y, nullptr};
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+    const NormIO io{x, false, residual, false, y, nullptr, ds->err, ds->sms};
     cudaError_t e = launch_norm(to_dt(dt), true, io, weight, nullptr, rows, static_cast<int>(cols),
                                 eps, reinterpret_cast<cudaStream_t>(s));
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "rmsnorm launch");
@@ -728,7 +732,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     // 1. input norm (absent in the reordered post-norm block)
     const void* attn_in = x;
     if (pre) {
-        e = launch_norm(t, rms, NormIO{x, false, nullptr, false, n1, nullptr}, w->attn_norm_w,
+        e = launch_norm(t, rms, NormIO{x, false, nullptr, false, n1, nullptr, ds->err, ds->sms}, w->attn_norm_w,
                         w->attn_norm_b, T, static_cast<int>(D), d->eps, cs);
         if (e != cudaSuccess) return cuda_fail(e, "input norm launch");
         BLK_STEP(BLK_STEP_INPUT_NORM);
@@ -768,7 +772,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
                         F32_OUT);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
-        e = launch_norm(t, rms, NormIO{hb, true, nullptr, false, n2, nullptr}, w->mlp_norm_w,
+        e = launch_norm(t, rms, NormIO{hb, true, nullptr, false, n2, nullptr, ds->err, ds->sms}, w->mlp_norm_w,
                         w->mlp_norm_b, T, static_cast<int>(D), d->eps, cs);
         if (e != cudaSuccess) return cuda_fail(e, "mlp norm launch");
         BLK_STEP(BLK_STEP_MLP_NORM);
@@ -781,7 +785,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
                         cs, ds, F32_OUT);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
-        e = launch_norm(t, true, NormIO{tmp, true, x, false, h16, static_cast<float*>(hb)},
+        e = launch_norm(t, true, NormIO{tmp, true, x, false, h16, static_cast<float*>(hb), ds->err, ds->sms},
                         w->post_attn_norm_w, nullptr, T, static_cast<int>(D), d->eps, cs);
         if (e != cudaSuccess) return cuda_fail(e, "post-attention norm launch");
         BLK_STEP(BLK_STEP_POST_ATTN_NORM);
@@ -805,7 +809,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
                     cs, ds, F32_OUT);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_DOWN);
-    e = launch_norm(t, true, NormIO{tmp, true, hb, true, y, nullptr}, w->post_mlp_norm_w, nullptr,
+    e = launch_norm(t, true, NormIO{tmp, true, hb, true, y, nullptr, ds->err, ds->sms}, w->post_mlp_norm_w, nullptr,
                     T, static_cast<int>(D), d->eps, cs);
     if (e != cudaSuccess) return cuda_fail(e, "post-mlp norm launch");
     BLK_STEP(BLK_STEP_POST_MLP_NORM);

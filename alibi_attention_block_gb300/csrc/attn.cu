@@ -63,11 +63,18 @@ struct AttnCfg {
     static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
 };
 
-// Walks this CTA's share of the (query tile, batch, head) items, heaviest
-// (latest) query tiles first, one 128-key tile at a time.
+// Walks this CTA's share of the (query tile, batch, head) items one 128-key
+// tile at a time. Items are ordered heaviest (latest query tile) first and
+// dealt to the CTAs in alternating directions (round r gives item
+// r*G + blockIdx on even rounds, r*G + G-1-blockIdx on odd ones), which
+// evens out the work per CTA.
 struct TileCursor {
     int item, it, j, nkv, qt, b, h, g;
     bool valid;
+    __device__ __forceinline__ int item_of(int round) const {
+        const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+        return round * G + ((round & 1) ? G - 1 - c : c);
+    }
     __device__ __forceinline__ void decode(const AttnArgs& a, int nq) {
         const int bh_count = a.B * a.H;
         qt = nq - 1 - item / bh_count;
@@ -78,8 +85,8 @@ struct TileCursor {
         nkv = qt + 1;
     }
     __device__ __forceinline__ void start(const AttnArgs& a, int nq, int n_items) {
-        item = blockIdx.x;
         it = 0;
+        item = item_of(0);
         j = 0;
         valid = item < n_items;
         if (valid) decode(a, nq);
@@ -88,7 +95,7 @@ struct TileCursor {
         if (++j < nkv) return;
         j = 0;
         ++it;
-        item += gridDim.x;
+        item = item_of(it);
         valid = item < n_items;
         if (valid) decode(a, nq);
     }

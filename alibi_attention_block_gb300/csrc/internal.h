@@ -24,6 +24,8 @@ struct NormIO {
     bool res_f32;
     void* y;
     float* y32;
+    unsigned* err;  // device error word (bounded waits)
+    int sms;        // SM count (persistent grid)
 };
 cudaError_t launch_norm(DType dt, bool rms, const NormIO& io, const void* gamma, const void* beta,
                         int64_t rows, int cols, float eps, cudaStream_t s);
