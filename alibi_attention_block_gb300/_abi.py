@@ -62,6 +62,7 @@ _PROTOS = {
     "blk_last_error": (C.c_char_p, []),
     "blk_version": (C.c_int, []),
     "blk_check_device_status": (C.c_int, [vp]),
+    "blk_selftest_bounded_wait": (C.c_int, [C.c_uint64, vp]),
     "blk_layernorm_bias": (C.c_int, [vp, vp, vp, vp, vp, i64, i64, f32, C.c_int, vp]),
     "blk_rmsnorm": (C.c_int, [vp, vp, vp, vp, i64, i64, f32, C.c_int, vp]),
     "blk_qkv_bias_rope_partial": (C.c_int, [C.POINTER(QkvDesc), vp, vp, vp, vp, vp, vp, vp, vp,

@@ -18,6 +18,16 @@ namespace blk {
 // Device error word, set by kernels whose bounded waits give up.
 __device__ unsigned int g_dev_err;
 
+// Self-test of the bounded-wait path: one thread waits on an mbarrier that
+// nothing arrives at; the wait gives up after limit_ns and sets the error word.
+__global__ void bounded_wait_selftest_kernel(unsigned* err, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_barrier_init();
+    if (!mbar_try_wait(b, 0)) mbar_wait_slow(b, 0, err, limit_ns);
+}
+
 namespace {
 
 thread_local std::string t_last_error;
@@ -505,6 +515,16 @@ blk_status blk_check_device_status(blk_stream_t s) {
         return fail(BLK_ETIMEOUT, "a bounded in-kernel wait gave up (device error code %u)", word);
     }
     return BLK_OK;
+}
+
+blk_status blk_selftest_bounded_wait(uint64_t limit_ns, blk_stream_t s) {
+    BLK_REQUIRE(limit_ns >= 1000 && limit_ns <= 5000000000ull, "limit_ns must be in [1 us, 5 s]");
+    DevState* ds = nullptr;
+    blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
+    bounded_wait_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(s)>>>(ds->err, limit_ns);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "self-test launch");
 }
 
 blk_status blk_layernorm_bias(const void* x, const void* residual, const void* gamma,

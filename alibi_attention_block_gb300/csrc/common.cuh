@@ -152,12 +152,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Slow path of mbar_wait: keep trying until kWaitLimitNs has passed.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned* err) {
+// Slow path of mbar_wait: keep trying until limit_ns has passed.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned* err,
+                                                   unsigned long long limit_ns = kWaitLimitNs) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((i & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) {
             report_error(err, DEV_ERR_TIMEOUT);
             return false;
         }

@@ -139,12 +139,151 @@ __global__ void __launch_bounds__(kRopeThreads) qk_norm_rope_kernel(QkNormRopeAr
     }
 }
 
+// Fast path: one warp per (token, q or k). Lane l holds the 16-byte vectors
+// V = l + 32 i of the token's heads laid end to end (head = V / vph,
+// vph = d / 8 vectors per head, vph dividing 32 so a head is a fixed group of
+// lanes); all loads are issued first. The full-width RMS sum is a warp
+// reduction, the per-head LayerNorm a reduction over the head's lane group,
+// and the rotary partner (dims j and j + r/2) is the same vector slot of the
+// lane r/16 away, fetched with a shuffle. Cosines and sines depend only on
+// the lane's vector slot within the head, so each lane evaluates them once.
+template <typename T, int NV>
+__global__ void __launch_bounds__(128) qk_warp_kernel(QkNormRopeArgs a, RopeParams rp) {
+    const int lane = threadIdx.x & 31;
+    const int wid = blockIdx.x * 4 + threadIdx.x / 32;
+    const int parts = a.Hk > 0 ? 2 : 1;
+    const int64_t tokens = static_cast<int64_t>(a.B) * a.S;
+    if (wid >= tokens * parts) return;  // whole warps exit together
+    const int part = wid % parts;
+    const int64_t token = wid / parts;
+    const int b = static_cast<int>(token / a.S);
+    const int s = static_cast<int>(token % a.S);
+    const int nh = part == 0 ? a.H : a.Hk;
+    T* base = static_cast<T*>(part == 0 ? a.q : a.k);
+    const T* bias = static_cast<const T*>(part == 0 ? a.q_bias : a.k_bias);
+    const T* w = static_cast<const T*>(part == 0 ? a.q_w : a.k_w);
+    const int d = a.d;
+    const int vph = d / 8;
+    const int nvec = nh * vph;
+    const int vin = lane % vph;  // same for every i because vph divides 32
+
+    float v[NV][8];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int V = lane + 32 * i;
+        if (V < nvec) {
+            const int head = V / vph;
+            load8(base + ((static_cast<int64_t>(b) * nh + head) * a.S + s) * d + vin * 8, v[i]);
+            if (bias) {
+                float bb[8];
+                load8(bias + V * 8, bb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] += bb[e];
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[i][e] = 0.f;
+        }
+    }
+    if (a.mode == QKN_RMS_FULL) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(v[i][e], v[i][e], acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const float rstd = rsqrtf(acc / static_cast<float>(nh * d) + a.eps);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int V = lane + 32 * i;
+            if (V < nvec) {
+                float g[8];
+                load8(w + V * 8, g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] *= rstd * g[e];
+            }
+        }
+    } else if (a.mode == QKN_LN_PER_HEAD) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sum += v[i][e];
+            for (int o = vph / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float mean = sum / static_cast<float>(d);
+            float sq = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float c = v[i][e] - mean;
+                sq = fmaf(c, c, sq);
+            }
+            for (int o = vph / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            const float rstd = rsqrtf(sq / static_cast<float>(d) + a.eps);
+            const int V = lane + 32 * i;
+            if (V < nvec) {
+                float g[8];
+                load8(w + V * 8, g);  // gamma [nh, d] read at head * d + vin * 8 = V * 8
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[i][e] = (v[i][e] - mean) * rstd * g[e];
+            }
+        }
+    }
+    const int hv = rp.span / 16;  // vectors in each rotated half
+    if (hv > 0) {
+        const bool lo = vin < hv;
+        const bool rot = vin < 2 * hv;
+        const int partner = lo ? lane + hv : lane - hv;
+        float c[8], sn[8];
+        if (rot) {
+            const int j0 = (lo ? vin : vin - hv) * 8;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rope_cos_sin(rp, s, j0 + e, c[e], sn[e]);
+        }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float other = __shfl_sync(0xffffffffu, v[i][e], rot ? partner : lane);
+                if (rot) v[i][e] = lo ? v[i][e] * c[e] - other * sn[e] : v[i][e] * c[e] + other * sn[e];
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int V = lane + 32 * i;
+        if (V < nvec)
+            store8(base + ((static_cast<int64_t>(b) * nh + V / vph) * a.S + s) * d + vin * 8, v[i]);
+    }
+}
+
+template <typename T>
+bool launch_warp_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
+    const int vph = a.d / 8;
+    const int maxh = a.H > a.Hk ? a.H : a.Hk;
+    const int nvec = maxh * vph;
+    if (a.d % 8 || vph > 32 || 32 % vph || (rp.span / 2) % 8 || nvec > 256) return false;
+    const int64_t warps = static_cast<int64_t>(a.B) * a.S * (a.Hk > 0 ? 2 : 1);
+    const int64_t blocks = (warps + 3) / 4;
+    if (blocks > 0x7fffffff) return false;
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (nvec <= 32) qk_warp_kernel<T, 1><<<g, 128, 0, s>>>(a, rp);
+    else if (nvec <= 64) qk_warp_kernel<T, 2><<<g, 128, 0, s>>>(a, rp);
+    else if (nvec <= 128) qk_warp_kernel<T, 4><<<g, 128, 0, s>>>(a, rp);
+    else qk_warp_kernel<T, 8><<<g, 128, 0, s>>>(a, rp);
+    return true;
+}
+
 }  // namespace
 
 cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopeParams& rp,
                                 cudaStream_t s) {
     const int64_t tokens = static_cast<int64_t>(a.B) * a.S;
     if (tokens == 0) return cudaSuccess;
+    if (dt == DType::F16 ? launch_warp_path<__half>(a, rp, s)
+                         : launch_warp_path<__nv_bfloat16>(a, rp, s))
+        return cudaGetLastError();
+    // general path (e.g. head_dim 160 or spans not a multiple of 16)
     const size_t smem = static_cast<size_t>(a.H + a.Hk) * a.d * sizeof(float);
     if (dt == DType::F16) {
         auto k = qk_norm_rope_kernel<__half>;

@@ -133,6 +133,78 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------- standalone kernels --
+def _time_back_to_back(fn, reps=50):
+    for _ in range(5):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def standalone_hbm(blk, dev):
+    """The bandwidth-bound kernels on inputs larger than L2 (so every launch
+    streams from HBM), back to back: achieved GB/s of algorithmic bytes."""
+    out = {}
+    rows, cols = 32768, 2048                       # 134 MB in, 134 MB out
+    x = workloads.draw((rows, cols), "bf16", 91).to(dev)
+    g = workloads.draw((cols,), "bf16", 92, "g").to(dev)
+    b = workloads.draw((cols,), "bf16", 93, "b").to(dev)
+    y = torch.empty_like(x)
+    ms = _time_back_to_back(lambda: blk.layernorm_bias(x, g, b, eps=1e-5, out=y))
+    out["layernorm_bias_32768x2048_bf16"] = {"ms": ms, "gbs": 2 * x.numel() * 2 / (ms / 1e3) / 1e9}
+    ms = _time_back_to_back(lambda: blk.rmsnorm(x, g, eps=1e-6, out=y))
+    out["rmsnorm_32768x2048_bf16"] = {"ms": ms, "gbs": 2 * x.numel() * 2 / (ms / 1e3) / 1e9}
+    del x, y
+    q = workloads.draw((16, 32, 2048, 64), "bf16", 94).to(dev)   # 134 MB of q
+    bias = workloads.draw((32 * 64,), "bf16", 95, "b").to(dev)
+    ms = _time_back_to_back(lambda: blk.rope_inplace(q, bias, rotary_span=16, rope_base=1e4))
+    out["bias_rope_inplace_16x32x2048x64_bf16"] = {"ms": ms, "gbs": 2 * q.numel() * 2 / (ms / 1e3) / 1e9}
+    del q
+    return out
+
+
+def run_attn_sweep(args, rank):
+    """Attention-only workloads: q, k, v already projected; the QKV bias and
+    partial rotary are applied by blk_rope_inplace, then blk_attn_prefill."""
+    import alibi_attention_block_gb300 as blk
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    peaks = _peaks()
+    res = {}
+    for name, c in workloads.ATTN_CONFIGS.items():
+        q, k, v, biases = workloads.attn_inputs(c)
+        q, k, v = q.to(dev), k.to(dev), v.to(dev)
+        if biases is not None:
+            biases = [t.to(dev) for t in biases]
+        o = torch.empty((c.batch, c.seq, c.n_heads, c.head_dim), dtype=q.dtype, device=dev)
+        def prologue():
+            blk.rope_inplace(q, biases[0] if biases else None, c.rotary_span, c.rope_base)
+            blk.rope_inplace(k, biases[1] if biases else None, c.rotary_span, c.rope_base)
+            if biases:
+                blk.rope_inplace(v, biases[2], 0, c.rope_base)
+        t_pro = _time_back_to_back(prologue, reps=5)
+        t_att = _time_back_to_back(lambda: blk.attn_prefill(q, k, v, alibi=c.alibi, out=o), reps=10)
+        flops = 4 * c.batch * c.n_heads * c.head_dim * c.seq * (c.seq + 1) // 2
+        tf = flops / (t_att / 1e3) / 1e12
+        res[name] = {"batch": c.batch, "seq": c.seq, "heads": c.n_heads, "kv_heads": c.n_kv_heads,
+                     "head_dim": c.head_dim, "attention_ms": t_att, "attention_tflops": tf,
+                     "frac_of_measured_bf16_peak": tf / peaks["bf16_tflops"],
+                     "bias_rope_prologue_ms": t_pro,
+                     "tokens_per_s": c.batch * c.seq / ((t_att + t_pro) / 1e3)}
+        del q, k, v, o
+        torch.cuda.empty_cache()
+    blk.check_device_status()
+    if rank == 0:
+        print(json.dumps({"metric": "attention-only prefill sweep (TFLOP/s, causal)", "sweep": res}),
+              flush=True)
+
+
 # ----------------------------------------------------------------- oracle --
 _INPUTS = {}
 
@@ -289,9 +361,12 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
+    standalone = standalone_hbm(blk, dev) if rank == 0 else None
     if rank != 0:
         return
     peaks = _peaks()
+    for v in standalone.values():
+        v["frac_of_measured_hbm"] = v["gbs"] / peaks["hbm_gbs"]
     work = step_work(cfg)
     dom = max(kernel_ms, key=kernel_ms.get)
     dw = work[dom]
@@ -340,6 +415,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         "e2e": {"value": world * cfg.tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": y.numel() * y.element_size()},
+        "hbm_kernels_standalone": standalone,
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
         "wall_s_timed": t_wall,
@@ -356,12 +432,16 @@ def main():
     ap.add_argument("--config", default="stablelm2_1p6b", choices=sorted(workloads.BLOCK_CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--attn-sweep", action="store_true",
+                    help="time the attention-only workloads instead of the block")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = workloads.BLOCK_CONFIGS[args.config]
     dist, rank, world, local_rank = _dist()
-    if args.impl == "reference":
+    if args.attn_sweep:
+        run_attn_sweep(args, rank)
+    elif args.impl == "reference":
         run_reference(args, cfg, rank, world)
     else:
         run_ours(args, cfg, rank, world, local_rank, dist)

@@ -67,6 +67,14 @@ int blk_version(void);
  * last check; BLK_ECUDA on a CUDA error. */
 blk_status blk_check_device_status(blk_stream_t s);
 
+/* Self-test of the failure path: enqueues one single-thread kernel that
+ * waits on a barrier nothing ever completes, with a wait limit of limit_ns
+ * (1 us .. 5 s) instead of the kernels' ~2 s. The wait gives up, sets the
+ * device error word and the kernel returns, so the next
+ * blk_check_device_status(s) reports BLK_ETIMEOUT (and clears it) while the
+ * context stays usable. No GPU fault, trap or hang is involved. */
+blk_status blk_selftest_bounded_wait(uint64_t limit_ns, blk_stream_t s);
+
 /* ---- norms ------------------------------------------------------------ */
 
 /* LayerNorm with bias ("StableLM-2: partial RoPE and a first
