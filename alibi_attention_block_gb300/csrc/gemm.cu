@@ -171,7 +171,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
     }
 }
 
-template <typename T, int BN, int EPI, int ROT>
+// CL = 2: a cluster of two CTAs takes vertically adjacent tiles (2m, n) and
+// (2m+1, n), which share the B tile. Each CTA loads its own A tile and one
+// half of the B tile, multicast into both CTAs' shared memory, so B crosses
+// from L2 once per pair (a third less L2 traffic per stage). A stage is
+// refilled only after both CTAs' MMAs have released it: each MMA completion
+// arrives on the empty barrier of both CTAs (multicast commit).
+template <typename T, int BN, int EPI, int ROT, int CL>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const GemmArgs g,
@@ -179,7 +185,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     using Cfg = GemmCfg<BN>;
     constexpr int kStages = Cfg::kStages;
     constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
-
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
@@ -190,13 +195,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto empty = [&](int i) { return bar0 + 8u * (kStages + i); };
     auto tfull = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
     auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 + i); };
-
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
+    const int rank = CL == 2 ? static_cast<int>(cluster_ctarank()) : 0;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(full(i), 1);
-            mbar_init(empty(i), 1);
+            mbar_init(empty(i), CL);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull(i), 1);
@@ -212,22 +217,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CL == 2)
+        cluster_sync();  // the peer's barriers exist before anything targets them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
     const int m_tiles = (g.M + kBM - 1) / kBM;
     const int n_tiles = (g.N + kBNOut - 1) / kBNOut;
-    const int num_tiles = m_tiles * n_tiles;
+    // work units: single tiles, or vertical pairs of tiles for a cluster
+    const int m_units = (m_tiles + CL - 1) / CL;
+    const int num_units = m_units * n_tiles;
+    const int unit0 = static_cast<int>(blockIdx.x) / CL;
+    const int unit_step = static_cast<int>(gridDim.x) / CL;
     const int kb_count = (g.K + kBK - 1) / kBK;
-
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const int mt = t % m_tiles, nt = t / m_tiles;
+            for (int u = unit0; u < num_units && ok; u += unit_step) {
+                const int mt = (u % m_units) * CL + rank, nt = u / m_units;
                 for (int kb = 0; kb < kb_count; ++kb) {
                     if (!mbar_wait(empty(stage), phase ^ 1u, g.err)) {
                         ok = false;
@@ -237,7 +247,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t sb = sa + Cfg::kABytes;
                     mbar_expect_tx(full(stage), Cfg::kStageBytes);
                     tma_load_2d(sa, &tmA, full(stage), kb * kBK, mt * kBM);
-                    if constexpr (EPI == EPI_SWIGLU) {
+                    if constexpr (CL == 2) {
+                        // this CTA's half of the B tile, into both CTAs
+                        if constexpr (EPI == EPI_SWIGLU)
+                            tma_load_2d_multicast(sb + rank * (BN / 2) * 128, rank ? &tmB2 : &tmB,
+                                                  full(stage), kb * kBK, nt * kBNOut, 0x3);
+                        else
+                            tma_load_2d_multicast(sb + rank * (BN / 2) * 128, &tmB, full(stage),
+                                                  kb * kBK, nt * BN + rank * (BN / 2), 0x3);
+                    } else if constexpr (EPI == EPI_SWIGLU) {
                         tma_load_2d(sb, &tmB, full(stage), kb * kBK, nt * kBNOut);
                         tma_load_2d(sb + (BN / 2) * 128, &tmB2, full(stage), kb * kBK, nt * kBNOut);
                     } else {
@@ -260,7 +278,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+            for (int u = unit0; u < num_units && ok; u += unit_step, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!mbar_wait(tempty(acc), acc_phase ^ 1u, g.err)) break;
@@ -277,7 +295,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
                         tc_mma_ss(d_tmem, ad + k * 2, bd + k * 2, idesc, (kb | k) != 0 ? 1u : 0u);
-                    tc_commit(empty(stage));
+                    if constexpr (CL == 2)
+                        tc_commit_multicast(empty(stage), 0x3);
+                    else
+                        tc_commit(empty(stage));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -290,12 +311,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         int it = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+        for (int u = unit0; u < num_units; u += unit_step, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!mbar_wait(tfull(acc), acc_phase, g.err)) break;
             tc_fence_after();
-            const int mt = t % m_tiles, nt = t / m_tiles;
+            const int mt = (u % m_units) * CL + rank, nt = u / m_units;
             const uint32_t tbase =
                 tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
             epilogue_tile<T, BN, EPI, ROT>(g, rp, tbase, mt * kBM + row, nt);
@@ -304,30 +325,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (lane == 0) mbar_arrive(tempty(acc));
         }
     }
-    __syncthreads();
+    // every MMA of this CTA has completed (its epilogue consumed the last
+    // accumulator), so all its arrivals on the peer's barriers have landed
+    if constexpr (CL == 2)
+        cluster_sync();
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
 }
 
-template <typename T, int BN, int EPI, int ROT = 0>
-cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
-                       const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
+template <typename T, int BN, int EPI, int ROT, int CL>
+cudaError_t launch_cl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                      const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
     using Cfg = GemmCfg<BN>;
     constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
-    auto kern = gemm_kernel<T, BN, EPI, ROT>;
+    auto kern = gemm_kernel<T, BN, EPI, ROT, CL>;
     static bool attr_set = false;  // per template instance
+    static int max_clusters = 0;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg::kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int64_t tiles = static_cast<int64_t>((g.M + kBM - 1) / kBM) * ((g.N + kBNOut - 1) / kBNOut);
-    const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-    kern<<<grid, kGemmThreads, Cfg::kSmem, s>>>(ta, tb, tb2, g, rp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t m_units = ((g.M + kBM - 1) / kBM + CL - 1) / CL;
+    const int64_t units = m_units * ((g.N + kBNOut - 1) / kBNOut);
+    int64_t slots = num_sms / CL;
+    if (CL > 1) {
+        if (max_clusters == 0) {
+            cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CL * CL), 1, 1);
+            if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess ||
+                max_clusters <= 0)
+                max_clusters = num_sms / CL;
+        }
+        slots = max_clusters;
+    }
+    const int64_t grid_units = units < slots ? units : slots;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_units * CL), 1, 1);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, g, rp);
+}
+
+template <typename T, int BN, int EPI, int ROT = 0>
+cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                       const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
+    if (g.M > kBM)
+        return launch_cl<T, BN, EPI, ROT, 2>(ta, tb, tb2, g, rp, num_sms, s);
+    return launch_cl<T, BN, EPI, ROT, 1>(ta, tb, tb2, g, rp, num_sms, s);
 }
 
 template <typename T>
@@ -335,7 +392,9 @@ cudaError_t launch_t(DType dt, int epi, const void* a, const void* b, const void
                      const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
     constexpr int BN = 256;
     CUtensorMap ta, tb, tb2;
-    const uint32_t b_box = epi == EPI_SWIGLU ? BN / 2 : BN;
+    // the B box is half a tile whenever the pair of CTAs splits the B tile
+    // (M > 128) or the tile stacks gate and up rows (SWIGLU)
+    const uint32_t b_box = (epi == EPI_SWIGLU || g.M > kBM) ? BN / 2 : BN;
     if (!make_tmap_2d(&ta, dt, a, g.M, g.K, kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_2d(&tb, dt, b, g.N, g.K, b_box)) return cudaErrorInvalidValue;
     tb2 = tb;

