@@ -21,7 +21,7 @@ from . import _abi
 from ._abi import BlkError  # noqa: F401
 
 __all__ = ["layernorm_bias", "rmsnorm", "qkv_bias_rope_partial", "rope_inplace", "attn_prefill",
-           "linear", "mlp", "block_desc", "forward_workspace_size", "forward",
+           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host",
            "check_device_status", "BlkError", "library_path"]
 
 library_path = _abi.LIB_PATH
@@ -210,6 +210,40 @@ def forward(cfg, weights: dict, x, workspace=None, out=None):
     _abi.check(_lib().blk_forward(C.byref(desc), C.byref(w), _p(x), _p(out), _p(workspace),
                                   workspace.numel(), _dt(x), _stream()), "blk_forward")
     return out
+
+
+def forward_host(cfg, weights: dict, x_host, y_host=None, x_dev=None, y_dev=None,
+                 workspace=None, n_chunks=2):
+    """The block on host tensors (pinned CPU memory), copies overlapped with
+    compute over n_chunks groups of sequences. x_dev / y_dev / workspace are
+    reusable device staging buffers (allocated here when None). Returns
+    y_host; it is ready when the current stream reaches the end of the call."""
+    if x_host.is_cuda or not x_host.is_pinned():
+        raise ValueError("x_host must be a pinned CPU tensor")
+    B, S, _ = x_host.shape
+    dev = torch.device("cuda", torch.cuda.current_device())
+    y_host = torch.empty_like(x_host).pin_memory() if y_host is None else y_host
+    if y_host.is_cuda or not y_host.is_pinned() or y_host.shape != x_host.shape:
+        raise ValueError("y_host must be a pinned CPU tensor shaped like x_host")
+    x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev) if x_dev is None else x_dev
+    y_dev = torch.empty_like(x_dev) if y_dev is None else y_dev
+    _same(x_host, x_dev, y_dev)
+    desc = block_desc(cfg, B, S)
+    ws_need = forward_workspace_size(cfg, B, S)
+    if workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
+    unknown = set(weights) - set(_abi.WEIGHT_SLOTS)
+    if unknown:
+        raise KeyError(f"unknown weight slots: {sorted(unknown)}")
+    for name, t in weights.items():
+        if name != "alibi_slopes":
+            _same(x_host, t)
+    w = _abi.BlockWeights(*[_p(weights.get(n)) for n in _abi.WEIGHT_SLOTS])
+    _abi.check(_lib().blk_forward_host(C.byref(desc), C.byref(w), C.c_void_p(x_host.data_ptr()),
+                                       C.c_void_p(y_host.data_ptr()), _p(x_dev), _p(y_dev),
+                                       _p(workspace), workspace.numel(), n_chunks, _dt(x_host),
+                                       _stream()), "blk_forward_host")
+    return y_host
 
 
 def check_device_status():

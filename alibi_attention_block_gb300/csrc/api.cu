@@ -46,10 +46,16 @@ blk_status cuda_fail(cudaError_t e, const char* what) {
     return fail(BLK_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+constexpr int kMaxHostChunks = 16;
 struct DevState {
     bool init = false;
     int sms = 0;
     unsigned* err = nullptr;
+    // copy streams and events of blk_forward_host (created on its first use)
+    bool pipe_init = false;
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_in[kMaxHostChunks] = {}, ev_out[kMaxHostChunks] = {},
+                ev_done = nullptr;
 };
 constexpr int kMaxDevices = 64;
 DevState g_dev[kMaxDevices];
@@ -835,6 +841,82 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     BLK_STEP(BLK_STEP_POST_MLP_NORM);
     return log.end();
 #undef BLK_STEP
+}
+
+blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
+                            const void* x_host, void* y_host, void* x_dev, void* y_dev,
+                            void* workspace, size_t ws_bytes, int32_t n_chunks, blk_dtype dt,
+                            blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    blk_status st = validate_block(d, w);
+    if (st != BLK_OK) return st;
+    BLK_REQUIRE(x_host && y_host, "x_host / y_host is NULL");
+    BLK_CHECK_PTR(x_dev, true);
+    BLK_CHECK_PTR(y_dev, true);
+    BLK_REQUIRE(x_dev != y_dev, "y_dev must not alias x_dev");
+    BLK_REQUIRE(n_chunks >= 1 && n_chunks <= kMaxHostChunks, "n_chunks must be in [1, 16]");
+    const int64_t B = d->qkv.batch;
+    const int chunks = static_cast<int>(n_chunks < B ? n_chunks : B);
+    const FwdLayout L = forward_layout(d);
+    if (!workspace || ws_bytes < L.total || !aligned16(workspace))
+        return fail(BLK_EWORKSPACE, "workspace needs %zu bytes, 16-byte aligned", L.total);
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!ds->pipe_init) {
+            cudaError_t e = cudaStreamCreateWithFlags(&ds->copy_in, cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ds->copy_out, cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds->ev_start, cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds->ev_done, cudaEventDisableTiming);
+            for (int i = 0; i < kMaxHostChunks && e == cudaSuccess; ++i) {
+                e = cudaEventCreateWithFlags(&ds->ev_in[i], cudaEventDisableTiming);
+                if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds->ev_out[i], cudaEventDisableTiming);
+            }
+            if (e != cudaSuccess) return cuda_fail(e, "copy stream/event set-up");
+            ds->pipe_init = true;
+        }
+    }
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    const size_t row_bytes = static_cast<size_t>(d->qkv.seq) * d->qkv.hidden * 2;  // one sequence
+    // everything earlier on s (a previous call's reads of x_dev / y_dev) comes first
+    cudaError_t e = cudaEventRecord(ds->ev_start, cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->copy_in, ds->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->copy_out, ds->ev_start, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "stream ordering");
+    int64_t b0[kMaxHostChunks + 1];
+    for (int c = 0; c <= chunks; ++c) b0[c] = B * c / chunks;
+    for (int c = 0; c < chunks; ++c) {
+        const size_t off = static_cast<size_t>(b0[c]) * row_bytes;
+        const size_t bytes = static_cast<size_t>(b0[c + 1] - b0[c]) * row_bytes;
+        e = cudaMemcpyAsync(static_cast<uint8_t*>(x_dev) + off,
+                            static_cast<const uint8_t*>(x_host) + off, bytes,
+                            cudaMemcpyHostToDevice, ds->copy_in);
+        if (e == cudaSuccess) e = cudaEventRecord(ds->ev_in[c], ds->copy_in);
+        if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    }
+    for (int c = 0; c < chunks; ++c) {
+        const size_t off = static_cast<size_t>(b0[c]) * row_bytes;
+        const size_t bytes = static_cast<size_t>(b0[c + 1] - b0[c]) * row_bytes;
+        e = cudaStreamWaitEvent(cs, ds->ev_in[c], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "stream ordering");
+        blk_block_desc dc = *d;
+        dc.qkv.batch = b0[c + 1] - b0[c];
+        st = blk_forward(&dc, w, static_cast<const uint8_t*>(x_dev) + off,
+                         static_cast<uint8_t*>(y_dev) + off, workspace, ws_bytes, dt, s);
+        if (st != BLK_OK) return st;
+        e = cudaEventRecord(ds->ev_out[c], cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->copy_out, ds->ev_out[c], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t*>(y_host) + off,
+                                static_cast<const uint8_t*>(y_dev) + off, bytes,
+                                cudaMemcpyDeviceToHost, ds->copy_out);
+        if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    }
+    // the call completes on s when the last copy out has landed
+    e = cudaEventRecord(ds->ev_done, ds->copy_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ds->ev_done, 0);
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "stream ordering");
 }
 
 }  // extern "C"

@@ -481,7 +481,7 @@ cudaError_t launch_a(DType dt, const AttnArgs& a, cudaStream_t s) {
 template <typename T>
 cudaError_t launch_t(DType dt, const AttnArgs& a, cudaStream_t s) {
     switch (a.d) {
-        case 64: return launch_a<T, 64>(dt, a, s);
+        case 64: return launch_attention_pair64(dt, a, s);
         case 128: return launch_a<T, 128>(dt, a, s);
         case 160: return launch_a<T, 160>(dt, a, s);
         default: return cudaErrorInvalidValue;

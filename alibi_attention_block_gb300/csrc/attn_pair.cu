@@ -1,0 +1,513 @@
+// K3 at head_dim 64: causal softmax attention on tcgen05 tensor cores, two
+// 128-query tiles per work item.
+//
+// At head_dim 64 a 128x128 score tile costs 64 FLOP of MMA per exponential,
+// so the softmax (one ex2 per score, 32 per clock per SM) and the tensor core
+// take about as long as each other on a tile: the kernel has to keep both busy
+// at once. Each CTA owns one SM and works on a pair of query tiles A = 2i and
+// B = 2i + 1 of one (batch, head); they share every K/V tile, and while one
+// tile's exponentials are computed the tensor core runs the other tile's
+// products. The MMA thread issues, per key tile j,
+//     S_A(j+1) = Q_A K_{j+1}^T,  O_A += P_A(j) V_j,  S_B(j+1),  O_B += P_B(j) V_j
+// so the scores of the next tile are ready when a softmax warpgroup finishes
+// the current one (each query tile's products come from its own issuing
+// thread, in that order). 12 warps:
+//   warp 0      TMA: both Q tiles of an item (double-buffered across items),
+//               then K and V tiles of 128 keys into a four-stage ring
+//               (128-byte swizzle, 64-column boxes, zero fill past S).
+//   warps 1, 2  one MMA-issuing thread per query tile (M=128, K=16 per
+//               instruction): S (N=128) from Q and K in shared memory, PV
+//               (N=64) from P in TMEM and V in shared memory (V MN-major).
+//               An MMA issue returns only about when the tensor core takes
+//               it, and a barrier test costs on the order of a hundred
+//               clocks, so one issuing thread that waits between groups
+//               leaves the tensor core idle; with one thread per query tile
+//               the other tile's products fill those gaps. Warp 1 also
+//               allocates TMEM.
+//               Keeping P out of shared memory matters: the tensor core's
+//               operand reads, the TMA writes and any P traffic share the
+//               SM's shared-memory bandwidth, and an all-shared-memory PV
+//               would make that the bound.
+//   warp 3      idle.
+//   warps 4..7  softmax of tile A, one thread per query row (TMEM lane);
+//   warps 8..11 softmax of tile B. Per key tile: one tcgen05.ld of the row's
+//               128 scores (the S buffer is released at once), the causal
+//               mask on the diagonal (and ragged last) tile only, the row max
+//               (3-input max), one paired (f32x2) FMA per two scores into ex2
+//               (scale log2(e)/sqrt(d) folded in; for ALiBi the bias
+//               -slope*(i-j), "Bloom in a sovereign engine", Contribution,
+//               enters as +slope*j, the -slope*i part being constant along
+//               the row), P rounded to the storage type and written to this
+//               tile's P columns in TMEM (after the previous PV has read them;
+//               in steady state that PV ends while S is being read and the
+//               max taken, since the tensor core runs the other tile between).
+//               O is rescaled in TMEM only when the running max
+//               grows by more than 2^8. At the end of an item O / l is read
+//               out of TMEM and written as [B, S, H, d].
+// TMEM columns: S_A [0, 128), S_B [128, 256), P_A [256, 320), P_B [320, 384)
+// (two 16-bit values per column), O_A [384, 448), O_B [448, 512).
+// Items are (query-tile pair, batch, head), heaviest pairs first, dealt to
+// the persistent CTAs in alternating directions.
+// Query scale head_dim^-0.5 and GQA (kv head = h / (H/Hk)) follow nnterp
+// "stablelm" 03 Notes.
+#include "internal.h"
+
+namespace blk {
+
+namespace {
+
+constexpr int kPairThreads = 384;
+constexpr int kTQ = 128;  // query rows per tile
+constexpr int kTK = 128;  // keys per tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest unnormalised p
+
+template <int D>
+struct PairCfg {
+    static_assert(D == 64, "the pair kernel is built for head_dim 64");
+    static constexpr int kSub = D / 64;                 // 64-column boxes per row
+    static constexpr int kQBytes = kSub * kTQ * 128;    // one Q tile
+    static constexpr int kKVBytes = kSub * kTK * 128;   // one K or V tile
+    static constexpr int kQBufs = 2;
+    static constexpr int kStages = 4;
+    static constexpr int kOffKV = kQBufs * 2 * kQBytes;
+    static constexpr int kOffBar = kOffKV + kStages * 2 * kKVBytes;
+    static constexpr int kSmem = kOffBar + 256 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t kColP = 256;              // P_x at kColP + 64 x
+    static constexpr uint32_t kColO = 384;              // O_x at kColO + D x
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+// This CTA's items: (pair i, batch b, head h), pair i = query tiles 2i and
+// 2i+1 (the second absent when the tile count is odd and i is the last pair).
+// Round r gives item r*G + blockIdx on even rounds and r*G + G-1-blockIdx on
+// odd ones; items are numbered heaviest pair first.
+struct PairCursor {
+    int item, it, i, b, h, g, nA, nB;
+    bool valid;
+    __device__ __forceinline__ int item_of(int round) const {
+        const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+        return round * G + ((round & 1) ? G - 1 - c : c);
+    }
+    __device__ __forceinline__ void decode(const AttnArgs& a, int nq, int np) {
+        const int bh_count = a.B * a.H;
+        i = np - 1 - item / bh_count;
+        const int bh = item % bh_count;
+        b = bh / a.H;
+        h = bh - b * a.H;
+        g = h / (a.H / a.Hk);
+        nA = 2 * i + 1;                          // key tiles of query tile 2i
+        nB = (2 * i + 1 < nq) ? 2 * i + 2 : 0;   // of query tile 2i+1, if present
+    }
+    __device__ __forceinline__ void start(const AttnArgs& a, int nq, int np, int n_items) {
+        it = 0;
+        item = item_of(0);
+        valid = item < n_items;
+        if (valid) decode(a, nq, np);
+    }
+    __device__ __forceinline__ void next(const AttnArgs& a, int nq, int np, int n_items) {
+        ++it;
+        item = item_of(it);
+        valid = item < n_items;
+        if (valid) decode(a, nq, np);
+    }
+    __device__ __forceinline__ int n_kv() const { return nB ? nB : nA; }
+};
+
+template <typename T, int D, bool ALIBI>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+    using Cfg = PairCfg<D>;
+    constexpr int kStages = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const uint32_t sQ = smem_u32(smem);      // Q[buf][x] at (2 buf + x) tiles
+    const uint32_t sKV = sQ + Cfg::kOffKV;   // stage s: K at 2s, V at 2s + 1 tiles
+    const uint32_t bar0 = sQ + Cfg::kOffBar;
+    // barriers (8 bytes each); x = 0 for query tile A, 1 for B
+    auto s_full = [&](int x) { return bar0 + 8u * x; };
+    auto s_free = [&](int x) { return bar0 + 16u + 8u * x; };
+    auto p_full = [&](int x) { return bar0 + 32u + 8u * x; };
+    auto pv_done = [&](int x) { return bar0 + 48u + 8u * x; };
+    auto o_free = [&](int x) { return bar0 + 64u + 8u * x; };
+    auto q_full = [&](int i) { return bar0 + 80u + 8u * i; };
+    auto q_empty = [&](int i) { return bar0 + 96u + 8u * i; };
+    auto k_full = [&](int i) { return bar0 + 112u + 8u * i; };
+    auto v_full = [&](int i) { return bar0 + 112u + 8u * (kStages + i); };
+    auto k_empty = [&](int i) { return bar0 + 112u + 8u * (2 * kStages + i); };
+    auto v_empty = [&](int i) { return bar0 + 112u + 8u * (3 * kStages + i); };
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 112 + 32 * kStages);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    const int nq = (a.S + kTQ - 1) / kTQ;
+    const int np = (nq + 1) / 2;
+    const int n_items = np * a.B * a.H;
+
+    if (threadIdx.x == 0) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(s_free(x), 4);
+            mbar_init(p_full(x), 4);
+            mbar_init(pv_done(x), 1);
+            mbar_init(o_free(x), 4);
+            mbar_init(q_full(x), 1);
+            mbar_init(q_empty(x), 2);
+        }
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(k_empty(i), 2);
+            mbar_init(v_empty(i), 2);
+        }
+        fence_barrier_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            PairCursor c;
+            c.start(a, nq, np, n_items);
+            int gkv = 0;  // K/V tiles loaded so far (ring position)
+            bool ok = true;
+            while (ok && c.valid) {
+                const int qb = c.it & 1;
+                if (!mbar_wait(q_empty(qb), ((c.it >> 1) & 1) ^ 1u, a.err)) break;
+                mbar_expect_tx(q_full(qb), (c.nB ? 2 : 1) * Cfg::kQBytes);
+                for (int x = 0; x < (c.nB ? 2 : 1); ++x) {
+#pragma unroll
+                    for (int sub = 0; sub < Cfg::kSub; ++sub)
+                        tma_load_3d(sQ + (2 * qb + x) * Cfg::kQBytes + sub * kTQ * 128, &tmQ,
+                                    q_full(qb), sub * 64, (2 * c.i + x) * kTQ, c.b * a.H + c.h);
+                }
+                const int nkv = c.n_kv();
+                for (int j = 0; j < nkv; ++j, ++gkv) {
+                    const int st = gkv % kStages;
+                    const uint32_t ph = (gkv / kStages) & 1;
+                    const uint32_t sK = sKV + (2 * st) * Cfg::kKVBytes;
+                    if (!mbar_wait(k_empty(st), ph ^ 1u, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(k_full(st), Cfg::kKVBytes);
+#pragma unroll
+                    for (int sub = 0; sub < Cfg::kSub; ++sub)
+                        tma_load_3d(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
+                                    c.b * a.Hk + c.g);
+                    if (!mbar_wait(v_empty(st), ph ^ 1u, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(v_full(st), Cfg::kKVBytes);
+#pragma unroll
+                    for (int sub = 0; sub < Cfg::kSub; ++sub)
+                        tma_load_3d(sK + Cfg::kKVBytes + sub * kTK * 128, &tmV, v_full(st),
+                                    sub * 64, j * kTK, c.b * a.Hk + c.g);
+                }
+                c.next(a, nq, np, n_items);
+            }
+        }
+    } else if (warp == 1 || warp == 2) {
+        if (lane == 0) {
+            // MMA issuer of query tile x (warp 1: A, warp 2: B). Two issuing
+            // threads keep the tensor core fed while either one waits on a
+            // barrier; each commits to the shared K/V and Q release barriers
+            // (count 2), also for key tiles its query tile does not use.
+            const int x = warp - 1;
+            constexpr uint32_t fmt = dt_traits<T>::mma_fmt;
+            constexpr uint32_t idesc_s = make_idesc_f16(fmt, kTQ, kTK, false);
+            constexpr uint32_t idesc_o = make_idesc_f16(fmt, kTQ, D, true);
+            constexpr uint64_t kQStep = Cfg::kQBytes >> 4;
+            constexpr uint64_t kStageStep = (2 * Cfg::kKVBytes) >> 4;
+            constexpr uint64_t kAtom = (kTQ * 128) >> 4;  // next 64-column atom
+            const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024) + x * kQStep;
+            const uint64_t dk0 = make_sdesc_sw128(sKV, 16, 1024);
+            const uint64_t dv0 = make_sdesc_sw128(sKV + Cfg::kKVBytes, kTK * 128, 1024);
+            const uint32_t tS = tmem_base + 128u * x;
+            const uint32_t tP = tmem_base + Cfg::kColP + 64u * x;
+            const uint32_t tO = tmem_base + Cfg::kColO + D * x;
+            int gs = 0, gp = 0, itx = 0;  // S and PV tiles issued, items with this tile
+            // S_x = Q_x K^T, once the softmax has read the previous S_x
+            auto issue_s = [&](uint64_t dq, uint64_t dk) -> bool {
+                if (gs > 0 && !mbar_wait(s_free(x), (gs - 1) & 1, a.err)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t off = (ks / 4) * kAtom + (ks % 4) * 2;
+                    tc_mma_ss(tS, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(s_full(x));
+                ++gs;
+                return true;
+            };
+            // O_x += P_x V once the softmax has written P_x (the first PV of an
+            // item overwrites O_x, so it also waits for the previous read-out)
+            auto issue_pv = [&](uint64_t dv, bool first) -> bool {
+                if (!mbar_wait(p_full(x), gp & 1, a.err)) return false;
+                if (first && itx > 0 && !mbar_wait(o_free(x), (itx - 1) & 1, a.err)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kTK / 16; ++ks)
+                    tc_mma_ts(tO, tP + ks * 8, dv + ks * ((16 * 128) >> 4), idesc_o,
+                              (!first || ks > 0) ? 1u : 0u);
+                tc_commit(pv_done(x));
+                ++gp;
+                return true;
+            };
+            PairCursor c;
+            c.start(a, nq, np, n_items);
+            int gkv = 0;
+            bool ok = true;
+            while (ok && c.valid) {
+                const int qb = c.it & 1;
+                const int nx = x ? c.nB : c.nA, nkv = c.n_kv();
+                if (!mbar_wait(q_full(qb), (c.it >> 1) & 1, a.err)) break;
+                const uint64_t dq = dq0 + (2 * qb) * kQStep;
+                // S of key tile 0
+                {
+                    const int st = gkv % kStages;
+                    if (!mbar_wait(k_full(st), (gkv / kStages) & 1, a.err)) break;
+                    if (nx > 0 && !issue_s(dq, dk0 + st * kStageStep)) break;
+                    tc_commit(k_empty(st));
+                    if (nx <= 1) tc_commit(q_empty(qb));
+                }
+                for (int j = 0; j < nkv; ++j) {
+                    const int gj = gkv + j;
+                    const int stj = gj % kStages;
+                    if (j + 1 < nkv) {
+                        // S of key tile j+1 ahead of PV of tile j
+                        const int stn = (gj + 1) % kStages;
+                        if (!mbar_wait(k_full(stn), ((gj + 1) / kStages) & 1, a.err)) {
+                            ok = false;
+                            break;
+                        }
+                        if (j + 1 < nx && !issue_s(dq, dk0 + stn * kStageStep)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_commit(k_empty(stn));
+                        if (j + 2 == nx) tc_commit(q_empty(qb));
+                    }
+                    if (!mbar_wait(v_full(stj), (gj / kStages) & 1, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j < nx && !issue_pv(dv0 + stj * kStageStep, j == 0)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_commit(v_empty(stj));
+                }
+                gkv += nkv;
+                if (nx > 0) ++itx;
+                c.next(a, nq, np, n_items);
+            }
+        }
+    } else if (warp >= 4) {
+        // softmax: warpgroup x = 0 (warps 4..7) for tile A, 1 (8..11) for B;
+        // warp w reads TMEM lanes 32 (w % 4) .. +31, one query row per thread
+        const int x = (warp - 4) >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem_base + 128u * x;
+        const uint32_t tO = tmem_base + Cfg::kColO + D * x;
+        const uint32_t tP = tmem_base + Cfg::kColP + 64u * x;
+        const float scale_l2 = a.scale * kLog2e;
+        PairCursor c;
+        c.start(a, nq, np, n_items);
+        int g = 0;  // key tiles processed (across items)
+        bool ok = true;
+        while (ok && c.valid) {
+            const int nx = x ? c.nB : c.nA;
+            if (nx == 0) {
+                c.next(a, nq, np, n_items);
+                continue;
+            }
+            const int qt = 2 * c.i + x;
+            const int qpos = qt * kTQ + row;
+            float m_used = -INFINITY;  // running max, log2 domain
+            float l = 0.f;
+            float slope_l2 = 0.f;
+            if constexpr (ALIBI) {
+                const float slope = a.slopes ? a.slopes[c.h]
+                                             : exp2f(-8.0f * static_cast<float>(c.h + 1) /
+                                                     static_cast<float>(a.H));
+                slope_l2 = slope * kLog2e;
+            }
+            for (int j = 0; j < nx; ++j, ++g) {
+                if (!mbar_wait(s_full(x), g & 1, a.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r[kTK];
+                tmem_ld128(tS + lane_off, r);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free(x));
+                const int kbase = j * kTK;
+                if constexpr (ALIBI) {
+                    const float sk = slope_l2 * static_cast<float>(kbase);
+#pragma unroll
+                    for (int i = 0; i < kTK; ++i)
+                        r[i] = __float_as_uint(fmaf(__uint_as_float(r[i]), scale_l2,
+                                                    fmaf(slope_l2, static_cast<float>(i), sk)));
+                }
+                if (j == qt || kbase + kTK > a.S) {
+                    const int lim = min(qpos, a.S - 1) - kbase;  // keys <= lim are visible
+#pragma unroll
+                    for (int i = 0; i < kTK; ++i)
+                        if (i > lim) r[i] = __float_as_uint(-INFINITY);
+                }
+                float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kTK; i += 8) {
+                    m0 = fmax3f(m0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                    m1 = fmax3f(m1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                    m2 = fmax3f(m2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                    m3 = fmax3f(m3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                }
+                float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+                if constexpr (!ALIBI) mx *= scale_l2;  // scale > 0: max commutes with it
+                float corr = 1.f;
+                if (mx > m_used + kRescaleThreshold) {
+                    corr = ex2_approx(m_used - mx);
+                    m_used = mx;
+                }
+                // the previous PV has read P_x and O_x is settled: rescale O
+                // if the max moved
+                if (j > 0) {
+                    if (!mbar_wait(pv_done(x), (g - 1) & 1, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+                        for (int cc = 0; cc < D / 16; ++cc) {
+                            uint32_t o[16];
+                            const uint32_t col = tO + lane_off + cc * 16;
+                            tmem_ld16(col, o);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                            tmem_st16_nowait(col, o);
+                        }
+                    }
+                }
+                // p = 2^(logit - m) in the storage type into P_x, 32 keys per
+                // store, and the row sum
+                const uint64_t mul2 = f2_pack(ALIBI ? 1.f : scale_l2, ALIBI ? 1.f : scale_l2);
+                const uint64_t neg2 = f2_pack(-m_used, -m_used);
+                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+                for (int cc = 0; cc < kTK / 32; ++cc) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const int k = cc * 32 + i;
+                        float e0, e1, e2, e3;
+                        ffma2(__uint_as_float(r[k]), __uint_as_float(r[k + 1]), mul2, neg2, e0,
+                              e1);
+                        ffma2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]), mul2, neg2,
+                              e2, e3);
+                        const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+                        const float p2 = ex2_approx(e2), p3 = ex2_approx(e3);
+                        fadd2_acc(acc0, p0, p1);
+                        fadd2_acc(acc1, p2, p3);
+                        pk[i / 2] = dt_traits<T>::pack2(p0, p1);
+                        pk[i / 2 + 1] = dt_traits<T>::pack2(p2, p3);
+                    }
+                    tmem_st16_nowait(tP + lane_off + cc * 16, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(x));
+                float s0, s1, s2, s3;
+                f2_unpack(acc0, s0, s1);
+                f2_unpack(acc1, s2, s3);
+                l = l * corr + ((s0 + s1) + (s2 + s3));
+            }
+            if (!ok) break;
+            // epilogue: O / l for this query tile
+            if (!mbar_wait(pv_done(x), (g - 1) & 1, a.err)) break;
+            tc_fence_after();
+            uint32_t o[D];
+            tmem_ld64(tO + lane_off, o);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free(x));
+            if (qpos < a.S) {
+                const float inv_l = 1.0f / l;
+                T* dst = static_cast<T*>(a.o) +
+                         ((static_cast<int64_t>(c.b) * a.S + qpos) * a.H + c.h) *
+                             static_cast<int64_t>(D);
+#pragma unroll
+                for (int v = 0; v < D / 8; ++v) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[v * 8 + e]) * inv_l;
+                    store8(dst + v * 8, f);
+                }
+            }
+            c.next(a, nq, np, n_items);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+template <typename T, bool ALIBI>
+cudaError_t launch_pair(DType dt, const AttnArgs& a, cudaStream_t s) {
+    constexpr int D = 64;
+    using Cfg = PairCfg<D>;
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_3d(&tq, dt, a.q, static_cast<uint64_t>(a.B) * a.H, a.S, D, kTQ) ||
+        !make_tmap_3d(&tk, dt, a.k, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kTK) ||
+        !make_tmap_3d(&tv, dt, a.v, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kTK))
+        return cudaErrorInvalidValue;
+    auto kern = attn_pair_kernel<T, D, ALIBI>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int64_t nq = (a.S + kTQ - 1) / kTQ;
+    const int64_t items = (nq + 1) / 2 * a.B * a.H;
+    if (items > 0x7fffffff) return cudaErrorInvalidValue;
+    const int64_t grid = items < a.num_sms ? items : a.num_sms;
+    kern<<<static_cast<unsigned>(grid), kPairThreads, Cfg::kSmem, s>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention_pair64(DType dt, const AttnArgs& a, cudaStream_t s) {
+    if (a.d != 64) return cudaErrorInvalidValue;
+    if (dt == DType::F16)
+        return a.alibi ? launch_pair<__half, true>(dt, a, s) : launch_pair<__half, false>(dt, a, s);
+    return a.alibi ? launch_pair<__nv_bfloat16, true>(dt, a, s)
+                   : launch_pair<__nv_bfloat16, false>(dt, a, s);
+}
+
+}  // namespace blk

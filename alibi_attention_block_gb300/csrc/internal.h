@@ -82,6 +82,8 @@ struct AttnArgs {
     int num_sms;          // persistent grid size
 };
 cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s);
+// head_dim 64: the paired-query-tile kernel (attn_pair.cu)
+cudaError_t launch_attention_pair64(DType dt, const AttnArgs& a, cudaStream_t s);
 
 // ---- per-device state and error reporting shared with other entry points (api.cu)
 // SM count and device error word of the current device (set up on first use).

@@ -270,6 +270,22 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
                           void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s,
                           void* const* events, int n_events, int32_t* step_kinds, int* n_launches);
 
+/* blk_forward on host buffers, with the copies overlapped with the compute.
+ * x_host and y_host are [batch, seq, hidden] in pinned host memory; x_dev and
+ * y_dev are device buffers of the same size (caller-owned, reused as
+ * staging); workspace holds at least blk_forward_workspace_size(d) bytes.
+ * The batch is split into n_chunks groups of whole sequences (1..16, at most
+ * batch): chunk c's host-to-device copy, forward and device-to-host copy run
+ * on two copy streams the library keeps per device and on s, so chunk c+1
+ * is copied in while chunk c is computed and chunk c-1 copied out. The call
+ * is ordered on s like any other: when s reaches the end of the call, y_host
+ * holds the result. Calls must not overlap on the GPU (they share x_dev, y_dev
+ * and the workspace). */
+blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
+                            const void* x_host, void* y_host, void* x_dev, void* y_dev,
+                            void* workspace, size_t ws_bytes, int32_t n_chunks, blk_dtype dt,
+                            blk_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

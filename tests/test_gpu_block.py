@@ -98,3 +98,52 @@ def test_block_full_size_sampled_rows(name):
     got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
     check(got, ref, f"{name} sampled rows", unit_scale=True, abs_tol=_abs_tol(cfg))
     assert torch.isfinite(y).all()
+
+
+@pytest.mark.parametrize("name,n_chunks", [("stablelm2_ragged_bf16", 2), ("olmo2_small", 1),
+                                           ("bloom_small", 16)])
+def test_forward_host_matches_device_forward(name, n_chunks):
+    """blk_forward_host (pinned host buffers, copies overlapped with compute
+    over groups of sequences) gives the device call's output bit for bit:
+    every kernel of the block is per token or per sequence, so splitting the
+    batch changes no arithmetic. n_chunks above the batch is clamped."""
+    cfg = SMALL[name]
+    x, w = workloads.block_inputs(cfg)
+    wd = {k: to_dev(t) for k, t in w.items()}
+    y_dev = blk.forward(cfg, wd, to_dev(x))
+    xh = x.pin_memory()
+    y_host = blk.forward_host(cfg, wd, xh, n_chunks=n_chunks)
+    torch.cuda.current_stream().synchronize()
+    blk.check_device_status()
+    assert torch.equal(y_host, y_dev.cpu())
+
+
+def test_forward_host_reuses_buffers_across_calls():
+    """Two calls in a row on the same staging buffers, with different inputs,
+    each return their own result (the second call's copies in wait for the
+    first call's reads on the stream)."""
+    cfg = SMALL["stablelm2_ragged_bf16"]
+    x, w = workloads.block_inputs(cfg)
+    wd = {k: to_dev(t) for k, t in w.items()}
+    x2 = (x.double() * -0.5).to(x.dtype)
+    dev = torch.device("cuda")
+    xd, yd = torch.empty_like(x, device=dev), torch.empty_like(x, device=dev)
+    ws = torch.empty(blk.forward_workspace_size(cfg, *x.shape[:2]), dtype=torch.uint8, device=dev)
+    xh1, xh2 = x.pin_memory(), x2.pin_memory()  # held until the copies have run
+    y1 = blk.forward_host(cfg, wd, xh1, x_dev=xd, y_dev=yd, workspace=ws)
+    y2 = blk.forward_host(cfg, wd, xh2, x_dev=xd, y_dev=yd, workspace=ws)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(y1, blk.forward(cfg, wd, to_dev(x)).cpu())
+    assert torch.equal(y2, blk.forward(cfg, wd, to_dev(x2)).cpu())
+
+
+def test_forward_host_rejects_bad_arguments():
+    cfg = SMALL["tiny_stablelm2"]
+    x, w = workloads.block_inputs(cfg)
+    wd = {k: to_dev(t) for k, t in w.items()}
+    with pytest.raises(ValueError):
+        blk.forward_host(cfg, wd, x)  # pageable host memory
+    with pytest.raises(blk.BlkError):
+        blk.forward_host(cfg, wd, x.pin_memory(), n_chunks=0)
+    with pytest.raises(blk.BlkError):
+        blk.forward_host(cfg, wd, x.pin_memory(), n_chunks=17)

@@ -191,6 +191,10 @@ ATTN_CASES = [
     (2, 4, 4, 200, 64, False),
     (1, 4, 2, 1000, 64, False),
     (2, 4, 4, 384, 64, True),
+    (1, 2, 2, 1, 64, False),
+    (1, 3, 3, 640, 64, False),     # odd tile count: the last pair has one query tile
+    (1, 2, 2, 129, 64, True),      # second query tile of one row
+    (4, 16, 4, 1152, 64, False),   # more items than SMs: several items per CTA
     (1, 2, 2, 333, 128, False),
     (1, 4, 4, 256, 128, True),
     (1, 4, 1, 300, 160, False),
@@ -210,6 +214,21 @@ def test_attention(dt, case):
     ref = oracle.attention(f64(q), f64(k), f64(v), slopes=oracle.alibi_slopes(H) if alibi else None)
     # outputs are convex combinations of unit-scale value rows: unit scale
     check(o, ref.transpose(0, 2, 1, 3), f"attention {case}", unit_scale=True)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_attention_growing_logits_rescale(d):
+    """Keys scaled up along the sequence make the running row max grow tile
+    after tile, so O is rescaled in flight many times."""
+    B, H, S = 1, 2, 900
+    q = draw((B, H, S, d), "bf16", 70 + d)
+    k = draw((B, H, S, d), "bf16", 71 + d)
+    v = draw((B, H, S, d), "bf16", 72 + d)
+    ramp = (1.0 + torch.arange(S, dtype=torch.float64) / 48.0).view(1, 1, S, 1)
+    k = (k.double() * ramp).to(torch.bfloat16)
+    o = blk.attn_prefill(to_dev(q), to_dev(k), to_dev(v))
+    ref = oracle.attention(f64(q), f64(k), f64(v))
+    check(o, ref.transpose(0, 2, 1, 3), f"attention growing logits d={d}", unit_scale=True)
 
 
 def test_attention_explicit_slopes_and_scale():
