@@ -37,10 +37,9 @@
 //               (scale log2(e)/sqrt(d) folded in; for ALiBi the bias
 //               -slope*(i-j), "Bloom in a sovereign engine", Contribution,
 //               enters as +slope*j, the -slope*i part being constant along
-//               the row), P rounded to the storage type and written to this
-//               tile's P columns in TMEM (after the previous PV has read them;
-//               in steady state that PV ends while S is being read and the
-//               max taken, since the tensor core runs the other tile between).
+//               the row), P rounded to the storage type and held in
+//               registers until the previous PV has read this tile's P
+//               columns in TMEM, so the exponentials overlap that PV.
 //               O is rescaled in TMEM only when the running max
 //               grows by more than 2^8. At the end of an item O / l is read
 //               out of TMEM and written as [B, S, H, d].
@@ -61,6 +60,9 @@ constexpr int kTQ = 128;  // query rows per tile
 constexpr int kTK = 128;  // keys per tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest unnormalised p
+// per-thread registers: at launch (65536 / 384, rounded down to a multiple of
+// 8), and after the split for warpgroup 0 and for the softmax warpgroups
+constexpr uint32_t kLaunchRegs = 168, kRegsControl = 64, kRegsSoftmax = 208;
 
 template <int D>
 struct PairCfg {
@@ -176,7 +178,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
+    // registers: the launch gives every thread kLaunchRegs; warpgroup 0 (TMA,
+    // MMA issue) gives most of its share to the two softmax warpgroups, which
+    // hold a row's 128 scores and 64 packed probabilities at once
+    static_assert(4 * kRegsControl + 8 * kRegsSoftmax <= 12 * kLaunchRegs,
+                  "register split exceeds the launch's registers");
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsControl>();
     if (warp == 0) {
         if (lane == 0) {
             PairCursor c;
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             bool ok = true;
             while (ok && c.valid) {
                 const int qb = c.it & 1;
-                if (!mbar_wait(q_empty(qb), ((c.it >> 1) & 1) ^ 1u, a.err)) break;
+                if (!mbar_wait_inl(q_empty(qb), ((c.it >> 1) & 1) ^ 1u, a.err)) break;
                 mbar_expect_tx(q_full(qb), (c.nB ? 2 : 1) * Cfg::kQBytes);
                 for (int x = 0; x < (c.nB ? 2 : 1); ++x) {
 #pragma unroll
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     const int st = gkv % kStages;
                     const uint32_t ph = (gkv / kStages) & 1;
                     const uint32_t sK = sKV + (2 * st) * Cfg::kKVBytes;
-                    if (!mbar_wait(k_empty(st), ph ^ 1u, a.err)) {
+                    if (!mbar_wait_inl(k_empty(st), ph ^ 1u, a.err)) {
                         ok = false;
                         break;
                     }
@@ -207,7 +215,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
                         tma_load_3d(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
                                     c.b * a.Hk + c.g);
-                    if (!mbar_wait(v_empty(st), ph ^ 1u, a.err)) {
+                    if (!mbar_wait_inl(v_empty(st), ph ^ 1u, a.err)) {
                         ok = false;
                         break;
                     }
@@ -242,7 +250,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             int gs = 0, gp = 0, itx = 0;  // S and PV tiles issued, items with this tile
             // S_x = Q_x K^T, once the softmax has read the previous S_x
             auto issue_s = [&](uint64_t dq, uint64_t dk) -> bool {
-                if (gs > 0 && !mbar_wait(s_free(x), (gs - 1) & 1, a.err)) return false;
+                if (gs > 0 && !mbar_wait_inl(s_free(x), (gs - 1) & 1, a.err)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
@@ -256,8 +264,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // O_x += P_x V once the softmax has written P_x (the first PV of an
             // item overwrites O_x, so it also waits for the previous read-out)
             auto issue_pv = [&](uint64_t dv, bool first) -> bool {
-                if (!mbar_wait(p_full(x), gp & 1, a.err)) return false;
-                if (first && itx > 0 && !mbar_wait(o_free(x), (itx - 1) & 1, a.err)) return false;
+                if (!mbar_wait_inl(p_full(x), gp & 1, a.err)) return false;
+                if (first && itx > 0 && !mbar_wait_inl(o_free(x), (itx - 1) & 1, a.err)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < kTK / 16; ++ks)
@@ -274,12 +282,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             while (ok && c.valid) {
                 const int qb = c.it & 1;
                 const int nx = x ? c.nB : c.nA, nkv = c.n_kv();
-                if (!mbar_wait(q_full(qb), (c.it >> 1) & 1, a.err)) break;
+                if (!mbar_wait_inl(q_full(qb), (c.it >> 1) & 1, a.err)) break;
                 const uint64_t dq = dq0 + (2 * qb) * kQStep;
                 // S of key tile 0
                 {
                     const int st = gkv % kStages;
-                    if (!mbar_wait(k_full(st), (gkv / kStages) & 1, a.err)) break;
+                    if (!mbar_wait_inl(k_full(st), (gkv / kStages) & 1, a.err)) break;
                     if (nx > 0 && !issue_s(dq, dk0 + st * kStageStep)) break;
                     tc_commit(k_empty(st));
                     if (nx <= 1) tc_commit(q_empty(qb));
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     if (j + 1 < nkv) {
                         // S of key tile j+1 ahead of PV of tile j
                         const int stn = (gj + 1) % kStages;
-                        if (!mbar_wait(k_full(stn), ((gj + 1) / kStages) & 1, a.err)) {
+                        if (!mbar_wait_inl(k_full(stn), ((gj + 1) / kStages) & 1, a.err)) {
                             ok = false;
                             break;
                         }
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         tc_commit(k_empty(stn));
                         if (j + 2 == nx) tc_commit(q_empty(qb));
                     }
-                    if (!mbar_wait(v_full(stj), (gj / kStages) & 1, a.err)) {
+                    if (!mbar_wait_inl(v_full(stj), (gj / kStages) & 1, a.err)) {
                         ok = false;
                         break;
                     }
@@ -316,7 +324,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 c.next(a, nq, np, n_items);
             }
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        setmaxnreg_inc<kRegsSoftmax>();
         // softmax: warpgroup x = 0 (warps 4..7) for tile A, 1 (8..11) for B;
         // warp w reads TMEM lanes 32 (w % 4) .. +31, one query row per thread
         const int x = (warp - 4) >> 2;
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 slope_l2 = slope * kLog2e;
             }
             for (int j = 0; j < nx; ++j, ++g) {
-                if (!mbar_wait(s_full(x), g & 1, a.err)) {
+                if (!mbar_wait_inl(s_full(x), g & 1, a.err)) {
                     ok = false;
                     break;
                 }
@@ -388,51 +398,46 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     corr = ex2_approx(m_used - mx);
                     m_used = mx;
                 }
-                // the previous PV has read P_x and O_x is settled: rescale O
-                // if the max moved
+                // p = 2^(logit - m) in the storage type, and the row sum; P is
+                // held in registers until the previous PV has read P_x
+                const uint64_t mul2 = f2_pack(ALIBI ? 1.f : scale_l2, ALIBI ? 1.f : scale_l2);
+                const uint64_t neg2 = f2_pack(-m_used, -m_used);
+                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+                uint32_t pk[kTK / 2];
+#pragma unroll
+                for (int k = 0; k < kTK; k += 4) {
+                    float e0, e1, e2, e3;
+                    ffma2(__uint_as_float(r[k]), __uint_as_float(r[k + 1]), mul2, neg2, e0, e1);
+                    ffma2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]), mul2, neg2, e2,
+                          e3);
+                    const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+                    const float p2 = ex2_approx(e2), p3 = ex2_approx(e3);
+                    fadd2_acc(acc0, p0, p1);
+                    fadd2_acc(acc1, p2, p3);
+                    pk[k / 2] = dt_traits<T>::pack2(p0, p1);
+                    pk[k / 2 + 1] = dt_traits<T>::pack2(p2, p3);
+                }
+                // the previous PV has read P_x and O_x is settled: publish P_x,
+                // then rescale O if the max moved (before this tile's PV)
                 if (j > 0) {
-                    if (!mbar_wait(pv_done(x), (g - 1) & 1, a.err)) {
+                    if (!mbar_wait_inl(pv_done(x), (g - 1) & 1, a.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll 1
-                        for (int cc = 0; cc < D / 16; ++cc) {
-                            uint32_t o[16];
-                            const uint32_t col = tO + lane_off + cc * 16;
-                            tmem_ld16(col, o);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-                            tmem_st16_nowait(col, o);
-                        }
-                    }
                 }
-                // p = 2^(logit - m) in the storage type into P_x, 32 keys per
-                // store, and the row sum
-                const uint64_t mul2 = f2_pack(ALIBI ? 1.f : scale_l2, ALIBI ? 1.f : scale_l2);
-                const uint64_t neg2 = f2_pack(-m_used, -m_used);
-                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+                tmem_st64_nowait(tP + lane_off, pk);
+                if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 16; ++cc) {
+                        uint32_t o[16];
+                        const uint32_t col = tO + lane_off + cc * 16;
+                        tmem_ld16(col, o);
 #pragma unroll
-                for (int cc = 0; cc < kTK / 32; ++cc) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const int k = cc * 32 + i;
-                        float e0, e1, e2, e3;
-                        ffma2(__uint_as_float(r[k]), __uint_as_float(r[k + 1]), mul2, neg2, e0,
-                              e1);
-                        ffma2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]), mul2, neg2,
-                              e2, e3);
-                        const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-                        const float p2 = ex2_approx(e2), p3 = ex2_approx(e3);
-                        fadd2_acc(acc0, p0, p1);
-                        fadd2_acc(acc1, p2, p3);
-                        pk[i / 2] = dt_traits<T>::pack2(p0, p1);
-                        pk[i / 2 + 1] = dt_traits<T>::pack2(p2, p3);
+                        for (int i = 0; i < 16; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        tmem_st16_nowait(col, o);
                     }
-                    tmem_st16_nowait(tP + lane_off + cc * 16, pk);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
             if (!ok) break;
             // epilogue: O / l for this query tile
-            if (!mbar_wait(pv_done(x), (g - 1) & 1, a.err)) break;
+            if (!mbar_wait_inl(pv_done(x), (g - 1) & 1, a.err)) break;
             tc_fence_after();
             uint32_t o[D];
             tmem_ld64(tO + lane_off, o);

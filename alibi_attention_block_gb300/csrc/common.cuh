@@ -134,6 +134,16 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Per-warpgroup register budget (every warp of the warpgroup executes the
+// same instruction; the increases of a block must be covered by its decreases).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 // One 16-byte shared-memory store at a shared-window address.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -166,6 +176,20 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) {
+            report_error(err, DEV_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+// The same wait with the slow path inlined: for kernels that change their
+// register budget per warpgroup (setmaxnreg), where a call to a function
+// compiled for the launch's register count is not allowed.
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity, unsigned* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
             report_error(err, DEV_ERR_TIMEOUT);
             return false;
         }
