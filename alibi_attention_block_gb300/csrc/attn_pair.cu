@@ -41,8 +41,9 @@
 //               registers until the previous PV has read this tile's P
 //               columns in TMEM, so the exponentials overlap that PV.
 //               O is rescaled in TMEM only when the running max
-//               grows by more than 2^8. At the end of an item O / l is read
-//               out of TMEM and written as [B, S, H, d].
+//               grows by more than 2^8. An item's O / l is read out of TMEM
+//               and written as [B, S, H, d] during the first tile of the
+//               warpgroup's next item, so no softmax waits on a last PV.
 // TMEM columns: S_A [0, 128), S_B [128, 256), P_A [256, 320), P_B [320, 384)
 // (two 16-bit values per column), O_A [384, 448), O_B [448, 512).
 // Items are (query-tile pair, batch, head), heaviest pairs first, dealt to
@@ -341,6 +342,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         c.start(a, nq, np, n_items);
         int g = 0;  // key tiles processed (across items)
         bool ok = true;
+        // The read-out of an item's O waits for its last PV; it is deferred to
+        // the first tile of this warpgroup's next item (after that tile's
+        // exponentials), so the next item's softmax overlaps the last PV.
+        bool pend = false;  // an item's O is still in TMEM
+        float pend_l = 0.f;
+        int64_t pend_row = -1;  // output row (b * S + qpos) * H + h, or -1 past S
         while (ok && c.valid) {
             const int nx = x ? c.nB : c.nA;
             if (nx == 0) {
@@ -417,14 +424,34 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     pk[k / 2] = dt_traits<T>::pack2(p0, p1);
                     pk[k / 2 + 1] = dt_traits<T>::pack2(p2, p3);
                 }
-                // the previous PV has read P_x and O_x is settled: publish P_x,
-                // then rescale O if the max moved (before this tile's PV)
-                if (j > 0) {
+                // the previous PV has read P_x and O_x is settled: read out the
+                // previous item's O if pending, publish P_x, then rescale O if
+                // the max moved (before this tile's PV)
+                if (j > 0 || pend) {
                     if (!mbar_wait_inl(pv_done(x), (g - 1) & 1, a.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                }
+                if (j == 0 && pend) {
+                    uint32_t o[D];
+                    tmem_ld64(tO + lane_off, o);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(o_free(x));
+                    if (pend_row >= 0) {
+                        const float inv_l = 1.0f / pend_l;
+                        T* dst = static_cast<T*>(a.o) + pend_row * static_cast<int64_t>(D);
+#pragma unroll
+                        for (int v = 0; v < D / 8; ++v) {
+                            float f[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[v * 8 + e]) * inv_l;
+                            store8(dst + v * 8, f);
+                        }
+                    }
+                    pend = false;
                 }
                 tmem_st64_nowait(tP + lane_off, pk);
                 if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
@@ -449,19 +476,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 l = l * corr + ((s0 + s1) + (s2 + s3));
             }
             if (!ok) break;
-            // epilogue: O / l for this query tile
-            if (!mbar_wait_inl(pv_done(x), (g - 1) & 1, a.err)) break;
+            pend = true;
+            pend_l = l;
+            pend_row = qpos < a.S ? (static_cast<int64_t>(c.b) * a.S + qpos) * a.H + c.h : -1;
+            c.next(a, nq, np, n_items);
+        }
+        // the last item's O
+        if (ok && pend && mbar_wait_inl(pv_done(x), (g - 1) & 1, a.err)) {
             tc_fence_after();
             uint32_t o[D];
             tmem_ld64(tO + lane_off, o);
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_free(x));
-            if (qpos < a.S) {
-                const float inv_l = 1.0f / l;
-                T* dst = static_cast<T*>(a.o) +
-                         ((static_cast<int64_t>(c.b) * a.S + qpos) * a.H + c.h) *
-                             static_cast<int64_t>(D);
+            if (pend_row >= 0) {
+                const float inv_l = 1.0f / pend_l;
+                T* dst = static_cast<T*>(a.o) + pend_row * static_cast<int64_t>(D);
 #pragma unroll
                 for (int v = 0; v < D / 8; ++v) {
                     float f[8];
@@ -470,7 +498,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     store8(dst + v * 8, f);
                 }
             }
-            c.next(a, nq, np, n_items);
         }
     }
     __syncthreads();
