@@ -9,7 +9,9 @@
 //               instruction, fp32 accumulators in TMEM, double-buffered so
 //               the epilogue of tile i overlaps the mainloop of tile i+1
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per load (one
-//               thread per output row), fused op, 16-byte global stores
+//               thread per output row), fused op, 16-byte global stores per
+//               row; fp32 outputs go through 4 KB of shared memory per warp
+//               so that each store instruction writes whole lines
 // Epilogues (the block's steps after each projection):
 //   EPI_LINEAR  + bias, + up to two residuals (o_proj and down_proj residual
 //               adds); residuals and output may be fp32 (the block keeps its
@@ -38,7 +40,8 @@ struct GemmCfg {
     static constexpr int kBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmem = kStages * kStageBytes + 1024 + kBarBytes;
+    static constexpr int kEpiBytes = 4 * 32 * 128;  // per epilogue warp: 32 rows x 32 fp32
+    static constexpr int kSmem = kStages * kStageBytes + 1024 + kBarBytes + kEpiBytes;
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 };
 
@@ -68,6 +71,34 @@ __device__ __forceinline__ void add_row32(const T* src, float (&o)[32], int vali
     }
 }
 
+// fp32 write-out of a warp's 32 output rows x 32 columns, held one row per
+// thread (the TMEM lane layout): staged through the warp's 4 KB of shared
+// memory (16-byte chunks XOR-swizzled by row, conflict-free both ways), then
+// stored 4 rows x 128 bytes per instruction, whole lines instead of 16 bytes
+// of each of 32 rows (half-sector writes). Storage-type rows (64 bytes per
+// chunk) are stored directly: there the staging only lengthens the epilogue.
+__device__ __forceinline__ void store_chunk_f32(const GemmArgs& g, uint32_t stg, int lane,
+                                                int m_base, int n0, const float (&o)[32]) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        st_shared_v4(stg + lane * 128 + ((v ^ (lane & 7)) << 4), __float_as_uint(o[4 * v]),
+                     __float_as_uint(o[4 * v + 1]), __float_as_uint(o[4 * v + 2]),
+                     __float_as_uint(o[4 * v + 3]));
+    __syncwarp();
+    const int cq = lane & 7;       // columns 4 cq .. 4 cq + 3 of the chunk
+    const int gcol = n0 + cq * 4;  // N % 8 == 0: four columns are all valid or none
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int rr = p * 4 + (lane >> 3);
+        const float4 v = ld_shared_v4(stg + rr * 128 + ((cq ^ (rr & 7)) << 4));
+        const int grow = m_base + rr;
+        if (grow < g.M && gcol < g.N)
+            *reinterpret_cast<float4*>(static_cast<float*>(g.out) +
+                                       static_cast<int64_t>(grow) * g.N + gcol) = v;
+    }
+    __syncwarp();
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
 __device__ __forceinline__ float gelu_tanh_f(float z) {
@@ -77,7 +108,8 @@ __device__ __forceinline__ float gelu_tanh_f(float z) {
 
 template <typename T, int BN, int EPI, int ROT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParams& rp,
-                                              uint32_t tbase, int m, int nt) {
+                                              uint32_t tbase, int m, int nt, uint32_t stg,
+                                              int lane, int m_base) {
     const bool row_ok = m < g.M;
     if constexpr (EPI == EPI_SWIGLU) {
         constexpr int kHalf = BN / 2;
@@ -146,7 +178,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             uint32_t r[32];
             tmem_ld32(tbase + c * 32, r);
             const int n0 = nt * BN + c * 32;
-            if (!row_ok || n0 >= g.N) continue;
+            if (n0 >= g.N) continue;  // uniform across the warp
             const int valid = g.N - n0;
             float o[32];
 #pragma unroll
@@ -157,16 +189,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
             }
             const int64_t off = static_cast<int64_t>(m) * g.N + n0;
-            if (g.res1) {
+            if (row_ok && g.res1) {
                 if (g.res1_f32) add_row32(static_cast<const float*>(g.res1) + off, o, valid);
                 else add_row32(static_cast<const T*>(g.res1) + off, o, valid);
             }
-            if (g.res2) {
+            if (row_ok && g.res2) {
                 if (g.res2_f32) add_row32(static_cast<const float*>(g.res2) + off, o, valid);
                 else add_row32(static_cast<const T*>(g.res2) + off, o, valid);
             }
-            if (g.out_f32) store_row32(static_cast<float*>(g.out) + off, o, valid);
-            else store_row32(static_cast<T*>(g.out) + off, o, valid);
+            if (g.out_f32)
+                store_chunk_f32(g, stg, lane, m_base, n0, o);  // all lanes (rows checked inside)
+            else if (row_ok)
+                store_row32(static_cast<T*>(g.out) + off, o, valid);
         }
     }
 }
@@ -225,7 +259,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int m_tiles = (g.M + kBM - 1) / kBM;
     const int n_tiles = (g.N + kBNOut - 1) / kBNOut;
-    // work units: single tiles, or vertical pairs of tiles for a cluster
+    // work units: single tiles, or vertical pairs of tiles for a cluster,
+    // numbered M-fastest (the CTAs running at any time share a few columns
+    // of B and all of A stays in L2) or, when A is too large to stay in L2,
+    // N-fastest (they share rows of A, read from DRAM once; B stays in L2)
     const int m_units = (m_tiles + CL - 1) / CL;
     const int num_units = m_units * n_tiles;
     const int unit0 = static_cast<int>(blockIdx.x) / CL;
@@ -237,7 +274,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int u = unit0; u < num_units && ok; u += unit_step) {
-                const int mt = (u % m_units) * CL + rank, nt = u / m_units;
+                const int mt = (g.n_fastest ? u / n_tiles : u % m_units) * CL + rank;
+                const int nt = g.n_fastest ? u % n_tiles : u / m_units;
                 for (int kb = 0; kb < kb_count; ++kb) {
                     if (!mbar_wait(empty(stage), phase ^ 1u, g.err)) {
                         ok = false;
@@ -310,16 +348,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else {
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        const uint32_t stg0 = smem_u32(smem) + kStages * Cfg::kStageBytes + Cfg::kBarBytes;
         int it = 0;
         for (int u = unit0; u < num_units; u += unit_step, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!mbar_wait(tfull(acc), acc_phase, g.err)) break;
             tc_fence_after();
-            const int mt = (u % m_units) * CL + rank, nt = u / m_units;
+            const int mt = (g.n_fastest ? u / n_tiles : u % m_units) * CL + rank;
+            const int nt = g.n_fastest ? u % n_tiles : u / m_units;
             const uint32_t tbase =
                 tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            epilogue_tile<T, BN, EPI, ROT>(g, rp, tbase, mt * kBM + row, nt);
+            epilogue_tile<T, BN, EPI, ROT>(g, rp, tbase, mt * kBM + row, nt,
+                                           stg0 + quarter * (32 * 128), lane,
+                                           mt * kBM + quarter * 32);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(acc));
@@ -420,8 +462,14 @@ cudaError_t launch_t(DType dt, int epi, const void* a, const void* b, const void
 cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const void* b2,
                         const GemmArgs& args, const RopeParams& rp, int num_sms, cudaStream_t s) {
     if (args.M == 0 || args.N == 0) return cudaSuccess;
-    if (dt == DType::F16) return launch_t<__half>(dt, epi, a, b, b2, args, rp, num_sms, s);
-    return launch_t<__nv_bfloat16>(dt, epi, a, b, b2, args, rp, num_sms, s);
+    // N-fastest units when A alone would take more than about a third of L2
+    // and is the larger operand (B rows: N, or 2N for gate + up)
+    GemmArgs g = args;
+    const double a_bytes = 2.0 * args.M * args.K;
+    const double b_bytes = 2.0 * args.N * args.K * (epi == EPI_SWIGLU ? 2 : 1);
+    g.n_fastest = a_bytes > 48.0 * (1 << 20) && a_bytes > b_bytes;
+    if (dt == DType::F16) return launch_t<__half>(dt, epi, a, b, b2, g, rp, num_sms, s);
+    return launch_t<__nv_bfloat16>(dt, epi, a, b, b2, g, rp, num_sms, s);
 }
 
 }  // namespace blk

@@ -63,6 +63,7 @@ struct GemmArgs {
     void* v;
     int S, H, Hk, d, interleaved;
     unsigned* err;
+    int n_fastest;        // work-unit order (set by launch_gemm)
 };
 // a: [M, K]; b: [N(or N rows of gate), K]; b2: up weights for SWIGLU.
 cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const void* b2,

@@ -81,14 +81,16 @@ def step_work(cfg):
 
 # ------------------------------------------------------------------ clocks --
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    """nvidia-smi sampled every 50 ms; only samples whose timestamps fall
+    inside the timed region (mark_start / mark_end) are summarised."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
         self.proc = None
+        self.t0 = self.t1 = None
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -96,7 +98,7 @@ class ClockSampler:
         except Exception:
             sel = ["-i", str(device_index)]
         self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                    "-lms", "100", *sel]
+                    "-lms", "50", *sel]
 
     def __enter__(self):
         try:
@@ -106,6 +108,12 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
         if self.proc:
             self.proc.terminate()
@@ -114,23 +122,40 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    @staticmethod
+    def _epoch(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         self.out.flush()
-        rows = []
+        rows, outside = [], 0
         for line in open(self.out.name):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) == 7:
-                try:
-                    rows.append((float(parts[0]), float(parts[1]), parts[3:]))
-                except ValueError:
-                    pass
+            if len(parts) != 8:
+                continue
+            t = self._epoch(parts[0])
+            try:
+                row = (float(parts[1]), float(parts[2]), float(parts[3]), parts[4:])
+            except ValueError:
+                continue
+            if t is not None and self.t0 is not None and not (self.t0 <= t <= self.t1):
+                outside += 1
+                continue
+            rows.append(row)
         os.unlink(self.out.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        reasons = sorted({names[i] for *_, r in rows for i, v in enumerate(r) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "power_w": statistics.median(r[2] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_outside_timed_region": outside}
 
 
 # ------------------------------------------------------- standalone kernels --
@@ -312,12 +337,14 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        clk.mark_start()
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
             one_step(evs[i])
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
+        clk.mark_end()
     if dist:
         dist.barrier()
     blk.check_device_status()
@@ -430,7 +457,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="stablelm2_1p6b", choices=sorted(workloads.BLOCK_CONFIGS))
