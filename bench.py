@@ -37,6 +37,34 @@ import workloads  # noqa: E402
 METRIC = "prefill tokens/s per block and attention TFLOP/s (% of GB300 FP16 peak) at 1 GPU"
 
 
+# DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum, one
+# capture of the default workload) for the kernels that can be the roofline's
+# dominant one, with the SHA-256 of the sources the kernel was built from when
+# the counters were taken: a kernel changed since then reports null.
+_KERNEL_SOURCES = {
+    "gemm": ("alibi_attention_block_gb300/csrc/gemm.cu", "alibi_attention_block_gb300/csrc/common.cuh",
+             "alibi_attention_block_gb300/csrc/internal.h"),
+}
+NCU_TRAFFIC = {}
+
+
+def _sources_sha(kind: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for rel in _KERNEL_SOURCES[kind]:
+        with open(os.path.join(root, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic(step: str):
+    ent = NCU_TRAFFIC.get(step)
+    if not ent or _sources_sha(ent["kind"]) != ent["sha256"]:
+        return None
+    return ent["bytes"]
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -404,12 +432,12 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops_sustained"],
-                "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "traffic": None,
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "traffic": _traffic(dom),
                 "peak_source": peaks["source"] + " sustained bf16"}
     else:
         achieved = dw["bytes"] / (kernel_ms[dom] / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(dom),
                 "peak_source": peaks["source"] + " copy"}
     kernels = {}
     for k, ms in kernel_ms.items():
