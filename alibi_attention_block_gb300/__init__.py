@@ -21,7 +21,7 @@ from . import _abi
 from ._abi import BlkError  # noqa: F401
 
 __all__ = ["layernorm_bias", "rmsnorm", "qkv_bias_rope_partial", "rope_inplace", "attn_prefill",
-           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host",
+           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host", "ForwardGraph",
            "check_device_status", "BlkError", "library_path"]
 
 library_path = _abi.LIB_PATH
@@ -244,6 +244,58 @@ def forward_host(cfg, weights: dict, x_host, y_host=None, x_dev=None, y_dev=None
                                        _p(workspace), workspace.numel(), n_chunks, _dt(x_host),
                                        _stream()), "blk_forward_host")
     return y_host
+
+
+class ForwardGraph:
+    """The block forward recorded once as a CUDA graph (blk_forward_graph_create)
+    for fixed tensors x, y, workspace and weights; launch() replays it on the
+    current stream. The tensors must stay alive while the graph is used."""
+
+    def __init__(self, cfg, weights: dict, x, y, workspace, events=None):
+        B, S, _ = x.shape
+        self._keep = (weights, x, y, workspace)
+        self.desc = block_desc(cfg, B, S)
+        unknown = set(weights) - set(_abi.WEIGHT_SLOTS)
+        if unknown:
+            raise KeyError(f"unknown weight slots: {sorted(unknown)}")
+        for name, t in weights.items():
+            if name != "alibi_slopes":
+                _same(x, t)
+        _same(x, y)
+        self.w = _abi.BlockWeights(*[_p(weights.get(n)) for n in _abi.WEIGHT_SLOTS])
+        ev = None
+        n_ev = 0
+        if events:
+            ev = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+            n_ev = len(events)
+        self.kinds = (C.c_int32 * 10)()
+        self.n_launches = C.c_int(0)
+        handle = C.c_void_p()
+        _abi.check(_lib().blk_forward_graph_create(C.byref(self.desc), C.byref(self.w), _p(x), _p(y),
+                                                   _p(workspace), workspace.numel(), _dt(x), ev,
+                                                   n_ev, self.kinds, C.byref(self.n_launches),
+                                                   C.byref(handle)), "blk_forward_graph_create")
+        self._h = handle
+
+    def launch(self, events=None):
+        """Replay on the current stream; events (torch.cuda.Event, created) replace
+        the recorded ones for this and later launches."""
+        if events is not None:
+            arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+            _abi.check(_lib().blk_graph_set_events(self._h, arr, len(events)),
+                       "blk_graph_set_events")
+        _abi.check(_lib().blk_graph_launch(self._h, _stream()), "blk_graph_launch")
+
+    def close(self):
+        if self._h:
+            _abi.check(_lib().blk_graph_destroy(self._h), "blk_graph_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def check_device_status():

@@ -78,6 +78,12 @@ _PROTOS = {
     "blk_forward_workspace_size": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(C.c_size_t)]),
     "blk_forward": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp,
                               C.c_size_t, C.c_int, vp]),
+    "blk_forward_graph_create": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp,
+                                           vp, C.c_size_t, C.c_int, C.POINTER(vp), C.c_int,
+                                           C.POINTER(i32), C.POINTER(C.c_int), C.POINTER(vp)]),
+    "blk_graph_launch": (C.c_int, [vp, vp]),
+    "blk_graph_set_events": (C.c_int, [vp, C.POINTER(vp), C.c_int]),
+    "blk_graph_destroy": (C.c_int, [vp]),
     "blk_forward_host": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp, vp,
                                    vp, C.c_size_t, i32, C.c_int, vp]),
     "blk_forward_ex": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp,

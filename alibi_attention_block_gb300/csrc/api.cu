@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <string>
 
 #include "blk.h"
@@ -367,20 +368,29 @@ struct StepLog {
     int* n_out;
     cudaStream_t s;
     int n = 0;
+    bool capturing = false;
+    // under stream capture an event record becomes a graph node only when
+    // recorded as external
+    blk_status record(int i) {
+        cudaEvent_t ev = static_cast<cudaEvent_t>(events[i]);
+        cudaError_t e = capturing ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                  : cudaEventRecord(ev, s);
+        return e == cudaSuccess ? BLK_OK : cuda_fail(e, "cudaEventRecord");
+    }
     blk_status begin() {
         if (events && n_events > 0) {
-            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[0]), s);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+            cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+            cudaError_t e = cudaStreamIsCapturing(s, &cst);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+            capturing = cst == cudaStreamCaptureStatusActive;
+            return record(0);
         }
         return BLK_OK;
     }
     blk_status step(int kind) {
         if (kinds && n < 10 && n + 1 < (n_events > 0 ? n_events : 11)) kinds[n] = kind;
         ++n;
-        if (events && n < n_events) {
-            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[n]), s);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
-        }
+        if (events && n < n_events) return record(n);
         return BLK_OK;
     }
     blk_status end() {
@@ -917,6 +927,105 @@ blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
     e = cudaEventRecord(ds->ev_done, ds->copy_out);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ds->ev_done, 0);
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "stream ordering");
+}
+
+constexpr int kMaxForwardEvents = 16;
+struct blk_graph {
+    cudaGraphExec_t exec = nullptr;
+    cudaGraph_t graph = nullptr;  // kept for the event-node handles
+    int device = -1;
+    int n_events = 0;
+    cudaGraphNode_t ev_nodes[kMaxForwardEvents] = {};
+};
+
+blk_status blk_forward_graph_create(const blk_block_desc* d, const blk_block_weights* w,
+                                    const void* x, void* y, void* workspace, size_t ws_bytes,
+                                    blk_dtype dt, void* const* events, int n_events,
+                                    int32_t* step_kinds, int* n_launches, blk_graph** out) {
+    BLK_REQUIRE(out != nullptr, "out is NULL");
+    *out = nullptr;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaStream_t cs = nullptr;
+    if ((e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e, "stream for capture");
+    if ((e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal)) != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return cuda_fail(e, "cudaStreamBeginCapture");
+    }
+    blk_status st = blk_forward_ex(d, w, x, y, workspace, ws_bytes, dt,
+                                   reinterpret_cast<blk_stream_t>(cs), events, n_events,
+                                   step_kinds, n_launches);
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(cs, &graph);
+    cudaStreamDestroy(cs);
+    if (st != BLK_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+    blk_graph* g = new (std::nothrow) blk_graph;
+    if (!g) {
+        cudaGraphDestroy(graph);
+        return fail(BLK_EINVAL, "out of host memory");
+    }
+    g->graph = graph;
+    g->device = dev;
+    // the capture of one stream is a chain: walk it from its root and keep
+    // the event-record nodes in recording order
+    size_t n_nodes = 0;
+    e = cudaGraphGetRootNodes(graph, nullptr, &n_nodes);
+    cudaGraphNode_t node = nullptr;
+    if (e == cudaSuccess && n_nodes == 1) e = cudaGraphGetRootNodes(graph, &node, &n_nodes);
+    while (e == cudaSuccess && node) {
+        cudaGraphNodeType type;
+        if ((e = cudaGraphNodeGetType(node, &type)) != cudaSuccess) break;
+        if (type == cudaGraphNodeTypeEventRecord && g->n_events < kMaxForwardEvents)
+            g->ev_nodes[g->n_events++] = node;
+        size_t n_next = 0;
+        if ((e = cudaGraphNodeGetDependentNodes(node, nullptr, nullptr, &n_next)) != cudaSuccess) break;
+        if (n_next != 1) break;
+        e = cudaGraphNodeGetDependentNodes(node, &node, nullptr, &n_next);
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, graph, 0);
+    if (e != cudaSuccess) {
+        blk_graph_destroy(g);
+        return cuda_fail(e, "graph instantiation");
+    }
+    *out = g;
+    return BLK_OK;
+}
+
+blk_status blk_graph_launch(blk_graph* g, blk_stream_t s) {
+    BLK_REQUIRE(g != nullptr && g->exec != nullptr, "graph handle is NULL");
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    BLK_REQUIRE(dev == g->device, "graph was created on device %d, current device is %d",
+                g->device, dev);
+    e = cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "cudaGraphLaunch");
+}
+
+blk_status blk_graph_set_events(blk_graph* g, void* const* events, int n_events) {
+    BLK_REQUIRE(g != nullptr && g->exec != nullptr, "graph handle is NULL");
+    BLK_REQUIRE(events != nullptr && n_events >= g->n_events,
+                "the graph records %d events, got %d", g->n_events, n_events);
+    for (int i = 0; i < g->n_events; ++i) {
+        cudaError_t e = cudaGraphExecEventRecordNodeSetEvent(
+            g->exec, g->ev_nodes[i], static_cast<cudaEvent_t>(events[i]));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGraphExecEventRecordNodeSetEvent");
+    }
+    return BLK_OK;
+}
+
+blk_status blk_graph_destroy(blk_graph* g) {
+    if (!g) return BLK_OK;
+    cudaError_t e = g->exec ? cudaGraphExecDestroy(g->exec) : cudaSuccess;
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "cudaGraphExecDestroy");
 }
 
 }  // extern "C"

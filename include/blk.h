@@ -286,6 +286,30 @@ blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
                             void* workspace, size_t ws_bytes, int32_t n_chunks, blk_dtype dt,
                             blk_stream_t s);
 
+/* A block forward recorded once as a CUDA graph and replayed: the same seven
+ * to nine kernels with the same pointers, without per-launch host work or
+ * the gaps between separately submitted launches. blk_forward_graph_create
+ * captures blk_forward_ex(d, w, x, y, workspace, ...) with its optional
+ * events (recorded inside the graph, re-recorded by every launch) on a
+ * private stream; nothing runs until blk_graph_launch. *out receives a
+ * handle owned by the caller (free with blk_graph_destroy). The buffers must
+ * stay valid and keep their addresses while the handle is used; their
+ * contents are read at launch time. step_kinds / n_launches as for
+ * blk_forward_ex. blk_graph_launch enqueues one forward on s. */
+typedef struct blk_graph blk_graph;
+blk_status blk_forward_graph_create(const blk_block_desc* d, const blk_block_weights* w,
+                                    const void* x, void* y, void* workspace, size_t ws_bytes,
+                                    blk_dtype dt, void* const* events, int n_events,
+                                    int32_t* step_kinds, int* n_launches, blk_graph** out);
+blk_status blk_graph_launch(blk_graph* g, blk_stream_t s);
+/* Point the graph's recorded events (created with n_events > 0; it records
+ * min(n_events, launches + 1) of them) at other cudaEvent_t handles for the
+ * launches enqueued after this call (earlier launches keep theirs), so
+ * consecutive launches can be timed per kernel without waiting in between.
+ * events[0 .. recorded-1] are used; n_events must be at least that. */
+blk_status blk_graph_set_events(blk_graph* g, void* const* events, int n_events);
+blk_status blk_graph_destroy(blk_graph* g);
+
 #ifdef __cplusplus
 }
 #endif

@@ -176,3 +176,30 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         blk.rmsnorm(x, torch.ones(64, dtype=torch.bfloat16))
+
+
+def test_graph_handle_validation(lib):
+    """The graph entry points reject a missing handle before any CUDA call;
+    destroying NULL is a no-op."""
+    assert lib.blk_forward_graph_create(C.byref(_block()), C.byref(_weights()), FAKE, FAKE + 4096,
+                                        FAKE, 1 << 30, 1, None, 0, None, None,
+                                        None) == _abi.BLK_EINVAL
+    assert "out" in _err(lib)
+    assert lib.blk_graph_launch(None, None) == _abi.BLK_EINVAL
+    assert lib.blk_graph_destroy(None) == _abi.BLK_OK
+
+
+def test_forward_host_validation(lib):
+    """blk_forward_host checks its host/device buffers and chunk count before
+    any CUDA call."""
+    args = (C.byref(_block()), C.byref(_weights()))
+    assert lib.blk_forward_host(*args, None, FAKE, FAKE, FAKE + 4096, FAKE, 1 << 30, 2, 1,
+                                None) == _abi.BLK_EINVAL
+    assert lib.blk_forward_host(*args, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, 2, 1,
+                                None) == _abi.BLK_EINVAL  # y_dev aliases x_dev
+    assert lib.blk_forward_host(*args, FAKE, FAKE, FAKE, FAKE + 4096, FAKE, 1 << 30, 0, 1,
+                                None) == _abi.BLK_EINVAL
+    assert "n_chunks" in _err(lib)
+    assert lib.blk_forward_host(*args, FAKE, FAKE, FAKE, FAKE + 4096, FAKE, 16, 2, 1,
+                                None) == _abi.BLK_EWORKSPACE
+    assert lib.blk_graph_set_events(None, None, 0) == _abi.BLK_EINVAL

@@ -147,3 +147,56 @@ def test_forward_host_rejects_bad_arguments():
         blk.forward_host(cfg, wd, x.pin_memory(), n_chunks=0)
     with pytest.raises(blk.BlkError):
         blk.forward_host(cfg, wd, x.pin_memory(), n_chunks=17)
+
+
+@pytest.mark.parametrize("name", ["stablelm2_ragged_bf16", "olmo2_small", "bloom_small"])
+def test_forward_graph_replays_forward(name):
+    """A block recorded as a CUDA graph (blk_forward_graph_create) replays the
+    same kernels: bit-equal to blk_forward, and it reads its input buffer at
+    launch time (new contents, same address, new result)."""
+    cfg = SMALL[name]
+    x, w = workloads.block_inputs(cfg)
+    wd = {k: to_dev(t) for k, t in w.items()}
+    xd = to_dev(x)
+    yd = torch.empty_like(xd)
+    ws = torch.empty(blk.forward_workspace_size(cfg, *x.shape[:2]), dtype=torch.uint8,
+                     device=xd.device)
+    g = blk.ForwardGraph(cfg, wd, xd, yd, ws)
+    assert g.n_launches.value >= 7
+    g.launch()
+    torch.cuda.synchronize()
+    blk.check_device_status()
+    assert torch.equal(yd, blk.forward(cfg, wd, xd))
+    x2 = (x.double() * 0.5 - 0.25).to(x.dtype)
+    xd.copy_(to_dev(x2))
+    g.launch()
+    g.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(yd, blk.forward(cfg, wd, to_dev(x2)))
+    g.close()
+
+
+def test_forward_graph_events_time_each_launch():
+    """Events recorded inside the graph and retargeted per launch
+    (blk_graph_set_events) time every kernel of consecutive replays."""
+    cfg = SMALL["stablelm2_ragged_bf16"]
+    x, w = workloads.block_inputs(cfg)
+    wd = {k: to_dev(t) for k, t in w.items()}
+    xd = to_dev(x)
+    yd = torch.empty_like(xd)
+    ws = torch.empty(blk.forward_workspace_size(cfg, *x.shape[:2]), dtype=torch.uint8,
+                     device=xd.device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(11)] for _ in range(3)]
+    for row in evs:
+        for e in row:
+            e.record()
+    g = blk.ForwardGraph(cfg, wd, xd, yd, ws, events=evs[0])
+    n = g.n_launches.value
+    for row in evs:
+        g.launch(row)
+    torch.cuda.synchronize()
+    for row in evs:
+        t = [row[i].elapsed_time(row[i + 1]) for i in range(n)]
+        assert all(v > 0 for v in t)
+    assert torch.equal(yd, blk.forward(cfg, wd, xd))
+    g.close()
