@@ -257,6 +257,170 @@ __global__ void __launch_bounds__(128) qk_warp_kernel(QkNormRopeArgs a, RopePara
     }
 }
 
+// Unit path, head_dim D of 64 or 128 and rotary spans r with r/2 a multiple
+// of 8: one warp per (token, q|k) as above, but each lane owns units of two
+// 16-byte vectors of one head, chosen so that no data crosses lanes for the
+// rotation: unit u < r/16 holds vectors u and u + r/16 (dims 8u..8u+7 and
+// their partners 8u+r/2..), the other units hold two neighbouring vectors of
+// the unrotated tail. The head index and the lane's unit are compile-time
+// shifts of the lane id, the full-width RMS is one warp reduction, the
+// per-head LayerNorm a reduction over the head's D/16 lanes.
+template <typename T, int D, int NU>
+__global__ void __launch_bounds__(128) qk_unit_kernel(QkNormRopeArgs a, RopeParams rp) {
+    constexpr int kLph = D / 16;  // lanes per head
+    constexpr int kVph = D / 8;   // 16-byte vectors per head row
+    const int lane = threadIdx.x & 31;
+    const int wid = blockIdx.x * 4 + threadIdx.x / 32;
+    const int parts = a.Hk > 0 ? 2 : 1;
+    const int tokens = a.B * a.S;
+    if (wid >= tokens * parts) return;  // whole warps exit together
+    const int part = wid % parts;
+    const int token = wid / parts;
+    const int b = token / a.S;
+    const int s = token - b * a.S;
+    const int nh = part == 0 ? a.H : a.Hk;
+    T* base = static_cast<T*>(part == 0 ? a.q : a.k);
+    const T* bias = static_cast<const T*>(part == 0 ? a.q_bias : a.k_bias);
+    const T* w = static_cast<const T*>(part == 0 ? a.q_w : a.k_w);
+    const int hv = rp.span / 16;  // rotated vectors in each half
+    const int u = lane % kLph;    // this lane's unit within its head (every slot)
+    const bool rot = u < hv;
+    const int va = rot ? u : 2 * hv + 2 * (u - hv);
+    const int vb = rot ? u + hv : va + 1;
+    const int nunits = nh * kLph;
+
+    float x[NU][16];
+#pragma unroll
+    for (int i = 0; i < NU; ++i) {
+        const int U = lane + 32 * i;
+        const int head = U / kLph;
+        if (U < nunits) {
+            const T* row = base + ((static_cast<int64_t>(b) * nh + head) * a.S + s) * D;
+            float f0[8], f1[8];
+            load8(row + va * 8, f0);
+            load8(row + vb * 8, f1);
+            if (bias) {
+                float b0[8], b1[8];
+                load8(bias + head * D + va * 8, b0);
+                load8(bias + head * D + vb * 8, b1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    f0[e] += b0[e];
+                    f1[e] += b1[e];
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                x[i][e] = f0[e];
+                x[i][8 + e] = f1[e];
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[i][e] = 0.f;
+        }
+    }
+    if (a.mode == QKN_RMS_FULL) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < NU; ++i)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc = fmaf(x[i][e], x[i][e], acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        const float rstd = rsqrtf(acc / static_cast<float>(nh * D) + a.eps);
+#pragma unroll
+        for (int i = 0; i < NU; ++i) {
+            const int U = lane + 32 * i;
+            if (U < nunits) {
+                const int head = U / kLph;
+                float g0[8], g1[8];
+                load8(w + head * D + va * 8, g0);
+                load8(w + head * D + vb * 8, g1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    x[i][e] *= rstd * g0[e];
+                    x[i][8 + e] *= rstd * g1[e];
+                }
+            }
+        }
+    } else if (a.mode == QKN_LN_PER_HEAD) {
+#pragma unroll
+        for (int i = 0; i < NU; ++i) {
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sum += x[i][e];
+#pragma unroll
+            for (int o = kLph / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float mean = sum / static_cast<float>(D);
+            float sq = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float c = x[i][e] - mean;
+                sq = fmaf(c, c, sq);
+            }
+#pragma unroll
+            for (int o = kLph / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            const float rstd = rsqrtf(sq / static_cast<float>(D) + a.eps);
+            const int U = lane + 32 * i;
+            if (U < nunits) {
+                const int head = U / kLph;
+                float g0[8], g1[8];
+                load8(w + head * D + va * 8, g0);  // gamma [nh, D]
+                load8(w + head * D + vb * 8, g1);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    x[i][e] = (x[i][e] - mean) * rstd * g0[e];
+                    x[i][8 + e] = (x[i][8 + e] - mean) * rstd * g1[e];
+                }
+            }
+        }
+    }
+    if (rot) {
+        float c[8], sn[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rope_cos_sin(rp, s, u * 8 + e, c[e], sn[e]);
+#pragma unroll
+        for (int i = 0; i < NU; ++i)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float x0 = x[i][e], x1 = x[i][8 + e];
+                x[i][e] = x0 * c[e] - x1 * sn[e];
+                x[i][8 + e] = x1 * c[e] + x0 * sn[e];
+            }
+    }
+#pragma unroll
+    for (int i = 0; i < NU; ++i) {
+        const int U = lane + 32 * i;
+        if (U < nunits) {
+            T* row = base + ((static_cast<int64_t>(b) * nh + U / kLph) * a.S + s) * D;
+            store8(row + va * 8, *reinterpret_cast<const float(*)[8]>(&x[i][0]));
+            store8(row + vb * 8, *reinterpret_cast<const float(*)[8]>(&x[i][8]));
+        }
+    }
+}
+
+template <typename T, int D>
+bool launch_unit_d(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
+    const int nunits = (a.H > a.Hk ? a.H : a.Hk) * (D / 16);
+    const int64_t warps = static_cast<int64_t>(a.B) * a.S * (a.Hk > 0 ? 2 : 1);
+    const int64_t blocks = (warps + 3) / 4;
+    if (nunits > 256 || blocks > 0x7fffffff || warps > 0x7fffffff) return false;
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (nunits <= 32) qk_unit_kernel<T, D, 1><<<g, 128, 0, s>>>(a, rp);
+    else if (nunits <= 64) qk_unit_kernel<T, D, 2><<<g, 128, 0, s>>>(a, rp);
+    else if (nunits <= 128) qk_unit_kernel<T, D, 4><<<g, 128, 0, s>>>(a, rp);
+    else qk_unit_kernel<T, D, 8><<<g, 128, 0, s>>>(a, rp);
+    return true;
+}
+
+template <typename T>
+bool launch_unit_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
+    if ((rp.span / 2) % 8 != 0) return false;
+    if (a.d == 64) return launch_unit_d<T, 64>(a, rp, s);
+    if (a.d == 128) return launch_unit_d<T, 128>(a, rp, s);
+    return false;
+}
+
 template <typename T>
 bool launch_warp_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
     const int vph = a.d / 8;
@@ -280,6 +444,9 @@ cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopePar
                                 cudaStream_t s) {
     const int64_t tokens = static_cast<int64_t>(a.B) * a.S;
     if (tokens == 0) return cudaSuccess;
+    if (dt == DType::F16 ? launch_unit_path<__half>(a, rp, s)
+                         : launch_unit_path<__nv_bfloat16>(a, rp, s))
+        return cudaGetLastError();
     if (dt == DType::F16 ? launch_warp_path<__half>(a, rp, s)
                          : launch_warp_path<__nv_bfloat16>(a, rp, s))
         return cudaGetLastError();
