@@ -21,6 +21,7 @@ from . import _abi
 from ._abi import BlkError  # noqa: F401
 
 __all__ = ["layernorm_bias", "rmsnorm", "qkv_bias_rope_partial", "rope_inplace", "attn_prefill",
+           "attn_decode", "attn_decode_workspace_size", "decode_desc",
            "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host", "ForwardGraph",
            "check_device_status", "BlkError", "library_path"]
 
@@ -130,6 +131,41 @@ def attn_prefill(q, k, v, alibi=False, slopes=None, scale=None, out=None):
     o = torch.empty((B, S, H, d), dtype=q.dtype, device=q.device) if out is None else out
     _abi.check(_lib().blk_attn_prefill(C.byref(desc), _p(q), _p(k), _p(v), _p(slopes), _p(o),
                                        _dt(q), _stream()), "blk_attn_prefill")
+    return o
+
+
+def decode_desc(batch, max_seq, n_heads, n_kv_heads, head_dim, alibi=False, scale=None):
+    return _abi.DecodeDesc(batch, max_seq, n_heads, n_kv_heads, head_dim,
+                           -1.0 if scale is None else scale, 1 if alibi else 0)
+
+
+def attn_decode_workspace_size(desc) -> int:
+    need = C.c_size_t(0)
+    _abi.check(_lib().blk_attn_decode_workspace_size(C.byref(desc), C.byref(need)),
+               "blk_attn_decode_workspace_size")
+    return need.value
+
+
+def attn_decode(q, k_cache, v_cache, lens, alibi=False, slopes=None, scale=None, out=None,
+                workspace=None):
+    """One decode step: q [B, H, d] (newest token of each sequence, at position
+    lens[b] - 1) against k/v caches [B, Hk, S_max, d]; lens int32 [B] on the
+    device. Returns o [B, H, d]."""
+    _same(q, k_cache, v_cache, out)
+    B, H, d = q.shape
+    Hk, S_max = k_cache.shape[1], k_cache.shape[2]
+    if lens.dtype != torch.int32:
+        raise TypeError("lens are int32")
+    if slopes is not None and slopes.dtype != torch.float32:
+        raise TypeError("ALiBi slopes are fp32")
+    desc = decode_desc(B, S_max, H, Hk, d, alibi, scale)
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_size(desc), dtype=torch.uint8,
+                                device=q.device)
+    o = torch.empty_like(q) if out is None else out
+    _abi.check(_lib().blk_attn_decode(C.byref(desc), _p(q), _p(k_cache), _p(v_cache), _p(lens),
+                                      _p(slopes), _p(o), _p(workspace), workspace.numel(), _dt(q),
+                                      _stream()), "blk_attn_decode")
     return o
 
 

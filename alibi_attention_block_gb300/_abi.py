@@ -39,6 +39,11 @@ class AttnDesc(C.Structure):
                 ("head_dim", i64), ("softmax_scale", f32), ("causal", i32), ("alibi", i32)]
 
 
+class DecodeDesc(C.Structure):
+    _fields_ = [("batch", i64), ("max_seq", i64), ("n_heads", i64), ("n_kv_heads", i64),
+                ("head_dim", i64), ("softmax_scale", f32), ("alibi", i32)]
+
+
 class MlpDesc(C.Structure):
     _fields_ = [("tokens", i64), ("hidden", i64), ("intermediate", i64), ("act", i32)]
 
@@ -78,6 +83,9 @@ _PROTOS = {
     "blk_forward_workspace_size": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(C.c_size_t)]),
     "blk_forward": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp,
                               C.c_size_t, C.c_int, vp]),
+    "blk_attn_decode_workspace_size": (C.c_int, [C.POINTER(DecodeDesc), C.POINTER(C.c_size_t)]),
+    "blk_attn_decode": (C.c_int, [C.POINTER(DecodeDesc), vp, vp, vp, vp, vp, vp, vp, C.c_size_t,
+                                  C.c_int, vp]),
     "blk_forward_graph_create": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp,
                                            vp, C.c_size_t, C.c_int, C.POINTER(vp), C.c_int,
                                            C.POINTER(i32), C.POINTER(C.c_int), C.POINTER(vp)]),

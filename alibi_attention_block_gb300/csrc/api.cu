@@ -620,6 +620,82 @@ blk_status blk_rope_inplace(void* x, const void* bias, int64_t batch, int64_t n_
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "rope launch");
 }
 
+static blk_status validate_decode_desc(const blk_decode_desc* d) {
+    BLK_REQUIRE(d != nullptr, "desc is NULL");
+    BLK_REQUIRE(d->batch >= 1 && d->batch <= kI32, "batch out of range");
+    BLK_REQUIRE(d->max_seq >= 1 && d->max_seq <= kI32, "max_seq out of range");
+    BLK_REQUIRE(d->n_heads >= 1 && d->n_kv_heads >= 1 && d->n_heads % d->n_kv_heads == 0,
+                "n_heads must be a positive multiple of n_kv_heads");
+    const int64_t g = d->n_heads / d->n_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(BLK_EUNSUPPORTED, "n_heads / n_kv_heads must be 1, 2, 4 or 8");
+    if (d->head_dim != 64 && d->head_dim != 128)
+        return fail(BLK_EUNSUPPORTED, "head_dim must be 64 or 128");
+    BLK_REQUIRE(d->batch * d->n_heads <= kI32 &&
+                    d->batch * d->n_kv_heads * d->max_seq * d->head_dim <= (int64_t(1) << 40),
+                "sizes out of range");
+    BLK_REQUIRE(d->alibi == 0 || d->alibi == 1, "alibi must be 0 or 1");
+    BLK_REQUIRE(std::isfinite(d->softmax_scale), "softmax_scale must be finite");
+    return BLK_OK;
+}
+
+static size_t decode_ws_bytes(const blk_decode_desc* d) {
+    return static_cast<size_t>(d->batch) * d->n_heads * decode_parts_max(d->max_seq) *
+           (d->head_dim + 2) * sizeof(float);
+}
+
+blk_status blk_attn_decode_workspace_size(const blk_decode_desc* d, size_t* bytes) {
+    blk_status st = validate_decode_desc(d);
+    if (st != BLK_OK) return st;
+    BLK_REQUIRE(bytes != nullptr, "bytes is NULL");
+    *bytes = decode_ws_bytes(d);
+    return BLK_OK;
+}
+
+blk_status blk_attn_decode(const blk_decode_desc* d, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* lens, const float* alibi_slopes,
+                           void* o, void* workspace, size_t ws_bytes, blk_dtype dt,
+                           blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    blk_status st = validate_decode_desc(d);
+    if (st != BLK_OK) return st;
+    BLK_CHECK_PTR(q, true);
+    BLK_CHECK_PTR(k_cache, true);
+    BLK_CHECK_PTR(v_cache, true);
+    BLK_CHECK_PTR(o, true);
+    BLK_REQUIRE(lens != nullptr && (reinterpret_cast<uintptr_t>(lens) & 3u) == 0,
+                "lens must be a 4-byte aligned device pointer");
+    BLK_REQUIRE(d->alibi || !alibi_slopes, "alibi_slopes given with alibi = 0");
+    if (d->alibi && !alibi_slopes && !is_pow2(d->n_heads))
+        return fail(BLK_EUNSUPPORTED, "standard ALiBi slopes need a power-of-two head count");
+    BLK_REQUIRE(!alibi_slopes || (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u) == 0,
+                "alibi_slopes must be 4-byte aligned");
+    const size_t need = decode_ws_bytes(d);
+    if (!workspace || ws_bytes < need || !aligned16(workspace))
+        return fail(BLK_EWORKSPACE, "workspace needs %zu bytes, 16-byte aligned", need);
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+    DecodeArgs a{};
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.o = o;
+    a.lens = lens;
+    a.slopes = alibi_slopes;
+    a.ws = static_cast<float*>(workspace);
+    a.B = static_cast<int>(d->batch);
+    a.H = static_cast<int>(d->n_heads);
+    a.Hk = static_cast<int>(d->n_kv_heads);
+    a.d = static_cast<int>(d->head_dim);
+    a.S_max = static_cast<int>(d->max_seq);
+    a.parts = decode_parts(d->batch, d->n_kv_heads, d->max_seq, ds->sms);
+    a.scale = d->softmax_scale > 0.f ? d->softmax_scale
+                                     : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
+    a.alibi = d->alibi;
+    const cudaError_t e = launch_attention_decode(to_dt(dt), a, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "decode attention launch");
+}
+
 blk_status blk_attn_prefill(const blk_attn_desc* d, const void* q, const void* k, const void* v,
                             const float* alibi_slopes, void* o, blk_dtype dt, blk_stream_t s) {
     BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");

@@ -86,6 +86,24 @@ cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s);
 // head_dim 64: the paired-query-tile kernel (attn_pair.cu)
 cudaError_t launch_attention_pair64(DType dt, const AttnArgs& a, cudaStream_t s);
 
+// ---- K6: decode-step attention over a KV cache (attn_decode.cu)
+struct DecodeArgs {
+    const void* q;        // [B, H, d]
+    const void* k;        // [B, Hk, S_max, d]
+    const void* v;
+    void* o;              // [B, H, d]
+    const int32_t* lens;  // device [B]
+    const float* slopes;  // device [H] or nullptr (standard slopes)
+    float* ws;            // [B, H, parts, d + 2] partial results
+    int B, H, Hk, d, S_max, parts;
+    float scale;
+    int alibi;
+};
+cudaError_t launch_attention_decode(DType dt, const DecodeArgs& a, cudaStream_t s);
+// number of key ranges per (batch, kv head), and its device-independent bound
+int decode_parts(int64_t B, int64_t Hk, int64_t S_max, int num_sms);
+int decode_parts_max(int64_t S_max);
+
 // ---- per-device state and error reporting shared with other entry points (api.cu)
 // SM count and device error word of the current device (set up on first use).
 blk_status current_device_info(int* sms, unsigned** err);

@@ -258,6 +258,43 @@ def run_attn_sweep(args, rank):
               flush=True)
 
 
+def run_decode(args, rank):
+    """Decode-step attention (blk_attn_decode) over KV caches larger than L2:
+    HBM bound, reported against the measured copy bandwidth. Algorithmic
+    bytes: K and V of every visible key, plus q and o."""
+    import alibi_attention_block_gb300 as blk
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    peaks = _peaks()
+    res = {}
+    for name, (B, H, Hk, S, d) in {"stablelm2_1p6b_b16_s2048": (16, 32, 32, 2048, 64),
+                                   "gqa4_d128_b16_s4096": (16, 32, 8, 4096, 128),
+                                   "stablelm2_1p6b_b64_s8192": (64, 32, 32, 8192, 64)}.items():
+        g = torch.Generator(device=dev).manual_seed(1)
+        q = torch.randn(B, H, d, device=dev, generator=g).to(torch.bfloat16)
+        k = torch.randn(B, Hk, S, d, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(B, Hk, S, d, device=dev, generator=g).to(torch.bfloat16)
+        lens = torch.full((B,), S, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        ws = torch.empty(blk.attn_decode_workspace_size(blk.decode_desc(B, S, H, Hk, d)),
+                         dtype=torch.uint8, device=dev)
+        t = _time_back_to_back(lambda: blk.attn_decode(q, k, v, lens, out=o, workspace=ws),
+                               reps=20)
+        nbytes = 2 * B * Hk * S * d * 2 + 2 * B * H * d * 2
+        gbs = nbytes / (t / 1e3) / 1e9
+        res[name] = {"batch": B, "heads": H, "kv_heads": Hk, "cache_len": S, "head_dim": d,
+                     "ms": t, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                     "tokens_per_s": B / (t / 1e3)}
+        del q, k, v, o, ws
+        torch.cuda.empty_cache()
+    blk.check_device_status()
+    if rank == 0:
+        print(json.dumps({"metric": "decode-step attention over a KV cache (GB/s)",
+                          "unit": "GB/s", "peak_source": peaks["source"] + " copy",
+                          "decode": res}), flush=True)
+
+
 # ----------------------------------------------------------------- oracle --
 _INPUTS = {}
 
@@ -514,6 +551,8 @@ def main():
                          "graph saves (0.715 vs 0.707 ms), without them it is 2.6%% faster")
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="groups of sequences blk_forward_host overlaps copies and compute over")
+    ap.add_argument("--decode", action="store_true",
+                    help="time decode-step attention over KV caches instead of the block")
     ap.add_argument("--attn-sweep", action="store_true",
                     help="time the attention-only workloads instead of the block")
     args = ap.parse_args()
@@ -523,6 +562,8 @@ def main():
     dist, rank, world, local_rank = _dist()
     if args.attn_sweep:
         run_attn_sweep(args, rank)
+    elif args.decode:
+        run_decode(args, rank)
     elif args.impl == "reference":
         run_reference(args, cfg, rank, world)
     else:

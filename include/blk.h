@@ -155,6 +155,35 @@ typedef struct {
 blk_status blk_attn_prefill(const blk_attn_desc* d, const void* q, const void* k, const void* v,
                             const float* alibi_slopes, void* o, blk_dtype dt, blk_stream_t s);
 
+/* ---- decode step ------------------------------------------------------ */
+
+typedef struct {
+    int64_t batch, max_seq, n_heads, n_kv_heads, head_dim;
+    float softmax_scale; /* <= 0 -> head_dim^-0.5 */
+    int32_t alibi;       /* 0 off; 1: score -= slope_h * (query_pos - key_pos) */
+} blk_decode_desc;
+
+/* One decode step of attention over a KV cache: the step after prefill (the
+ * pages state prefill; this applies the same attention, nnterp "stablelm" 03
+ * Notes and "Bloom in a sovereign engine", Contribution, to one new token).
+ *   q [batch, H, d]: each sequence's newest token, at position lens[b] - 1
+ *   k_cache, v_cache [batch, Hk, max_seq, d]: positions 0 .. lens[b] - 1 of
+ *     sequence b (the newest already written); later entries are not read
+ *   lens: device int32 [batch], each in [1, max_seq]. They are read on the
+ *     device, so they cannot be checked here: a value outside the range is
+ *     clamped to it, and a length of 0 gives a zero output row
+ *   alibi_slopes: as for blk_attn_prefill
+ *   o [batch, H, d]
+ * GQA: kv head = h / (H / Hk), H / Hk in {1, 2, 4, 8}; head_dim 64 or 128.
+ * Two launches (key ranges per (batch, kv head), then their merge); the
+ * workspace holds the partial results, at least
+ * blk_attn_decode_workspace_size bytes, 16-byte aligned. */
+blk_status blk_attn_decode_workspace_size(const blk_decode_desc* d, size_t* bytes);
+blk_status blk_attn_decode(const blk_decode_desc* d, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* lens, const float* alibi_slopes,
+                           void* o, void* workspace, size_t ws_bytes, blk_dtype dt,
+                           blk_stream_t s);
+
 /* ---- linear and MLP --------------------------------------------------- */
 
 /* y = x W^T [+ bias] [+ res1] [+ res2] on tcgen05 tensor cores.

@@ -19,5 +19,5 @@ unpinned by the pages.
 from .block import (  # noqa: F401
     as_f64, layer_norm, rms_norm, linear, split_qkv, split_heads, merge_heads,
     qk_norm_full_rms, qk_norm_per_head_ln, rope_inv_freq, rope, alibi_slopes,
-    attention, silu, gelu_tanh, mlp, block_forward, attention_forward,
+    attention, attention_decode, silu, gelu_tanh, mlp, block_forward, attention_forward,
 )

@@ -227,6 +227,29 @@ def attention(q, k, v, scale=None, slopes=None, causal=True, q_positions=None,
     return (o, probs) if return_probs else o
 
 
+def attention_decode(q, k_cache, v_cache, lens, scale=None, slopes=None):
+    """One decode step of causal attention over a KV cache (the step after
+    prefill; the pages state prefill only, this follows the same attention
+    definition, [NNT] 03 Notes and [BLM] Contribution for ALiBi).
+
+    q [B, H, d]: the newest token of each sequence, at position lens[b] - 1;
+    k_cache, v_cache [B, Hk, S_max, d] hold positions 0 .. lens[b] - 1 (the
+    newest included); entries at lens[b] and beyond are not part of the
+    sequence. Returns o [B, H, d]: each query attends to its sequence's
+    lens[b] keys, which is attention() with one query row at that position.
+    """
+    q, k_cache, v_cache = as_f64(q), as_f64(k_cache), as_f64(v_cache)
+    B, H, d = q.shape
+    o = np.empty((B, H, v_cache.shape[-1]), dtype=np.float64)
+    for b in range(B):
+        n = int(lens[b])
+        if not 1 <= n <= k_cache.shape[2]:
+            raise ValueError("lens must be in [1, S_max]")
+        o[b] = attention(q[b:b + 1, :, None, :], k_cache[b:b + 1, :, :n], v_cache[b:b + 1, :, :n],
+                         scale=scale, slopes=slopes, q_positions=[n - 1])[0, :, 0]
+    return o
+
+
 # -------------------------------------------------------------- MLP ----
 
 def silu(z):

@@ -203,3 +203,22 @@ def test_forward_host_validation(lib):
     assert lib.blk_forward_host(*args, FAKE, FAKE, FAKE, FAKE + 4096, FAKE, 16, 2, 1,
                                 None) == _abi.BLK_EWORKSPACE
     assert lib.blk_graph_set_events(None, None, 0) == _abi.BLK_EINVAL
+
+
+def test_decode_validation(lib):
+    """blk_attn_decode: shape rules and workspace size without a GPU."""
+    d = _abi.DecodeDesc(4, 2048, 32, 8, 64, -1.0, 0)
+    need = C.c_size_t(0)
+    assert lib.blk_attn_decode_workspace_size(C.byref(d), C.byref(need)) == _abi.BLK_OK
+    assert need.value == 4 * 32 * 32 * (64 + 2) * 4  # parts <= ceil(2048 / 64) = 32
+    bad = _abi.DecodeDesc(4, 2048, 32, 8, 96, -1.0, 0)
+    assert lib.blk_attn_decode_workspace_size(C.byref(bad), C.byref(need)) == _abi.BLK_EUNSUPPORTED
+    bad = _abi.DecodeDesc(4, 2048, 24, 8, 64, -1.0, 0)  # group of 3
+    assert lib.blk_attn_decode_workspace_size(C.byref(bad), C.byref(need)) == _abi.BLK_EUNSUPPORTED
+    assert lib.blk_attn_decode(C.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 1 << 30, 1,
+                               None) == _abi.BLK_EINVAL  # lens NULL
+    assert lib.blk_attn_decode(C.byref(d), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 16, 1,
+                               None) == _abi.BLK_EWORKSPACE
+    ali = _abi.DecodeDesc(1, 16, 12, 12, 64, -1.0, 1)  # standard slopes need 2^k heads
+    assert lib.blk_attn_decode(C.byref(ali), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 1 << 30, 1,
+                               None) == _abi.BLK_EUNSUPPORTED
