@@ -11,12 +11,16 @@
 // a contiguous range of keys; the warp keeps, for each of the kv head's
 // query heads, the running max, the running sum and the unnormalised output
 // (lane c owns output columns c*d/32 ..), and walks its range 32 keys at a
-// time: lane l takes key l, computes its scores from 16-byte loads of its K
-// row against the queries (shared memory, broadcast), then the warp takes
-// the max and sum by shuffles and accumulates p * V with one coalesced load
-// of each V row. Each part writes (max, sum, output) to the workspace.
+// time through its own three-stage shared-memory ring filled by cp.async
+// (blocks i+1 and i+2 are in flight while block i is used, and in-flight
+// data costs no registers): lane l scores key l against the queries
+// (shared memory, broadcast), the warp takes the max and sum by shuffles
+// and accumulates p * V reading one V row per key. Each part writes (max,
+// sum, output) to the workspace.
 // Pass 2 (decode_combine_kernel): one warp per (b, query head) merges the
 // parts: o = sum_i e^{m_i - m} O_i / sum_i e^{m_i - m} l_i.
+#include <type_traits>
+
 #include "internal.h"
 
 namespace blk {
@@ -26,15 +30,28 @@ namespace {
 constexpr int kDecThreads = 128;  // 4 warps per block, one part each
 constexpr float kLog2eDec = 1.4426950408889634f;
 
+template <int D>
+struct DecCfg {
+    static constexpr int kStages = 3;                    // key blocks in flight per warp
+    static constexpr int kBlockBytes = 32 * D * 2;       // 32 K (or V) rows
+    static constexpr int kStageBytes = 2 * kBlockBytes;  // K then V
+    static constexpr int kWarpBytes = kStages * kStageBytes;
+    static constexpr int kSmem = 4 * kWarpBytes;
+};
+
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs a) {
+    using Cfg = DecCfg<D>;
     constexpr int kCols = D / 32;  // output columns per lane
+    constexpr int kChunks = D / 8; // 16-byte pieces per row
     __shared__ float qs[4][G][D];  // this warp's queries, pre-scaled (log2 domain)
+    extern __shared__ __align__(128) uint8_t dsm[];
     const int lane = threadIdx.x & 31;
     const int wl = threadIdx.x / 32;
     const int64_t wid = static_cast<int64_t>(blockIdx.x) * 4 + wl;
     const int64_t total = static_cast<int64_t>(a.B) * a.Hk * a.parts;
     if (wid >= total) return;  // whole warps exit together
+    const uint32_t ring = smem_u32(dsm) + wl * Cfg::kWarpBytes;
     const int part = static_cast<int>(wid % a.parts);
     const int bg = static_cast<int>(wid / a.parts);
     const int b = bg / a.Hk;
@@ -45,6 +62,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
     const int per = (a.S_max + a.parts - 1) / a.parts;
     const int j0 = part * per;
     const int j1 = min(n, j0 + per);
+    const int nblk = j1 > j0 ? (j1 - j0 + 31) / 32 : 0;
     const float qscale = a.scale * kLog2eDec;
     const T* qp = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.H + g * G) * D;
     for (int i = lane; i < G * D / 8; i += 32) {
@@ -53,7 +71,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
 #pragma unroll
         for (int e = 0; e < 8; ++e) qs[wl][(i * 8) / D][(i * 8) % D + e] = f[e] * qscale;
     }
-    __syncwarp();
     float slope[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -66,6 +83,27 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
             slope[h] = sl * kLog2eDec;
         }
     }
+    const int64_t kv_base = (static_cast<int64_t>(b) * a.Hk + g) * a.S_max;
+    const T* kp = static_cast<const T*>(a.k) + kv_base * D;
+    const T* vp = static_cast<const T*>(a.v) + kv_base * D;
+    // copy key block i into its stage: K rows with their 16-byte pieces
+    // XOR-swizzled by row (conflict-free when lane l reads row l), V rows
+    // plain (lanes read one row together); rows past the range are zeros
+    auto issue = [&](int i) {
+        if (i < nblk) {
+            const int jb = j0 + i * 32;
+            const uint32_t st = ring + (i % Cfg::kStages) * Cfg::kStageBytes;
+#pragma unroll
+            for (int q = lane; q < 32 * kChunks; q += 32) {
+                const int r = q / kChunks, c = q % kChunks;
+                const bool ok = jb + r < j1;
+                const int64_t src = static_cast<int64_t>(ok ? jb + r : j0) * D + c * 8;
+                cp_async16(st + r * (D * 2) + ((c ^ (r & 7)) << 4), kp + src, ok ? 16u : 0u);
+                cp_async16(st + Cfg::kBlockBytes + r * (D * 2) + (c << 4), vp + src, ok ? 16u : 0u);
+            }
+        }
+        cp_async_commit();  // one group per block index, empty past the end
+    };
     float m[G], l[G], acc[G][kCols];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -74,27 +112,34 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
 #pragma unroll
         for (int c = 0; c < kCols; ++c) acc[h][c] = 0.f;
     }
-    const int64_t kv_base = (static_cast<int64_t>(b) * a.Hk + g) * a.S_max;
-    const T* kp = static_cast<const T*>(a.k) + kv_base * D;
-    const T* vp = static_cast<const T*>(a.v) + kv_base * D;
+#pragma unroll
+    for (int i = 0; i < Cfg::kStages - 1; ++i) issue(i);
+    __syncwarp();
     const float qpos = static_cast<float>(n - 1);
-    for (int jb = j0; jb < j1; jb += 32) {
+    for (int i = 0; i < nblk; ++i) {
+        issue(i + Cfg::kStages - 1);
+        cp_async_wait<Cfg::kStages - 1>();  // block i has landed (this lane's copies)
+        __syncwarp();                       // ... and every lane's
+        const uint32_t st = ring + (i % Cfg::kStages) * Cfg::kStageBytes;
+        const int jb = j0 + i * 32;
         const int j = jb + lane;
         const bool valid = j < j1;
         // scores of key j against the G queries (log2 domain)
         float sc[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[h] = 0.f;
-        if (valid) {
-            const T* krow = kp + static_cast<int64_t>(j) * D;
-#pragma unroll 4
-            for (int c = 0; c < D / 8; ++c) {
-                float kf[8];
-                load8(krow + c * 8, kf);
 #pragma unroll
-                for (int h = 0; h < G; ++h)
+        for (int c = 0; c < kChunks; ++c) {
+            const uint4 kv = ld_shared_u4(st + lane * (D * 2) + ((c ^ (lane & 7)) << 4));
+            const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) sc[h] = fmaf(qs[wl][h][c * 8 + e], kf[e], sc[h]);
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const float2 kf = dt_traits<T>::unpack2(w4[e2]);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    sc[h] = fmaf(qs[wl][h][c * 8 + 2 * e2], kf.x, sc[h]);
+                    sc[h] = fmaf(qs[wl][h][c * 8 + 2 * e2 + 1], kf.y, sc[h]);
+                }
             }
         }
 #pragma unroll
@@ -113,24 +158,29 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
             m[h] = mn;
 #pragma unroll
             for (int c = 0; c < kCols; ++c) acc[h][c] *= corr;
-            sc[h] = p;
+            sc[h] = p;  // 0 for keys past the range (their V rows are zeros)
         }
-        // O += p V over this block's keys, one coalesced row load per key
-        const int nk = min(32, j1 - jb);
-        for (int t = 0; t < nk; ++t) {
-            const T* vrow = vp + static_cast<int64_t>(jb + t) * D + lane * kCols;
+        // O += p V over the block's keys
+        const uint32_t vrow0 = st + Cfg::kBlockBytes + lane * (kCols * 2);
+#pragma unroll 8
+        for (int t = 0; t < 32; ++t) {
             float vf[kCols];
             if constexpr (kCols == 2) {
-                const float2 u = dt_traits<T>::unpack2(*reinterpret_cast<const uint32_t*>(vrow));
-                vf[0] = u.x;
-                vf[1] = u.y;
+                uint32_t u;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(u) : "r"(vrow0 + t * (D * 2)));
+                const float2 f = dt_traits<T>::unpack2(u);
+                vf[0] = f.x;
+                vf[1] = f.y;
             } else {
-                const uint2 u = *reinterpret_cast<const uint2*>(vrow);
-                const float2 u0 = dt_traits<T>::unpack2(u.x), u1 = dt_traits<T>::unpack2(u.y);
-                vf[0] = u0.x;
-                vf[1] = u0.y;
-                vf[2] = u1.x;
-                vf[3] = u1.y;
+                uint32_t u0, u1;
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                             : "=r"(u0), "=r"(u1)
+                             : "r"(vrow0 + t * (D * 2)));
+                const float2 f0 = dt_traits<T>::unpack2(u0), f1 = dt_traits<T>::unpack2(u1);
+                vf[0] = f0.x;
+                vf[1] = f0.y;
+                vf[2] = f1.x;
+                vf[3] = f1.y;
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -139,7 +189,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
                 for (int c = 0; c < kCols; ++c) acc[h][c] = fmaf(pt, vf[c], acc[h][c]);
             }
         }
+        __syncwarp();  // the stage is refilled by the next issue
     }
+    cp_async_wait<0>();
     // (max, sum, output) of this part for each query head; an empty part
     // (j0 >= n) writes max = -inf, sum = 0
     float* rec = a.ws + (static_cast<int64_t>(b) * a.H + g * G) * a.parts * (D + 2);
@@ -184,7 +236,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_combine_kernel(DecodeArgs 
 template <typename T, int D, int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
     const int64_t warps = static_cast<int64_t>(a.B) * a.Hk * a.parts;
-    decode_partial_kernel<T, D, G><<<static_cast<unsigned>((warps + 3) / 4), kDecThreads, 0, s>>>(a);
+    auto kern = decode_partial_kernel<T, D, G>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecCfg<D>::kSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    kern<<<static_cast<unsigned>((warps + 3) / 4), kDecThreads, DecCfg<D>::kSmem, s>>>(a);
     const int64_t cw = static_cast<int64_t>(a.B) * a.H;
     decode_combine_kernel<T, D><<<static_cast<unsigned>((cw + 3) / 4), kDecThreads, 0, s>>>(a);
     return cudaGetLastError();
