@@ -431,6 +431,7 @@ blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, cons
     if (log && (st = log->step(BLK_STEP_QKV)) != BLK_OK) return st;
     if (!fuse_rope) {
         QkNormRopeArgs a{};
+        a.num_sms = ds->sms;
         a.q = q;
         a.k = k;
         a.q_w = q_norm_w;
@@ -606,7 +607,11 @@ blk_status blk_rope_inplace(void* x, const void* bias, int64_t batch, int64_t n_
                 "rotary_span must be even and in [0, head_dim]");
     BLK_REQUIRE(rotary_span == 0 || (std::isfinite(rope_base) && rope_base > 1.f),
                 "rope_base must be > 1 when rotary is on");
+    DevState* ds = nullptr;
+    blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
     QkNormRopeArgs a{};
+    a.num_sms = ds->sms;
     a.q = x;
     a.q_bias = bias;
     a.B = static_cast<int>(batch);

@@ -42,6 +42,7 @@ struct QkNormRopeArgs {
     int B, S, H, Hk, d;
     int mode;           // QkNormMode
     float eps;
+    int num_sms;        // persistent grid size for the unit path
 };
 cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopeParams& rp,
                                 cudaStream_t s);

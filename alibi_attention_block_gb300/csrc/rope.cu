@@ -258,158 +258,218 @@ __global__ void __launch_bounds__(128) qk_warp_kernel(QkNormRopeArgs a, RopePara
 }
 
 // Unit path, head_dim D of 64 or 128 and rotary spans r with r/2 a multiple
-// of 8: one warp per (token, q|k) as above, but each lane owns units of two
-// 16-byte vectors of one head, chosen so that no data crosses lanes for the
-// rotation: unit u < r/16 holds vectors u and u + r/16 (dims 8u..8u+7 and
-// their partners 8u+r/2..), the other units hold two neighbouring vectors of
-// the unrotated tail. The head index and the lane's unit are compile-time
-// shifts of the lane id, the full-width RMS is one warp reduction, the
-// per-head LayerNorm a reduction over the head's D/16 lanes.
+// of 8: a warp per (token, q|k) item as above, but each lane owns units of
+// two 16-byte vectors of one head, chosen so that no data crosses lanes for
+// the rotation: unit u < r/16 holds vectors u and u + r/16 (dims 8u..8u+7
+// and their partners 8u+r/2..), the other units hold two neighbouring
+// vectors of the unrotated tail. The head index and the lane's unit are
+// compile-time shifts of the lane id, the full-width RMS is one warp
+// reduction, the per-head LayerNorm a reduction over the head's D/16 lanes.
+// Persistent warps walk their items with a three-stage cp.async ring in
+// shared memory, so the next two items' bytes are in flight (without
+// holding registers) while one is computed.
+template <int NU>
+struct UnitCfg {
+    static constexpr int kStages = 3;                 // tokens in flight per warp
+    static constexpr int kStageBytes = NU * 2 * 512;  // [slot][vector a|b][lane] x 16 B
+    static constexpr int kSmem = 4 * kStages * kStageBytes;
+};
+
 template <typename T, int D, int NU>
 __global__ void __launch_bounds__(128) qk_unit_kernel(QkNormRopeArgs a, RopeParams rp) {
+    using Cfg = UnitCfg<NU>;
     constexpr int kLph = D / 16;  // lanes per head
-    constexpr int kVph = D / 8;   // 16-byte vectors per head row
+    extern __shared__ __align__(128) uint8_t usm[];
     const int lane = threadIdx.x & 31;
-    const int wid = blockIdx.x * 4 + threadIdx.x / 32;
     const int parts = a.Hk > 0 ? 2 : 1;
-    const int tokens = a.B * a.S;
-    if (wid >= tokens * parts) return;  // whole warps exit together
-    const int part = wid % parts;
-    const int token = wid / parts;
-    const int b = token / a.S;
-    const int s = token - b * a.S;
-    const int nh = part == 0 ? a.H : a.Hk;
-    T* base = static_cast<T*>(part == 0 ? a.q : a.k);
-    const T* bias = static_cast<const T*>(part == 0 ? a.q_bias : a.k_bias);
-    const T* w = static_cast<const T*>(part == 0 ? a.q_w : a.k_w);
+    const int total = a.B * a.S * parts;
+    const int nwarps = static_cast<int>(gridDim.x) * 4;
+    const int w0 = blockIdx.x * 4 + threadIdx.x / 32;
+    const uint32_t ring = smem_u32(usm) + (threadIdx.x / 32) * Cfg::kStages * Cfg::kStageBytes;
     const int hv = rp.span / 16;  // rotated vectors in each half
     const int u = lane % kLph;    // this lane's unit within its head (every slot)
     const bool rot = u < hv;
     const int va = rot ? u : 2 * hv + 2 * (u - hv);
     const int vb = rot ? u + hv : va + 1;
-    const int nunits = nh * kLph;
+    // this warp's k-th item: (token, q|k)
+    auto item = [&](int k, int& part, int& b, int& s) {
+        const int w = w0 + k * nwarps;
+        part = w % parts;
+        const int token = w / parts;
+        b = token / a.S;
+        s = token - b * a.S;
+    };
+    // cp.async of the k-th item's units into its stage (lane-private slots)
+    auto issue = [&](int k) {
+        if (w0 + k * nwarps < total) {
+            int part, b, s;
+            item(k, part, b, s);
+            const int nh = part == 0 ? a.H : a.Hk;
+            const T* base = static_cast<const T*>(part == 0 ? a.q : a.k);
+            const uint32_t st = ring + (k % Cfg::kStages) * Cfg::kStageBytes;
+#pragma unroll
+            for (int i = 0; i < NU; ++i) {
+                const int U = lane + 32 * i;
+                if (U < nh * kLph) {
+                    const T* row = base + ((static_cast<int64_t>(b) * nh + U / kLph) * a.S + s) * D;
+                    cp_async16(st + ((2 * i) * 32 + lane) * 16, row + va * 8, 16u);
+                    cp_async16(st + ((2 * i + 1) * 32 + lane) * 16, row + vb * 8, 16u);
+                }
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < Cfg::kStages - 1; ++k) issue(k);
+    for (int k = 0; w0 + k * nwarps < total; ++k) {
+        issue(k + Cfg::kStages - 1);
+        cp_async_wait<Cfg::kStages - 1>();  // this lane's copies of item k landed
+        int part, b, s;
+        item(k, part, b, s);
+        const int nh = part == 0 ? a.H : a.Hk;
+        T* base = static_cast<T*>(part == 0 ? a.q : a.k);
+        const T* bias = static_cast<const T*>(part == 0 ? a.q_bias : a.k_bias);
+        const T* w = static_cast<const T*>(part == 0 ? a.q_w : a.k_w);
+        const int nunits = nh * kLph;
+        const uint32_t st = ring + (k % Cfg::kStages) * Cfg::kStageBytes;
+        float x[NU][16];
+#pragma unroll
+        for (int i = 0; i < NU; ++i) {
+            const int U = lane + 32 * i;
+            if (U < nunits) {
+                const uint4 r0 = ld_shared_u4(st + ((2 * i) * 32 + lane) * 16);
+                const uint4 r1 = ld_shared_u4(st + ((2 * i + 1) * 32 + lane) * 16);
+                const uint32_t w8[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 f = dt_traits<T>::unpack2(w8[e]);
+                    x[i][(e / 4) * 8 + (e % 4) * 2] = f.x;
+                    x[i][(e / 4) * 8 + (e % 4) * 2 + 1] = f.y;
+                }
+                if (bias) {
+                    const int head = U / kLph;
+                    float b0[8], b1[8];
+                    load8(bias + head * D + va * 8, b0);
+                    load8(bias + head * D + vb * 8, b1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        x[i][e] += b0[e];
+                        x[i][8 + e] += b1[e];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[i][e] = 0.f;
+            }
+        }
+        if (a.mode == QKN_RMS_FULL) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < NU; ++i)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc = fmaf(x[i][e], x[i][e], acc);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            const float rstd = rsqrtf(acc / static_cast<float>(nh * D) + a.eps);
+#pragma unroll
+            for (int i = 0; i < NU; ++i) {
+                const int U = lane + 32 * i;
+                if (U < nunits) {
+                    const int head = U / kLph;
+                    float g0[8], g1[8];
+                    load8(w + head * D + va * 8, g0);
+                    load8(w + head * D + vb * 8, g1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        x[i][e] *= rstd * g0[e];
+                        x[i][8 + e] *= rstd * g1[e];
+                    }
+                }
+            }
+        } else if (a.mode == QKN_LN_PER_HEAD) {
+#pragma unroll
+            for (int i = 0; i < NU; ++i) {
+                float sum = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) sum += x[i][e];
+#pragma unroll
+                for (int o = kLph / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                const float mean = sum / static_cast<float>(D);
+                float sq = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float c = x[i][e] - mean;
+                    sq = fmaf(c, c, sq);
+                }
+#pragma unroll
+                for (int o = kLph / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                const float rstd = rsqrtf(sq / static_cast<float>(D) + a.eps);
+                const int U = lane + 32 * i;
+                if (U < nunits) {
+                    const int head = U / kLph;
+                    float g0[8], g1[8];
+                    load8(w + head * D + va * 8, g0);  // gamma [nh, D]
+                    load8(w + head * D + vb * 8, g1);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        x[i][e] = (x[i][e] - mean) * rstd * g0[e];
+                        x[i][8 + e] = (x[i][8 + e] - mean) * rstd * g1[e];
+                    }
+                }
+            }
+        }
+        if (rot) {
+            float c[8], sn[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rope_cos_sin(rp, s, u * 8 + e, c[e], sn[e]);
+#pragma unroll
+            for (int i = 0; i < NU; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float x0 = x[i][e], x1 = x[i][8 + e];
+                    x[i][e] = x0 * c[e] - x1 * sn[e];
+                    x[i][8 + e] = x1 * c[e] + x0 * sn[e];
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < NU; ++i) {
+            const int U = lane + 32 * i;
+            if (U < nunits) {
+                T* row = base + ((static_cast<int64_t>(b) * nh + U / kLph) * a.S + s) * D;
+                store8(row + va * 8, *reinterpret_cast<const float(*)[8]>(&x[i][0]));
+                store8(row + vb * 8, *reinterpret_cast<const float(*)[8]>(&x[i][8]));
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
 
-    float x[NU][16];
-#pragma unroll
-    for (int i = 0; i < NU; ++i) {
-        const int U = lane + 32 * i;
-        const int head = U / kLph;
-        if (U < nunits) {
-            const T* row = base + ((static_cast<int64_t>(b) * nh + head) * a.S + s) * D;
-            float f0[8], f1[8];
-            load8(row + va * 8, f0);
-            load8(row + vb * 8, f1);
-            if (bias) {
-                float b0[8], b1[8];
-                load8(bias + head * D + va * 8, b0);
-                load8(bias + head * D + vb * 8, b1);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    f0[e] += b0[e];
-                    f1[e] += b1[e];
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                x[i][e] = f0[e];
-                x[i][8 + e] = f1[e];
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[i][e] = 0.f;
-        }
+template <typename T, int D, int NU>
+void launch_unit(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s, int64_t warps) {
+    using Cfg = UnitCfg<NU>;
+    auto kern = qk_unit_kernel<T, D, NU>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+        attr_set = true;
     }
-    if (a.mode == QKN_RMS_FULL) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < NU; ++i)
-#pragma unroll
-            for (int e = 0; e < 16; ++e) acc = fmaf(x[i][e], x[i][e], acc);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        const float rstd = rsqrtf(acc / static_cast<float>(nh * D) + a.eps);
-#pragma unroll
-        for (int i = 0; i < NU; ++i) {
-            const int U = lane + 32 * i;
-            if (U < nunits) {
-                const int head = U / kLph;
-                float g0[8], g1[8];
-                load8(w + head * D + va * 8, g0);
-                load8(w + head * D + vb * 8, g1);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[i][e] *= rstd * g0[e];
-                    x[i][8 + e] *= rstd * g1[e];
-                }
-            }
-        }
-    } else if (a.mode == QKN_LN_PER_HEAD) {
-#pragma unroll
-        for (int i = 0; i < NU; ++i) {
-            float sum = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sum += x[i][e];
-#pragma unroll
-            for (int o = kLph / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            const float mean = sum / static_cast<float>(D);
-            float sq = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float c = x[i][e] - mean;
-                sq = fmaf(c, c, sq);
-            }
-#pragma unroll
-            for (int o = kLph / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            const float rstd = rsqrtf(sq / static_cast<float>(D) + a.eps);
-            const int U = lane + 32 * i;
-            if (U < nunits) {
-                const int head = U / kLph;
-                float g0[8], g1[8];
-                load8(w + head * D + va * 8, g0);  // gamma [nh, D]
-                load8(w + head * D + vb * 8, g1);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[i][e] = (x[i][e] - mean) * rstd * g0[e];
-                    x[i][8 + e] = (x[i][8 + e] - mean) * rstd * g1[e];
-                }
-            }
-        }
-    }
-    if (rot) {
-        float c[8], sn[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) rope_cos_sin(rp, s, u * 8 + e, c[e], sn[e]);
-#pragma unroll
-        for (int i = 0; i < NU; ++i)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float x0 = x[i][e], x1 = x[i][8 + e];
-                x[i][e] = x0 * c[e] - x1 * sn[e];
-                x[i][8 + e] = x1 * c[e] + x0 * sn[e];
-            }
-    }
-#pragma unroll
-    for (int i = 0; i < NU; ++i) {
-        const int U = lane + 32 * i;
-        if (U < nunits) {
-            T* row = base + ((static_cast<int64_t>(b) * nh + U / kLph) * a.S + s) * D;
-            store8(row + va * 8, *reinterpret_cast<const float(*)[8]>(&x[i][0]));
-            store8(row + vb * 8, *reinterpret_cast<const float(*)[8]>(&x[i][8]));
-        }
-    }
+    // persistent: as many 4-warp blocks as fit (shared memory bound) on every SM
+    const int per_sm = (200 * 1024) / Cfg::kSmem > 0 ? (200 * 1024) / Cfg::kSmem : 1;
+    int64_t blocks = (warps + 3) / 4;
+    const int64_t cap = static_cast<int64_t>(per_sm < 8 ? per_sm : 8) * a.num_sms;
+    if (blocks > cap) blocks = cap;
+    kern<<<static_cast<unsigned>(blocks), 128, Cfg::kSmem, s>>>(a, rp);
 }
 
 template <typename T, int D>
 bool launch_unit_d(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
     const int nunits = (a.H > a.Hk ? a.H : a.Hk) * (D / 16);
     const int64_t warps = static_cast<int64_t>(a.B) * a.S * (a.Hk > 0 ? 2 : 1);
-    const int64_t blocks = (warps + 3) / 4;
-    if (nunits > 256 || blocks > 0x7fffffff || warps > 0x7fffffff) return false;
-    const unsigned g = static_cast<unsigned>(blocks);
-    if (nunits <= 32) qk_unit_kernel<T, D, 1><<<g, 128, 0, s>>>(a, rp);
-    else if (nunits <= 64) qk_unit_kernel<T, D, 2><<<g, 128, 0, s>>>(a, rp);
-    else if (nunits <= 128) qk_unit_kernel<T, D, 4><<<g, 128, 0, s>>>(a, rp);
-    else qk_unit_kernel<T, D, 8><<<g, 128, 0, s>>>(a, rp);
+    if (nunits > 256 || warps > 0x7fffffff || a.num_sms <= 0) return false;
+    if (nunits <= 32) launch_unit<T, D, 1>(a, rp, s, warps);
+    else if (nunits <= 64) launch_unit<T, D, 2>(a, rp, s, warps);
+    else if (nunits <= 128) launch_unit<T, D, 4>(a, rp, s, warps);
+    else launch_unit<T, D, 8>(a, rp, s, warps);
     return true;
 }
 
