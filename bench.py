@@ -45,7 +45,11 @@ _KERNEL_SOURCES = {
     "gemm": ("alibi_attention_block_gb300/csrc/gemm.cu", "alibi_attention_block_gb300/csrc/common.cuh",
              "alibi_attention_block_gb300/csrc/internal.h"),
 }
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/gemm_gate_up_and_down_stablelm2_1p6b.md: 80.16 MB read + 63.29 MB written
+    "mlp_up": {"kind": "gemm", "bytes": 143453184,
+               "sha256": "91fc6fa84aca5b434a5e08ab5dc006bb1c739059d7e8b1c72b942693e82c101b"},
+}
 
 
 def _sources_sha(kind: str) -> str:
