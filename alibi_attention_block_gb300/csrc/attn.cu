@@ -482,7 +482,7 @@ template <typename T>
 cudaError_t launch_t(DType dt, const AttnArgs& a, cudaStream_t s) {
     switch (a.d) {
         case 64: return launch_attention_pair64(dt, a, s);
-        case 128: return launch_a<T, 128>(dt, a, s);
+        case 128: return launch_attention_pair128(dt, a, s);
         case 160: return launch_a<T, 160>(dt, a, s);
         default: return cudaErrorInvalidValue;
     }

@@ -84,8 +84,9 @@ struct AttnArgs {
     int num_sms;          // persistent grid size
 };
 cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s);
-// head_dim 64: the paired-query-tile kernel (attn_pair.cu)
+// head_dim 64 / 128: the paired-query-tile kernels (attn_pair.cu, attn_pair128.cu)
 cudaError_t launch_attention_pair64(DType dt, const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_attention_pair128(DType dt, const AttnArgs& a, cudaStream_t s);
 
 // ---- K6: decode-step attention over a KV cache (attn_decode.cu)
 struct DecodeArgs {

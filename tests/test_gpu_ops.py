@@ -196,6 +196,8 @@ ATTN_CASES = [
     (1, 2, 2, 129, 64, True),      # second query tile of one row
     (4, 16, 4, 1152, 64, False),   # more items than SMs: several items per CTA
     (1, 2, 2, 333, 128, False),
+    (2, 16, 4, 1536, 128, False),  # more items than SMs at head_dim 128, GQA
+    (1, 3, 3, 640, 128, False),    # odd tile count: the last pair has one query tile
     (1, 4, 4, 256, 128, True),
     (1, 4, 1, 300, 160, False),
     (2, 2, 2, 129, 160, False),
