@@ -1,34 +1,34 @@
 // K3 at head_dim 128: causal softmax attention on tcgen05 tensor cores, two
-// 128-query tiles per work item (the structure of attn_pair.cu, head_dim 64).
+// 128-query tiles per work item (as attn_pair.cu does at head_dim 64).
 //
-// At head_dim 128 a 128x128 score tile carries twice the MMA work of head_dim
-// 64 against the same exponentials, and S, P and O no longer fit 512 TMEM
-// columns twice over: P is written over its own tile's S (bf16 pairs in S's
-// first 64 columns). A query tile's chain is therefore serial:
-//     softmax(j) writes P_x(j) -> O_x += P_x(j) V_j -> S_x(j+1) = Q_x K_{j+1}^T
-// (the next QK^T is issued once the PV that reads P has completed, since it
-// overwrites P), and the tensor core runs the other query tile's chain in
-// between. Items are (query-tile pair, batch, head) as in attn_pair.cu.
+// At head_dim 128 two query tiles' S, P and O do not fit 512 TMEM columns
+// twice over, so the tiles share one S buffer: S [0, 128) holds S_A or S_B,
+// P_A [128, 192) and P_B [192, 256) (bf16 pairs), O_A [256, 384),
+// O_B [384, 512). One thread issues every MMA in a fixed order,
+//     S_A(0), S_B(0), then per key tile j:
+//     PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+// so each QK^T follows the other tile's PV: by the time the tensor core is
+// free for S_x(j+1), the other tile's softmax has read S out of the shared
+// buffer, and each PV finds its P written while the tensor core ran the
+// other tile's PV and QK^T.
 // 12 warps:
 //   warp 0      TMA: each query tile's Q (its own buffer, reloaded once the
 //               tile's last QK^T of the item has completed), K and V tiles of
 //               128 keys into a two-stage ring (128-byte swizzle, 64-column
 //               boxes, zero fill past S).
-//   warps 1, 2  one MMA-issuing thread per query tile: S (M=128, N=128,
-//               K=128: Q and K K-major in shared memory), PV (N=128: P from
-//               TMEM, V MN-major). Warp 1 also allocates TMEM.
-//   warp 3      idle.
+//   warp 1      TMEM allocator and MMA issuer: S (M=128, N=128, K=128: Q and
+//               K K-major in shared memory), PV (N=128: P from TMEM, V
+//               MN-major).
+//   warps 2, 3  idle.
 //   warps 4..7  softmax of tile A, 8..11 of tile B, one thread per query row:
-//               one tcgen05.ld of the row's 128 scores, causal mask on the
-//               diagonal (and ragged last) tile, 3-input max, paired f32x2 FMA
-//               into ex2 (scale log2(e)/sqrt(d); ALiBi as +slope*key), P
-//               packed to the storage type and stored over S; O rescaled in
-//               TMEM when the running max grows by more than 2^8. The
-//               previous PV has always completed when S is ready, so the
-//               softmax never waits for it. An item's O / l is read out
-//               during the warpgroup's first tile of its next item.
-// TMEM columns: S_A (and P_A) [0, 128), S_B (and P_B) [128, 256),
-// O_A [256, 384), O_B [384, 512).
+//               one tcgen05.ld of the row's 128 scores (the shared S is
+//               released at once), causal mask on the diagonal (and ragged
+//               last) tile, 3-input max, paired f32x2 FMA into ex2 (scale
+//               log2(e)/sqrt(d); ALiBi as +slope*key), P packed to the storage
+//               type in registers; once the previous PV has read P_x, one
+//               64-column store, and O rescaled in TMEM when the running max
+//               grew by more than 2^8. An item's O / l is read out during the
+//               warpgroup's first tile of its next item.
 // Query scale head_dim^-0.5 and GQA (kv head = h / (H/Hk)) follow nnterp
 // "stablelm" 03 Notes; ALiBi "Bloom in a sovereign engine", Contribution.
 #include "internal.h"
@@ -43,7 +43,7 @@ constexpr int kTK = 128;
 constexpr int D = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr uint32_t kLaunchRegs = 168, kRegsControl = 64, kRegsSoftmax = 208;
+constexpr uint32_t kLaunchRegs = 168, kRegsControl = 96, kRegsSoftmax = 192;
 
 struct Cfg {
     static constexpr int kSub = D / 64;
@@ -53,6 +53,7 @@ struct Cfg {
     static constexpr int kOffKV = 2 * kQBytes;         // Q_A, Q_B
     static constexpr int kOffBar = kOffKV + kStages * 2 * kKVBytes;
     static constexpr int kSmem = kOffBar + 256 + 1024;
+    static constexpr uint32_t kColP = 128;             // P_x at kColP + 64 x
     static constexpr uint32_t kColO = 256;             // O_x at kColO + D x
     static constexpr uint32_t kTmemCols = 512;
 };
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kP128Threads, 1)
     const uint32_t sKV = sQ + Cfg::kOffKV;  // stage s: K at 2s, V at 2s + 1 tiles
     const uint32_t bar0 = sQ + Cfg::kOffBar;
     auto s_full = [&](int x) { return bar0 + 8u * x; };
+    const uint32_t s_free = bar0 + 96u + 32u * kStages;  // the shared S buffer was read
     auto p_full = [&](int x) { return bar0 + 16u + 8u * x; };
     auto pv_done = [&](int x) { return bar0 + 32u + 8u * x; };
     auto o_free = [&](int x) { return bar0 + 48u + 8u * x; };
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(kP128Threads, 1)
     auto v_full = [&](int i) { return bar0 + 96u + 8u * (kStages + i); };
     auto k_empty = [&](int i) { return bar0 + 96u + 8u * (2 * kStages + i); };
     auto v_empty = [&](int i) { return bar0 + 96u + 8u * (3 * kStages + i); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 96 + 32 * kStages);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffBar + 104 + 32 * kStages);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
@@ -130,9 +132,10 @@ __global__ void __launch_bounds__(kP128Threads, 1)
         for (int i = 0; i < kStages; ++i) {
             mbar_init(k_full(i), 1);
             mbar_init(v_full(i), 1);
-            mbar_init(k_empty(i), 2);
-            mbar_init(v_empty(i), 2);
+            mbar_init(k_empty(i), 1);
+            mbar_init(v_empty(i), 1);
         }
+        mbar_init(s_free, 4);
         fence_barrier_init();
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -195,88 +198,110 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                 }
                 c.next(a, nq, np, n_items);
             }
-        } else if ((warp == 1 || warp == 2) && lane == 0) {
-            const int x = warp - 1;
+        } else if (warp == 1 && lane == 0) {
             constexpr uint32_t fmt = dt_traits<T>::mma_fmt;
             constexpr uint32_t idesc_s = make_idesc_f16(fmt, kTQ, kTK, false);
             constexpr uint32_t idesc_o = make_idesc_f16(fmt, kTQ, D, true);
             constexpr uint64_t kStageStep = (2 * Cfg::kKVBytes) >> 4;
             constexpr uint64_t kAtom = (kTQ * 128) >> 4;
-            const uint64_t dq = make_sdesc_sw128(sQ + x * Cfg::kQBytes, 16, 1024);
+            constexpr uint64_t kQStep = Cfg::kQBytes >> 4;
+            const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024);
             const uint64_t dk0 = make_sdesc_sw128(sKV, 16, 1024);
             const uint64_t dv0 = make_sdesc_sw128(sKV + Cfg::kKVBytes, kTK * 128, 1024);
-            const uint32_t tS = tmem_base + 128u * x;  // P_x lives in S_x's first 64 columns
-            const uint32_t tO = tmem_base + Cfg::kColO + D * x;
-            int gs = 0, gp = 0, itx = 0;
-            // S_x = Q_x K^T. It overwrites P_x, so the previous PV of this
-            // query tile must have completed.
-            auto issue_s = [&](uint64_t dk) -> bool {
-                if (gp > 0 && !mbar_wait_inl(pv_done(x), (gp - 1) & 1, a.err)) return false;
+            int ns = 0;                 // S products issued (the shared buffer's fills)
+            int gp[2] = {0, 0};         // PV products issued per query tile
+            int itx[2] = {0, 0};        // items started per query tile
+            // S_x = Q_x K^T into the shared buffer once the previous S has been read
+            auto issue_s = [&](int x, int st) -> bool {
+                if (ns > 0 && !mbar_wait_inl(s_free, (ns - 1) & 1, a.err)) return false;
                 tc_fence_after();
+                const uint64_t dq = dq0 + x * kQStep, dk = dk0 + st * kStageStep;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint64_t off = (ks / 4) * kAtom + (ks % 4) * 2;
-                    tc_mma_ss(tS, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
+                    tc_mma_ss(tmem_base, dq + off, dk + off, idesc_s, ks > 0 ? 1u : 0u);
                 }
                 tc_commit(s_full(x));
-                ++gs;
+                ++ns;
                 return true;
             };
-            auto issue_pv = [&](uint64_t dv, bool first) -> bool {
-                if (!mbar_wait_inl(p_full(x), gp & 1, a.err)) return false;
-                if (first && itx > 0 && !mbar_wait_inl(o_free(x), (itx - 1) & 1, a.err))
-                    return false;
+            // O_x += P_x V once the softmax has written P_x (the first PV of an
+            // item overwrites O_x, so it also waits for the previous read-out)
+            auto issue_pv = [&](int x, int st, bool first) -> bool {
+                if (!mbar_wait_inl(p_full(x), gp[x] & 1, a.err)) return false;
+                if (first) {
+                    if (itx[x] > 0 && !mbar_wait_inl(o_free(x), (itx[x] - 1) & 1, a.err))
+                        return false;
+                    ++itx[x];
+                }
                 tc_fence_after();
+                const uint32_t tP = tmem_base + Cfg::kColP + 64u * x;
+                const uint32_t tO = tmem_base + Cfg::kColO + D * x;
+                const uint64_t dv = dv0 + st * kStageStep;
 #pragma unroll
                 for (int ks = 0; ks < kTK / 16; ++ks)
-                    tc_mma_ts(tO, tS + ks * 8, dv + ks * ((16 * 128) >> 4), idesc_o,
+                    tc_mma_ts(tO, tP + ks * 8, dv + ks * ((16 * 128) >> 4), idesc_o,
                               (!first || ks > 0) ? 1u : 0u);
                 tc_commit(pv_done(x));
-                ++gp;
+                ++gp[x];
                 return true;
             };
             PairCursor c;
             c.start(a, nq, np, n_items);
             int gkv = 0;
+            int itq[2] = {0, 0};
             bool ok = true;
-            while (ok && c.valid) {
-                const int nx = x ? c.nB : c.nA, nkv = c.n_kv();
-                if (nx > 0 && !mbar_wait_inl(q_full(x), itx & 1, a.err)) break;
-                {
-                    const int st = gkv % kStages;
-                    if (!mbar_wait_inl(k_full(st), (gkv / kStages) & 1, a.err)) break;
-                    if (nx > 0 && !issue_s(dk0 + st * kStageStep)) break;
-                    tc_commit(k_empty(st));
-                    if (nx == 1) tc_commit(q_empty(x));
+            auto s_step = [&](int x, int j, int nx, int gj) -> bool {
+                // QK^T of key tile j for query tile x (K slot gj already waited)
+                if (j >= nx) return true;
+                if (j == 0 && !mbar_wait_inl(q_full(x), itq[x] & 1, a.err)) return false;
+                if (!issue_s(x, gj % kStages)) return false;
+                if (j == nx - 1) {
+                    tc_commit(q_empty(x));
+                    ++itq[x];
                 }
+                return true;
+            };
+            while (ok && c.valid) {
+                const int nA = c.nA, nB = c.nB, nkv = c.n_kv();
+                // key tile 0: S_A(0), S_B(0)
+                if (!mbar_wait_inl(k_full(gkv % kStages), (gkv / kStages) & 1, a.err)) break;
+                if (!s_step(0, 0, nA, gkv) || !s_step(1, 0, nB, gkv)) break;
+                tc_commit(k_empty(gkv % kStages));
                 for (int j = 0; j < nkv; ++j) {
                     const int gj = gkv + j;
                     const int stj = gj % kStages;
+                    const bool more = j + 1 < nkv;
                     if (!mbar_wait_inl(v_full(stj), (gj / kStages) & 1, a.err)) {
                         ok = false;
                         break;
                     }
-                    if (j < nx && !issue_pv(dv0 + stj * kStageStep, j == 0)) {
+                    if (more && !mbar_wait_inl(k_full((gj + 1) % kStages),
+                                               ((gj + 1) / kStages) & 1, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    // PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+                    if (j < nA && !issue_pv(0, stj, j == 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (more && !s_step(0, j + 1, nA, gj + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j < nB && !issue_pv(1, stj, j == 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (more && !s_step(1, j + 1, nB, gj + 1)) {
                         ok = false;
                         break;
                     }
                     tc_commit(v_empty(stj));
-                    if (j + 1 < nkv) {
-                        const int stn = (gj + 1) % kStages;
-                        if (!mbar_wait_inl(k_full(stn), ((gj + 1) / kStages) & 1, a.err)) {
-                            ok = false;
-                            break;
-                        }
-                        if (j + 1 < nx && !issue_s(dk0 + stn * kStageStep)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_commit(k_empty(stn));
-                        if (j + 2 == nx) tc_commit(q_empty(x));
-                    }
+                    if (more) tc_commit(k_empty((gj + 1) % kStages));
                 }
                 gkv += nkv;
-                if (nx > 0) ++itx;
                 c.next(a, nq, np, n_items);
             }
         }
@@ -286,7 +311,8 @@ __global__ void __launch_bounds__(kP128Threads, 1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tS = tmem_base + 128u * x;
+        const uint32_t tS = tmem_base;  // shared by both query tiles
+        const uint32_t tP = tmem_base + Cfg::kColP + 64u * x;
         const uint32_t tO = tmem_base + Cfg::kColO + D * x;
         const float scale_l2 = a.scale * kLog2e;
         PairCursor c;
@@ -296,8 +322,8 @@ __global__ void __launch_bounds__(kP128Threads, 1)
         bool pend = false;
         float pend_l = 0.f;
         int64_t pend_row = -1;
-        // O / l of the previous item, 32 columns at a time (O is final: this
-        // query tile's next QK^T was issued after its last PV completed)
+        // O / l of the previous item, 32 columns at a time, once its last PV
+        // has completed
         auto flush = [&]() {
             const float inv_l = 1.0f / pend_l;
 #pragma unroll 1
@@ -339,15 +365,11 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                     break;
                 }
                 tc_fence_after();
-                if (j == 0 && pend) {
-                    flush();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(o_free(x));
-                    pend = false;
-                }
                 uint32_t r[kTK];
                 tmem_ld128(tS + lane_off, r);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
                 const int kbase = j * kTK;
                 if constexpr (ALIBI) {
                     const float sk = slope_l2 * static_cast<float>(kbase);
@@ -394,8 +416,24 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                     pk[k / 2] = dt_traits<T>::pack2(p0, p1);
                     pk[k / 2 + 1] = dt_traits<T>::pack2(p2, p3);
                 }
-                // P over S (S is in registers); O rescaled if the max moved
-                tmem_st64_nowait(tS + lane_off, pk);
+                // the previous PV has read P_x and O_x is settled: read out the
+                // previous item's O if pending, publish P_x, rescale O if the
+                // max moved (before this tile's PV)
+                if (j > 0 || pend) {
+                    if (!mbar_wait_inl(pv_done(x), (g - 1) & 1, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (j == 0 && pend) {
+                    flush();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(o_free(x));
+                    pend = false;
+                }
+                tmem_st64_nowait(tP + lane_off, pk);
                 if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
 #pragma unroll 1
                     for (int cc = 0; cc < D / 16; ++cc) {
@@ -423,9 +461,8 @@ __global__ void __launch_bounds__(kP128Threads, 1)
             pend_row = qpos < a.S ? (static_cast<int64_t>(c.b) * a.S + qpos) * a.H + c.h : -1;
             c.next(a, nq, np, n_items);
         }
-        // the last item's O: its PV must complete first (no later QK^T here)
+        // the last item's O
         if (ok && pend) {
-            // this query tile's PV count equals its tile count g
             if (mbar_wait_inl(pv_done(x), (g - 1) & 1, a.err)) {
                 tc_fence_after();
                 flush();
