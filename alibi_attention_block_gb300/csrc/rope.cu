@@ -20,6 +20,7 @@ namespace blk {
 namespace {
 
 constexpr int kRopeThreads = 128;
+constexpr int kRopeBatch = 8;  // 16-byte loads in flight per thread and round
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -34,9 +35,9 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kRopeThreads) qk_norm_rope_kernel(QkNormRopeArgs a,
-                                                                    RopeParams rp) {
-    extern __shared__ float buf[];  // (H + Hk) * d floats
+__global__ void __launch_bounds__(kRopeThreads, 5) qk_norm_rope_kernel(QkNormRopeArgs a,
+                                                                       RopeParams rp) {
+    extern __shared__ float buf[];  // (H + Hk) * d floats, then cos[r/2], sin[r/2]
     __shared__ float red[kRopeThreads / 32];
     const int token = blockIdx.x;
     const int b = token / a.S;
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(kRopeThreads) qk_norm_rope_kernel(QkNormRopeAr
     const int nh = a.H + a.Hk;
     const int nvec = nh * d / 8;
     const int vpr = d / 8;  // vectors per head row
+    const int half = rp.span / 2;
+    float* cs_tab = buf + nh * d;
 
     auto row_ptr = [&](int head) -> T* {
         if (head < a.H)
@@ -53,21 +56,51 @@ __global__ void __launch_bounds__(kRopeThreads) qk_norm_rope_kernel(QkNormRopeAr
                ((static_cast<int64_t>(b) * a.Hk + (head - a.H)) * a.S + s) * d;
     };
 
-    // 1. load (+ bias)
-    for (int i = threadIdx.x; i < nvec; i += kRopeThreads) {
-        const int head = i / vpr;
-        const int c = (i % vpr) * 8;
-        float f[8];
-        load8(row_ptr(head) + c, f);
-        const T* bias = head < a.H ? static_cast<const T*>(a.q_bias) : static_cast<const T*>(a.k_bias);
-        if (bias) {
-            float bb[8];
-            load8(bias + (head < a.H ? head : head - a.H) * d + c, bb);
+    // 0. cos / sin of this token's position, shared by every head
+    for (int j = threadIdx.x; j < half; j += kRopeThreads)
+        rope_cos_sin(rp, s, j, cs_tab[j], cs_tab[half + j]);
+
+    // 1. load (+ bias): in rounds of kRopeBatch 16-byte vectors per thread,
+    // every load of a round (and its bias vector) issued before any is used,
+    // so a token's rows cost one memory latency, not one per vector
+    const T* q_bias = static_cast<const T*>(a.q_bias);
+    const T* k_bias = static_cast<const T*>(a.k_bias);
+    for (int base = 0; base < nvec; base += kRopeThreads * kRopeBatch) {
+        uint4 raw[kRopeBatch], rb[kRopeBatch];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] += bb[e];
+        for (int t = 0; t < kRopeBatch; ++t) {
+            const int i = base + t * kRopeThreads + static_cast<int>(threadIdx.x);
+            raw[t] = make_uint4(0u, 0u, 0u, 0u);
+            rb[t] = raw[t];
+            if (i < nvec) {
+                const int head = i / vpr;
+                const int c = (i - head * vpr) * 8;
+                raw[t] = *reinterpret_cast<const uint4*>(row_ptr(head) + c);
+                const T* bias = head < a.H ? q_bias : k_bias;
+                if (bias)
+                    rb[t] = *reinterpret_cast<const uint4*>(
+                        bias + (head < a.H ? head : head - a.H) * d + c);
+            }
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) buf[head * d + c + e] = f[e];
+        for (int t = 0; t < kRopeBatch; ++t) {
+            const int i = base + t * kRopeThreads + static_cast<int>(threadIdx.x);
+            if (i < nvec) {
+                const uint32_t w[4] = {raw[t].x, raw[t].y, raw[t].z, raw[t].w};
+                const uint32_t wb[4] = {rb[t].x, rb[t].y, rb[t].z, rb[t].w};
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 v = dt_traits<T>::unpack2(w[e]);
+                    const float2 vb = dt_traits<T>::unpack2(wb[e]);
+                    f[2 * e] = v.x + vb.x;
+                    f[2 * e + 1] = v.y + vb.y;
+                }
+                float4* dst = reinterpret_cast<float4*>(buf + i * 8);  // = head * d + c
+                dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+                dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
     }
     __syncthreads();
 
@@ -113,13 +146,11 @@ __global__ void __launch_bounds__(kRopeThreads) qk_norm_rope_kernel(QkNormRopeAr
     }
 
     // 3. rotary over the first rp.span dims of every q and k head
-    const int half = rp.span / 2;
     if (half > 0) {
         for (int i = threadIdx.x; i < nh * half; i += kRopeThreads) {
             const int head = i / half;
-            const int j = i % half;
-            float c, sn;
-            rope_cos_sin(rp, s, j, c, sn);
+            const int j = i - head * half;
+            const float c = cs_tab[j], sn = cs_tab[half + j];
             float* r = buf + head * d;
             const float x1 = r[j], x2 = r[j + half];
             r[j] = x1 * c - x2 * sn;
@@ -481,6 +512,181 @@ bool launch_unit_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_
     return false;
 }
 
+// Head-row path (any head_dim d <= 256 with d % 8 == 0; per-head LayerNorm
+// or none): a CTA per token. Its q and k rows are first copied into shared
+// memory with cp.async by all threads (one memory latency per token, no
+// registers held for data in flight); then each warp takes head rows warp,
+// warp + 8, ... (q heads, then k heads), lane l holding the row's 16-byte
+// vector l (dims 8l .. 8l + 7), so the per-head LayerNorm is a warp
+// reduction. The rotary partner of dim g (g + r/2 for g < r/2, g - r/2 for
+// r/2 <= g < r) lies (g +- r/2) / 8 lanes away at slot (g +- r/2) mod 8: with
+// HM = (r/2) mod 8 a template parameter the slot is a compile-time register
+// and only the lane offset is computed. cos / sin of the token's position
+// come from a shared table filled once per token.
+constexpr int kHeadWarps = 8;
+
+template <typename T, int HM>
+__global__ void __launch_bounds__(kHeadWarps * 32) qk_head_kernel(QkNormRopeArgs a,
+                                                                  RopeParams rp) {
+    __shared__ float cs_tab[2 * kMaxRotaryPairs];  // cos[r/2], then sin[r/2]
+    extern __shared__ __align__(16) uint8_t rows[];  // (H + Hk) rows of d values
+    const int token = blockIdx.x;
+    const int b = token / a.S;
+    const int s = token - b * a.S;
+    const int d = a.d;
+    const int nv = d / 8;
+    const int nh = a.H + a.Hk;
+    const int half = rp.span / 2;
+    const int hq = half >> 3;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool active = lane < nv;
+    const bool ln = a.mode == QKN_LN_PER_HEAD;
+    auto row_ptr = [&](int head) -> T* {
+        if (head < a.H)
+            return static_cast<T*>(a.q) + ((static_cast<int64_t>(b) * a.H + head) * a.S + s) * d;
+        return static_cast<T*>(a.k) +
+               ((static_cast<int64_t>(b) * a.Hk + (head - a.H)) * a.S + s) * d;
+    };
+    const uint32_t srow = smem_u32(rows);
+    if (active)
+        for (int head = warp; head < nh; head += kHeadWarps)
+            cp_async16(srow + (head * nv + lane) * 16, row_ptr(head) + lane * 8, 16u);
+    cp_async_commit();
+    for (int j = threadIdx.x; j < half; j += kHeadWarps * 32)
+        rope_cos_sin(rp, s, j, cs_tab[j], cs_tab[kMaxRotaryPairs + j]);
+    __syncthreads();
+    // this lane's rotary coefficients, the same for every head of the token:
+    // x'_g = x_g c_g + x_{g+r/2} f_g + x_{g-r/2} b_g, with f = -sin for
+    // g < r/2, b = +sin for r/2 <= g < r, zero otherwise (the direction is
+    // data, not a predicate kept live across the head loop). With (r/2) mod 8
+    // = 0 or 4 both partners sit in the same slot: one shuffle from the lane
+    // src_l serves either direction.
+    float rot_c[8], rot_f[8], rot_b[8];
+    int src_l[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int g = lane * 8 + e;
+        rot_c[e] = 1.f;
+        rot_f[e] = 0.f;
+        rot_b[e] = 0.f;
+        src_l[e] = lane - hq - (e < HM ? 1 : 0);
+        if (g < half) {
+            rot_c[e] = cs_tab[g];
+            rot_f[e] = -cs_tab[kMaxRotaryPairs + g];
+            src_l[e] = lane + hq + ((e + HM) >> 3);
+        } else if (g < 2 * half) {
+            rot_c[e] = cs_tab[g - half];
+            rot_b[e] = cs_tab[kMaxRotaryPairs + g - half];
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int head = warp; head < nh; head += kHeadWarps) {
+        const bool isq = head < a.H;
+        const int hh = isq ? head : head - a.H;
+        const T* bias = static_cast<const T*>(isq ? a.q_bias : a.k_bias);
+        uint4 rb = make_uint4(0u, 0u, 0u, 0u), rg = rb, raw = rb;
+        if (active) {
+            if (bias) rb = *reinterpret_cast<const uint4*>(bias + hh * d + lane * 8);
+            if (ln)
+                rg = *reinterpret_cast<const uint4*>(static_cast<const T*>(isq ? a.q_w : a.k_w) +
+                                                     hh * d + lane * 8);
+            raw = ld_shared_u4(srow + (head * nv + lane) * 16);
+        }
+        float x[8];
+        {
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            const uint32_t wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 v = dt_traits<T>::unpack2(w[e]);
+                const float2 vb = dt_traits<T>::unpack2(wb[e]);
+                x[2 * e] = v.x + vb.x;
+                x[2 * e + 1] = v.y + vb.y;
+            }
+        }
+        if (ln) {
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sum += x[e];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float mean = sum / static_cast<float>(d);
+            float sq = 0.f;
+            if (active) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float c = x[e] - mean;
+                    sq = fmaf(c, c, sq);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            const float rstd = rsqrtf(sq / static_cast<float>(d) + a.eps);
+            const uint32_t wg[4] = {rg.x, rg.y, rg.z, rg.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 g = dt_traits<T>::unpack2(wg[e]);
+                x[2 * e] = (x[2 * e] - mean) * rstd * g.x;
+                x[2 * e + 1] = (x[2 * e + 1] - mean) * rstd * g.y;
+            }
+        }
+        if (half > 0) {
+            // every lane takes part in the shuffles; past r the coefficients
+            // are (1, 0). With (r/2) mod 8 = 0 or 4 both partners sit in the
+            // same slot, so one shuffle per slot serves both directions.
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if constexpr ((HM & 3) == 0) {
+                    const float p = __shfl_sync(0xffffffffu, x[(e + HM) & 7], src_l[e]);
+                    y[e] = fmaf(p, rot_f[e] + rot_b[e], x[e] * rot_c[e]);
+                } else {
+                    const float pf = __shfl_sync(0xffffffffu, x[(e + HM) & 7],
+                                                 lane + hq + ((e + HM) >> 3));
+                    const float pb = __shfl_sync(0xffffffffu, x[(e + 8 - HM) & 7],
+                                                 lane - hq - (e < HM ? 1 : 0));
+                    y[e] = fmaf(pb, rot_b[e], fmaf(pf, rot_f[e], x[e] * rot_c[e]));
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = y[e];
+        }
+        if (active) store8(row_ptr(head) + lane * 8, x);
+    }
+}
+
+template <typename T, int HM>
+void launch_head(unsigned grid, size_t smem, const QkNormRopeArgs& a, const RopeParams& rp,
+                 cudaStream_t s) {
+    auto kern = qk_head_kernel<T, HM>;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    kern<<<grid, kHeadWarps * 32, smem, s>>>(a, rp);
+}
+
+template <typename T>
+bool launch_head_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
+    if (a.mode == QKN_RMS_FULL || a.d % 8 || a.d > 256) return false;
+    const int64_t tokens = static_cast<int64_t>(a.B) * a.S;
+    if (tokens > 0x7fffffff) return false;
+    const unsigned g = static_cast<unsigned>(tokens);
+    const size_t smem = static_cast<size_t>(a.H + a.Hk) * a.d * sizeof(T);
+    if (smem > 200 * 1024) return false;
+    switch ((rp.span / 2) & 7) {
+        case 0: launch_head<T, 0>(g, smem, a, rp, s); break;
+        case 1: launch_head<T, 1>(g, smem, a, rp, s); break;
+        case 2: launch_head<T, 2>(g, smem, a, rp, s); break;
+        case 3: launch_head<T, 3>(g, smem, a, rp, s); break;
+        case 4: launch_head<T, 4>(g, smem, a, rp, s); break;
+        case 5: launch_head<T, 5>(g, smem, a, rp, s); break;
+        case 6: launch_head<T, 6>(g, smem, a, rp, s); break;
+        default: launch_head<T, 7>(g, smem, a, rp, s); break;
+    }
+    return true;
+}
+
 template <typename T>
 bool launch_warp_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
     const int vph = a.d / 8;
@@ -510,8 +716,12 @@ cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopePar
     if (dt == DType::F16 ? launch_warp_path<__half>(a, rp, s)
                          : launch_warp_path<__nv_bfloat16>(a, rp, s))
         return cudaGetLastError();
-    // general path (e.g. head_dim 160 or spans not a multiple of 16)
-    const size_t smem = static_cast<size_t>(a.H + a.Hk) * a.d * sizeof(float);
+    if (dt == DType::F16 ? launch_head_path<__half>(a, rp, s)
+                         : launch_head_path<__nv_bfloat16>(a, rp, s))
+        return cudaGetLastError();
+    // general path (full-width RMSNorm at other head sizes or spans)
+    const size_t smem =
+        (static_cast<size_t>(a.H + a.Hk) * a.d + 2 * static_cast<size_t>(rp.span / 2)) * sizeof(float);
     if (dt == DType::F16) {
         auto k = qk_norm_rope_kernel<__half>;
         if (smem > 48 * 1024)

@@ -119,9 +119,12 @@ QKV_CASES = {
     "bloom_interleaved": (2, 130, 256, 4, 4, 64, "head_interleaved", "none", 0, 1e4, True),
     "olmo_rms_full_r128": (2, 150, 256, 2, 2, 128, "stacked", "rms_full", 128, 5e5, False),
     "gqa_ln_per_head_r40": (1, 140, 320, 8, 2, 160, "stacked", "ln_per_head", 40, 1e4, False),
+    "gqa_ln_per_head_r40_bias": (2, 70, 320, 8, 2, 160, "stacked", "ln_per_head", 40, 1e4, True),
     "full_span_r64": (1, 128, 256, 4, 4, 64, "stacked", "none", 64, 1e4, True),
     "ln_per_head_d128_r32": (1, 140, 256, 4, 2, 128, "stacked", "ln_per_head", 32, 1e4, True),
     "rms_full_d64_r16_gqa": (2, 100, 256, 8, 2, 64, "stacked", "rms_full", 16, 1e4, False),
+    "rms_full_d96_r24": (1, 90, 192, 2, 2, 96, "stacked", "rms_full", 24, 1e4, True),
+    "ln_per_head_d96_r24_bias": (1, 90, 192, 2, 1, 96, "stacked", "ln_per_head", 24, 1e4, True),
 }
 
 
@@ -172,16 +175,28 @@ def test_qkv_bias_rope_partial(dt, name):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
-@pytest.mark.parametrize("r,bias", [(16, True), (0, True), (64, False)])
-def test_rope_inplace(dt, r, bias):
-    x = draw((2, 4, 100, 64), dt, 21 + r)
-    b = draw((4 * 64,), dt, 22, "b") if bias else None
+@pytest.mark.parametrize("H,d,r,bias", [
+    (4, 64, 16, True), (4, 64, 0, True), (4, 64, 64, False),
+    # spans that are not a multiple of 16 and other head sizes take the
+    # head-row path: its rotary partner slot is (r/2) mod 8, its lane offset
+    # (r/2) / 8; the cases cover offsets 0..16 lanes and slots 0, 2, 3, 4, 5
+    (4, 64, 20, True),     # r/2 = 10: slot 2, one lane
+    (3, 96, 24, False),    # head_dim 96, r/2 = 12: slot 4
+    (72, 160, 40, True),   # 72 heads x 160: r/2 = 20, slot 4, two lanes
+    (2, 160, 160, False),  # full span at 160: slot 0, ten lanes
+    (5, 48, 6, True),      # head_dim 48 (six active lanes), r/2 = 3: slot 3, zero lanes
+    (4, 104, 26, True),    # head_dim 104, r/2 = 13: slot 5
+    (2, 256, 250, True),   # head_dim 256 (every lane active), r/2 = 125: slot 5, 15 lanes
+])
+def test_rope_inplace(dt, H, d, r, bias):
+    x = draw((2, H, 100, d), dt, 21 + r + H)
+    b = draw((H * d,), dt, 22, "b") if bias else None
     xd = to_dev(x)
     blk.rope_inplace(xd, to_dev(b), rotary_span=r, rope_base=1e4)
     ref = f64(x)
     if bias:
-        ref = ref + f64(b).reshape(4, 64)[None, :, None, :]
-    check(xd, oracle.rope(ref, np.arange(100), r, 1e4), f"rope r={r}")
+        ref = ref + f64(b).reshape(H, d)[None, :, None, :]
+    check(xd, oracle.rope(ref, np.arange(100), r, 1e4), f"rope H={H} d={d} r={r}")
 
 
 # -------------------------------------------------------------- attention --
