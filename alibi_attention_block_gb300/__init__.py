@@ -22,7 +22,7 @@ from ._abi import BlkError  # noqa: F401
 
 __all__ = ["layernorm_bias", "rmsnorm", "qkv_bias_rope_partial", "rope_inplace", "attn_prefill",
            "attn_decode", "attn_decode_workspace_size", "decode_desc",
-           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host", "ForwardGraph",
+           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host", "ForwardGraph", "HostPipe",
            "check_device_status", "BlkError", "library_path"]
 
 library_path = _abi.LIB_PATH
@@ -280,6 +280,57 @@ def forward_host(cfg, weights: dict, x_host, y_host=None, x_dev=None, y_dev=None
                                        _p(workspace), workspace.numel(), n_chunks, _dt(x_host),
                                        _stream()), "blk_forward_host")
     return y_host
+
+
+class HostPipe:
+    """Block forwards over a stream of pinned host batches (blk_host_pipe_*):
+    submit() enqueues one batch on the current stream and returns; batch n's
+    copy in overlaps batch n-1's forward and its copy out batch n+1's.
+    x_host must hold the batch at submit time; y_host is complete once the
+    stream has passed a later flush(). Host tensors must stay alive until
+    then; the pipe's device memory (staging slots and workspace) is
+    allocated here."""
+
+    def __init__(self, cfg, batch, seq, dtype=torch.bfloat16, depth=2):
+        self.desc = block_desc(cfg, batch, seq)
+        self.shape = (batch, seq, cfg.hidden)
+        self.dtype = dtype
+        n = C.c_size_t(0)
+        _abi.check(_lib().blk_host_pipe_mem_size(C.byref(self.desc), depth, C.byref(n)),
+                   "blk_host_pipe_mem_size")
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.mem = torch.empty(n.value, dtype=torch.uint8, device=dev)
+        handle = C.c_void_p()
+        dt = _abi.BLK_F16 if dtype == torch.float16 else _abi.BLK_BF16
+        _abi.check(_lib().blk_host_pipe_create(C.byref(self.desc), depth, dt, _p(self.mem),
+                                               n.value, C.byref(handle)), "blk_host_pipe_create")
+        self._h = handle
+
+    def submit(self, weights: dict, x_host, y_host):
+        for t in (x_host, y_host):
+            if t.is_cuda or not t.is_pinned() or tuple(t.shape) != self.shape or t.dtype != self.dtype:
+                raise ValueError(f"host batches must be pinned CPU tensors {self.shape} {self.dtype}")
+        unknown = set(weights) - set(_abi.WEIGHT_SLOTS)
+        if unknown:
+            raise KeyError(f"unknown weight slots: {sorted(unknown)}")
+        w = _abi.BlockWeights(*[_p(weights.get(n)) for n in _abi.WEIGHT_SLOTS])
+        _abi.check(_lib().blk_host_pipe_submit(self._h, C.byref(w), C.c_void_p(x_host.data_ptr()),
+                                               C.c_void_p(y_host.data_ptr()), _stream()),
+                   "blk_host_pipe_submit")
+
+    def flush(self):
+        _abi.check(_lib().blk_host_pipe_flush(self._h, _stream()), "blk_host_pipe_flush")
+
+    def close(self):
+        if self._h:
+            _abi.check(_lib().blk_host_pipe_destroy(self._h), "blk_host_pipe_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class ForwardGraph:

@@ -94,6 +94,12 @@ _PROTOS = {
     "blk_graph_destroy": (C.c_int, [vp]),
     "blk_forward_host": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp, vp,
                                    vp, C.c_size_t, i32, C.c_int, vp]),
+    "blk_host_pipe_mem_size": (C.c_int, [C.POINTER(BlockDesc), i32, C.POINTER(C.c_size_t)]),
+    "blk_host_pipe_create": (C.c_int, [C.POINTER(BlockDesc), i32, C.c_int, vp, C.c_size_t,
+                                       C.POINTER(vp)]),
+    "blk_host_pipe_submit": (C.c_int, [vp, C.POINTER(BlockWeights), vp, vp, vp]),
+    "blk_host_pipe_flush": (C.c_int, [vp, vp]),
+    "blk_host_pipe_destroy": (C.c_int, [vp]),
     "blk_forward_ex": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp,
                                  C.c_size_t, C.c_int, vp, C.POINTER(vp), C.c_int,
                                  C.POINTER(i32), C.POINTER(C.c_int)]),

@@ -1010,6 +1010,167 @@ blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "stream ordering");
 }
 
+constexpr int kMaxPipeDepth = 4;
+struct blk_host_pipe {
+    blk_block_desc d{};
+    blk_dtype dt = BLK_BF16;
+    int depth = 0;
+    int device = -1;
+    size_t io_bytes = 0;  // one batch of x (or y)
+    uint8_t* x_dev[kMaxPipeDepth] = {};
+    uint8_t* y_dev[kMaxPipeDepth] = {};
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    // ev_fwd[k]: the forward that last read x slot k and wrote y slot k;
+    // ev_out[k]: the copy-out that last read y slot k
+    cudaEvent_t ev_base = nullptr, ev_flush = nullptr;
+    cudaEvent_t ev_in[kMaxPipeDepth] = {}, ev_fwd[kMaxPipeDepth] = {}, ev_out[kMaxPipeDepth] = {};
+    int64_t n = 0;            // submits since create or the last flush
+    cudaStream_t s = nullptr;  // their stream
+};
+
+namespace {
+
+size_t pipe_io_bytes(const blk_block_desc* d) {
+    return align256(static_cast<size_t>(d->qkv.batch) * d->qkv.seq * d->qkv.hidden * 2);
+}
+
+blk_status pipe_release(blk_host_pipe* p) {
+    cudaError_t first = cudaSuccess;
+    auto keep = [&](cudaError_t e) {
+        if (first == cudaSuccess && e != cudaSuccess) first = e;
+    };
+    for (int k = 0; k < kMaxPipeDepth; ++k) {
+        if (p->ev_in[k]) keep(cudaEventDestroy(p->ev_in[k]));
+        if (p->ev_fwd[k]) keep(cudaEventDestroy(p->ev_fwd[k]));
+        if (p->ev_out[k]) keep(cudaEventDestroy(p->ev_out[k]));
+    }
+    if (p->ev_base) keep(cudaEventDestroy(p->ev_base));
+    if (p->ev_flush) keep(cudaEventDestroy(p->ev_flush));
+    if (p->copy_in) keep(cudaStreamDestroy(p->copy_in));
+    if (p->copy_out) keep(cudaStreamDestroy(p->copy_out));
+    delete p;
+    return first == cudaSuccess ? BLK_OK : cuda_fail(first, "host pipe release");
+}
+
+}  // namespace
+
+blk_status blk_host_pipe_mem_size(const blk_block_desc* d, int32_t depth, size_t* bytes) {
+    BLK_REQUIRE(d && bytes, "NULL argument");
+    BLK_REQUIRE(depth >= 2 && depth <= kMaxPipeDepth, "depth must be in [2, 4]");
+    size_t ws = 0;
+    blk_status st = blk_forward_workspace_size(d, &ws);
+    if (st != BLK_OK) return st;
+    *bytes = 2 * static_cast<size_t>(depth) * pipe_io_bytes(d) + ws;
+    return BLK_OK;
+}
+
+blk_status blk_host_pipe_create(const blk_block_desc* d, int32_t depth, blk_dtype dt,
+                                void* dev_mem, size_t bytes, blk_host_pipe** out) {
+    BLK_REQUIRE(out != nullptr, "out is NULL");
+    *out = nullptr;
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    size_t need = 0;
+    blk_status st = blk_host_pipe_mem_size(d, depth, &need);
+    if (st != BLK_OK) return st;
+    BLK_CHECK_PTR(dev_mem, true);
+    if (bytes < need) return fail(BLK_EWORKSPACE, "dev_mem needs %zu bytes", need);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    auto* p = new (std::nothrow) blk_host_pipe;
+    if (!p) return fail(BLK_ECUDA, "out of host memory");
+    p->d = *d;
+    p->dt = dt;
+    p->depth = depth;
+    p->device = dev;
+    p->io_bytes = pipe_io_bytes(d);
+    uint8_t* m = static_cast<uint8_t*>(dev_mem);
+    for (int k = 0; k < depth; ++k) {
+        p->x_dev[k] = m + (2 * k) * p->io_bytes;
+        p->y_dev[k] = m + (2 * k + 1) * p->io_bytes;
+    }
+    p->ws = m + 2 * static_cast<size_t>(depth) * p->io_bytes;
+    p->ws_bytes = bytes - 2 * static_cast<size_t>(depth) * p->io_bytes;
+    e = cudaStreamCreateWithFlags(&p->copy_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->copy_out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_base, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_flush, cudaEventDisableTiming);
+    for (int k = 0; k < depth && e == cudaSuccess; ++k) {
+        e = cudaEventCreateWithFlags(&p->ev_in[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fwd[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_out[k], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        pipe_release(p);
+        return cuda_fail(e, "host pipe streams/events");
+    }
+    *out = p;
+    return BLK_OK;
+}
+
+blk_status blk_host_pipe_submit(blk_host_pipe* p, const blk_block_weights* w, const void* x_host,
+                                void* y_host, blk_stream_t s) {
+    BLK_REQUIRE(p != nullptr, "pipe is NULL");
+    BLK_REQUIRE(x_host && y_host, "x_host / y_host is NULL");
+    blk_status st = validate_block(&p->d, w);
+    if (st != BLK_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    BLK_REQUIRE(dev == p->device, "the pipe belongs to device %d, current device is %d", p->device,
+                dev);
+    BLK_REQUIRE(p->n == 0 || cs == p->s,
+                "submits between two flushes must use the same stream");
+    const int k = static_cast<int>(p->n % p->depth);
+    const size_t io = static_cast<size_t>(p->d.qkv.batch) * p->d.qkv.seq * p->d.qkv.hidden * 2;
+    if (p->n == 0) {
+        p->s = cs;
+        e = cudaEventRecord(p->ev_base, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "stream ordering");
+    }
+    // copy in once the forward that last read slot k is done
+    e = cudaStreamWaitEvent(p->copy_in, p->n < p->depth ? p->ev_base : p->ev_fwd[k], 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(p->x_dev[k], x_host, io, cudaMemcpyHostToDevice, p->copy_in);
+    if (e == cudaSuccess) e = cudaEventRecord(p->ev_in[k], p->copy_in);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy");
+    // the forward waits for its input and for the copy-out that last read y slot k
+    e = cudaStreamWaitEvent(cs, p->ev_in[k], 0);
+    if (e == cudaSuccess && p->n >= p->depth) e = cudaStreamWaitEvent(cs, p->ev_out[k], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "stream ordering");
+    st = blk_forward(&p->d, w, p->x_dev[k], p->y_dev[k], p->ws, p->ws_bytes, p->dt, s);
+    if (st != BLK_OK) return st;
+    e = cudaEventRecord(p->ev_fwd[k], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->copy_out, p->ev_fwd[k], 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(y_host, p->y_dev[k], io, cudaMemcpyDeviceToHost, p->copy_out);
+    if (e == cudaSuccess) e = cudaEventRecord(p->ev_out[k], p->copy_out);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy");
+    ++p->n;
+    return BLK_OK;
+}
+
+blk_status blk_host_pipe_flush(blk_host_pipe* p, blk_stream_t s) {
+    BLK_REQUIRE(p != nullptr, "pipe is NULL");
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    if (p->n == 0) return BLK_OK;
+    BLK_REQUIRE(cs == p->s, "flush on the stream of the submits");
+    // copy-outs run in submit order on one stream: its tail is the last one
+    cudaError_t e = cudaEventRecord(p->ev_flush, p->copy_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, p->ev_flush, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "stream ordering");
+    p->n = 0;
+    return BLK_OK;
+}
+
+blk_status blk_host_pipe_destroy(blk_host_pipe* p) {
+    if (!p) return BLK_OK;
+    return pipe_release(p);
+}
+
 constexpr int kMaxForwardEvents = 16;
 struct blk_graph {
     cudaGraphExec_t exec = nullptr;

@@ -449,24 +449,44 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
     ms_per_step = total_ms / args.steps
     value = world * cfg.tokens * args.steps / (total_ms / 1e3)
 
-    # e2e through the public API: pinned host x -> blk_forward_host (copy in, block,
-    # copy out, overlapped over groups of sequences) -> pinned host y
+    # e2e through the public API, pinned host x -> pinned host y every step:
+    # blk_host_pipe_* (default: step n's copy in overlaps step n-1's block, its
+    # copy out step n+1's; the flush after the last step is inside the timed
+    # region) or blk_forward_host (copies overlapped over groups of sequences
+    # within one step)
     x_host = x_cpu.pin_memory()
     y_host = torch.empty_like(x_host).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    x_e2e = torch.empty_like(x)
+    if args.e2e_api == "pipe":
+        del ws  # the pipe holds its own staging slots and workspace
+        pipe = blk.HostPipe(cfg, cfg.batch, cfg.seq, dtype=x.dtype, depth=2)
 
-    def e2e_step():
-        blk.forward_host(cfg, wd, x_host, y_host=y_host, x_dev=x_e2e, y_dev=y, workspace=ws,
-                         n_chunks=args.e2e_chunks)
+        def e2e_step():
+            pipe.submit(wd, x_host, y_host)
+
+        def e2e_end():
+            pipe.flush()
+    else:
+        x_e2e = torch.empty_like(x)
+
+        def e2e_step():
+            blk.forward_host(cfg, wd, x_host, y_host=y_host, x_dev=x_e2e, y_dev=y, workspace=ws,
+                             n_chunks=args.e2e_chunks)
+
+        def e2e_end():
+            pass
 
     for _ in range(3):
         e2e_step()
+    e2e_end()
     torch.cuda.synchronize()
+    e2e_set = (ws_bytes + 2 * x.numel() * x.element_size()
+               + sum(t.numel() * t.element_size() for t in wd.values()))
     e2e_steps = max(1, min(args.steps, 50))
     e0.record()
     for _ in range(e2e_steps):
         e2e_step()
+    e2e_end()
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -530,8 +550,16 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         "e2e": {"value": world * cfg.tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": y.numel() * y.element_size(),
-                "ms_per_step": e2e_ms, "n_chunks": args.e2e_chunks,
-                "api": "blk_forward_host (pinned host buffers)"},
+                "ms_per_step": e2e_ms,
+                "l2": ("not flushed between steps: a step moves %.2f GB of distinct buffers "
+                       "(staging, workspace, weights), %.1fx L2; the device-timed leg writes "
+                       "512 MiB before each step and pays that write-back in its first kernel"
+                       % (e2e_set / 1e9, e2e_set / (129 << 20))),
+                **({"api": "blk_host_pipe_submit/flush (pinned host buffers; step n's copies "
+                           "overlap steps n-1 and n+1)", "depth": 2}
+                   if args.e2e_api == "pipe" else
+                   {"api": "blk_forward_host (pinned host buffers)",
+                    "n_chunks": args.e2e_chunks})},
         "hbm_kernels_standalone": standalone,
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
@@ -553,6 +581,9 @@ def main():
                     help="timed steps launch the block directly (default), or replay it as a "
                          "CUDA graph; the per-kernel events inside a graph cost more than the "
                          "graph saves (0.715 vs 0.707 ms), without them it is 2.6%% faster")
+    ap.add_argument("--e2e-api", choices=["pipe", "chunks"], default="pipe",
+                    help="e2e leg through blk_host_pipe_* (copies overlapped across steps) or "
+                         "blk_forward_host (copies overlapped over groups of sequences)")
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="groups of sequences blk_forward_host overlaps copies and compute over")
     ap.add_argument("--decode", action="store_true",

@@ -315,6 +315,32 @@ blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
                             void* workspace, size_t ws_bytes, int32_t n_chunks, blk_dtype dt,
                             blk_stream_t s);
 
+/* A pipeline of block forwards over a stream of host batches, for serving:
+ * blk_host_pipe_submit enqueues one batch and returns. Batch n is copied in
+ * (pinned x_host, [batch, seq, hidden] as in the desc) on a copy stream the
+ * pipe owns while batch n-1's forward runs on s, and copied out (to pinned
+ * y_host) on a second copy stream while batch n+1's forward runs, through
+ * depth (2..4) device staging slots. The forwards themselves run in order on
+ * s. Two departures from plain stream order, by design:
+ *  - x_host must already hold the batch when submit is called: its copy may
+ *    start at once (the first depth submits after create or a flush wait
+ *    for the work enqueued on s before the first of them);
+ *  - y_host of a batch is complete once s has passed a later
+ *    blk_host_pipe_flush.
+ * All submits between two flushes use the same stream s (BLK_EINVAL
+ * otherwise). The pipe is not thread-safe. dev_mem (blk_host_pipe_mem_size
+ * bytes, 16-byte aligned, caller-owned) holds the staging slots and the
+ * forward's workspace; it must stay valid until the submitted work has
+ * completed. destroy does not wait for that work. */
+typedef struct blk_host_pipe blk_host_pipe;
+blk_status blk_host_pipe_mem_size(const blk_block_desc* d, int32_t depth, size_t* bytes);
+blk_status blk_host_pipe_create(const blk_block_desc* d, int32_t depth, blk_dtype dt,
+                                void* dev_mem, size_t bytes, blk_host_pipe** out);
+blk_status blk_host_pipe_submit(blk_host_pipe* p, const blk_block_weights* w, const void* x_host,
+                                void* y_host, blk_stream_t s);
+blk_status blk_host_pipe_flush(blk_host_pipe* p, blk_stream_t s);
+blk_status blk_host_pipe_destroy(blk_host_pipe* p);
+
 /* A block forward recorded once as a CUDA graph and replayed: the same seven
  * to nine kernels with the same pointers, without per-launch host work or
  * the gaps between separately submitted launches. blk_forward_graph_create

@@ -205,6 +205,31 @@ def test_forward_host_validation(lib):
     assert lib.blk_graph_set_events(None, None, 0) == _abi.BLK_EINVAL
 
 
+def test_host_pipe_validation(lib):
+    """blk_host_pipe_*: sizes, depth range and argument checks without a GPU;
+    destroying NULL is a no-op."""
+    d = _block()
+    n = C.c_size_t(0)
+    ws = C.c_size_t(0)
+    assert lib.blk_forward_workspace_size(C.byref(d), C.byref(ws)) == _abi.BLK_OK
+    assert lib.blk_host_pipe_mem_size(C.byref(d), 2, C.byref(n)) == _abi.BLK_OK
+    io = d.qkv.batch * d.qkv.seq * d.qkv.hidden * 2
+    io = (io + 255) // 256 * 256
+    assert n.value == 4 * io + ws.value  # two slots of x and y, then the workspace
+    for bad in (1, 5):
+        assert lib.blk_host_pipe_mem_size(C.byref(d), bad, C.byref(n)) == _abi.BLK_EINVAL
+        assert "depth" in _err(lib)
+    out = C.c_void_p()
+    assert lib.blk_host_pipe_create(C.byref(d), 2, 1, FAKE, 1 << 40, None) == _abi.BLK_EINVAL
+    assert lib.blk_host_pipe_create(C.byref(d), 2, 7, FAKE, 1 << 40, C.byref(out)) == _abi.BLK_EINVAL
+    assert lib.blk_host_pipe_create(C.byref(d), 2, 1, None, 1 << 40, C.byref(out)) == _abi.BLK_EINVAL
+    assert lib.blk_host_pipe_create(C.byref(d), 2, 1, FAKE, 16, C.byref(out)) == _abi.BLK_EWORKSPACE
+    assert out.value is None
+    assert lib.blk_host_pipe_submit(None, C.byref(_weights()), FAKE, FAKE, None) == _abi.BLK_EINVAL
+    assert lib.blk_host_pipe_flush(None, None) == _abi.BLK_EINVAL
+    assert lib.blk_host_pipe_destroy(None) == _abi.BLK_OK
+
+
 def test_decode_validation(lib):
     """blk_attn_decode: shape rules and workspace size without a GPU."""
     d = _abi.DecodeDesc(4, 2048, 32, 8, 64, -1.0, 0)

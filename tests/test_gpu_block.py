@@ -149,6 +149,54 @@ def test_forward_host_rejects_bad_arguments():
         blk.forward_host(cfg, wd, x.pin_memory(), n_chunks=17)
 
 
+@pytest.mark.parametrize("name,depth", [("stablelm2_ragged_bf16", 2), ("olmo2_small", 3),
+                                        ("bloom_small", 2)])
+def test_host_pipe_matches_device_forward(name, depth):
+    """Five batches through a host pipe (copies of one batch overlapping the
+    neighbouring batches' forwards, staging slots reused): each y_host equals
+    blk_forward on that batch bit for bit, and a second round after a flush
+    still does."""
+    cfg = SMALL[name]
+    x, w = workloads.block_inputs(cfg)
+    wd = {k: to_dev(t) for k, t in w.items()}
+    B, S, _ = x.shape
+    xs = [(x.double() * (1.0 - 0.3 * i)).to(x.dtype) for i in range(5)]
+    refs = [blk.forward(cfg, wd, to_dev(xi)).cpu() for xi in xs]
+    pipe = blk.HostPipe(cfg, B, S, dtype=x.dtype, depth=depth)
+    xh = [xi.pin_memory() for xi in xs]
+    for _ in range(2):
+        yh = [torch.empty_like(xi).pin_memory() for xi in xs]
+        for a, b in zip(xh, yh):
+            pipe.submit(wd, a, b)
+        pipe.flush()
+        torch.cuda.current_stream().synchronize()
+        blk.check_device_status()
+        for i, (got, ref) in enumerate(zip(yh, refs)):
+            assert torch.equal(got, ref), f"batch {i}"
+    pipe.close()
+
+
+def test_host_pipe_rejects_a_second_stream():
+    """Submits between two flushes share one stream (their forwards share the
+    pipe's workspace); a submit on another stream is refused."""
+    cfg = SMALL["tiny_stablelm2"]
+    x, w = workloads.block_inputs(cfg)
+    wd = {k: to_dev(t) for k, t in w.items()}
+    pipe = blk.HostPipe(cfg, *x.shape[:2], dtype=x.dtype)
+    xh, yh = x.pin_memory(), torch.empty_like(x).pin_memory()
+    pipe.submit(wd, xh, yh)
+    other = torch.cuda.Stream()
+    with torch.cuda.stream(other):
+        with pytest.raises(blk.BlkError):
+            pipe.submit(wd, xh, yh)
+    pipe.flush()
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(yh, blk.forward(cfg, wd, to_dev(x)).cpu())
+    with pytest.raises(ValueError):
+        pipe.submit(wd, x, yh)  # pageable
+    pipe.close()
+
+
 @pytest.mark.parametrize("name", ["stablelm2_ragged_bf16", "olmo2_small", "bloom_small"])
 def test_forward_graph_replays_forward(name):
     """A block recorded as a CUDA graph (blk_forward_graph_create) replays the
