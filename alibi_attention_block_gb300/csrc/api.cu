@@ -331,7 +331,7 @@ blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w) {
 }
 
 struct FwdLayout {
-    size_t n1, q, k, v, o, h, n2, a, h16, tmp, total;
+    size_t n1, q, k, v, o, h, n2, a, h16, tmp, split, total;
 };
 
 FwdLayout forward_layout(const blk_block_desc* d) {
@@ -355,6 +355,7 @@ FwdLayout forward_layout(const blk_block_desc* d) {
     L.a = take(T * static_cast<size_t>(d->intermediate));
     L.h16 = take(T * D);      // storage-dtype copy of h (post-norm MLP input)
     L.tmp = take(2 * T * D);  // fp32 sublayer output (parallel residual, post-norm input)
+    L.split = take(kGemmSplitBytes / 2);  // partial tiles + counters of split GEMM rounds
     L.total = off;
     return L;
 }
@@ -402,9 +403,18 @@ struct StepLog {
 // Launch the projection (+bias, +rotary when it can be fused) and, when a
 // qk-norm or a wider rotary span sits between the projection and attention,
 // the in-place qk-norm/rotary kernel.
+// split: GEMM scratch (kGemmSplitBytes, counters zero) or nullptr
+void set_split(GemmArgs& g, void* split) {
+    if (!split) return;
+    g.split_ws = static_cast<float*>(split);
+    g.split_cnt = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(split) +
+                                              static_cast<size_t>(kGemmSplitSlots) * 128 * 256 * 4);
+}
+
 blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, const void* b_qkv,
                    const void* q_norm_w, const void* k_norm_w, void* q, void* k, void* v,
-                   DType dt, cudaStream_t s, DevState* ds, StepLog* log = nullptr) {
+                   DType dt, cudaStream_t s, DevState* ds, StepLog* log = nullptr,
+                   void* split = nullptr) {
     // the GEMM epilogue rotates spans of 16 or 32 dims in registers; other
     // spans, and any qk-norm (which must precede the rotary), run in the
     // qk-norm/rotary kernel after the projection
@@ -425,6 +435,7 @@ blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, cons
     g.d = static_cast<int>(d->head_dim);
     g.interleaved = d->qkv_layout == BLK_QKV_HEAD_INTERLEAVED;
     g.err = ds->err;
+    set_split(g, split);
     cudaError_t e = launch_gemm(dt, EPI_QKV, x, w_qkv, nullptr, g, rp, ds->sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "qkv projection launch");
     blk_status st;
@@ -454,8 +465,10 @@ enum : int { F32_OUT = 1, F32_RES1 = 2, F32_RES2 = 4 };
 
 blk_status run_linear(DType dt, int epi, const void* x, const void* w, const void* w2,
                       const void* bias, const void* r1, const void* r2, void* y, int64_t m,
-                      int64_t n, int64_t k, cudaStream_t s, DevState* ds, int f32 = 0) {
+                      int64_t n, int64_t k, cudaStream_t s, DevState* ds, int f32 = 0,
+                      void* split = nullptr) {
     GemmArgs g{};
+    set_split(g, split);
     g.out_f32 = (f32 & F32_OUT) != 0;
     g.res1_f32 = (f32 & F32_RES1) != 0;
     g.res2_f32 = (f32 & F32_RES2) != 0;
@@ -833,6 +846,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     void* ab = ws + L.a;
     void* tmp = ws + L.tmp;
     void* h16 = ws + L.h16;
+    void* split = ws + L.split;
     const int64_t T = q.batch * q.seq, D = q.hidden, F = d->intermediate;
     const bool rms = d->norm_kind == BLK_NORM_RMS;
     const bool pre = d->norm_place == BLK_NORM_PRE;
@@ -841,6 +855,12 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     cudaError_t e;
     StepLog log{events, n_events, step_kinds, n_launches, cs};
     if ((st = log.begin()) != BLK_OK) return st;
+    // the split GEMM rounds' arrival counters start at zero (each launch
+    // leaves them zero again)
+    e = cudaMemsetAsync(static_cast<uint8_t*>(split) +
+                            static_cast<size_t>(kGemmSplitSlots) * 128 * 256 * 4,
+                        0, kGemmSplitCounters * sizeof(unsigned), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "split counters");
 #define BLK_STEP(kind)                                   \
     do {                                                 \
         if ((st = log.step(kind)) != BLK_OK) return st;  \
@@ -857,7 +877,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     }
     // 2. projection (+bias), qk-norm, rotary, head split
     st = run_qkv(&q, attn_in, w->w_qkv, w->b_qkv, w->q_norm_w, w->k_norm_w, qb, kb, vb, t, cs, ds,
-                 &log);
+                 &log, split);
     if (st != BLK_OK) return st;
     // 3. causal attention (+ALiBi)
     blk_attn_desc ad{q.batch, q.seq, q.n_heads, q.n_kv_heads, q.head_dim, 0.f, 1, d->alibi};
@@ -869,15 +889,16 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
         // 4p. attn_out = o W_o^T (+b_o) kept in fp32; mlp on the same normed
         // input; y = x + attn_out + mlp
         st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
-                        cs, ds, F32_OUT);
+                        cs, ds, F32_OUT, split);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
         st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, attn_in, swiglu ? w->w_gate : w->w_up,
-                        swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds);
+                        swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
+                        split);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_UP);
         st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, x, tmp, y, T, D, F, cs,
-                        ds, F32_RES2);
+                        ds, F32_RES2, split);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
         return log.end();
@@ -886,7 +907,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     if (pre) {
         // 4. h = x + o W_o^T (+b_o), fp32;  5. n2 = norm(h)
         st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, x, nullptr, hb, T, D, Hd, cs, ds,
-                        F32_OUT);
+                        F32_OUT, split);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
         e = launch_norm(t, rms, NormIO{hb, true, nullptr, false, n2, nullptr, ds->err, ds->sms}, w->mlp_norm_w,
@@ -899,7 +920,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
         // rounding would be magnified);  5. h = x + RMS(a) * w_post_attn
         // (fp32, and a storage copy for the MLP)
         st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
-                        cs, ds, F32_OUT);
+                        cs, ds, F32_OUT, split);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
         e = launch_norm(t, true, NormIO{tmp, true, x, false, h16, static_cast<float*>(hb), ds->err, ds->sms},
@@ -910,20 +931,21 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     }
     // 6. MLP up (+activation)
     st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, mlp_in, swiglu ? w->w_gate : w->w_up,
-                    swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds);
+                    swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
+                        split);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_UP);
     if (pre) {
         // 7. y = h + a W_d^T (+b_d)
         st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, hb, nullptr, y, T, D, F, cs,
-                        ds, F32_RES1);
+                        ds, F32_RES1, split);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
         return log.end();
     }
     // 7. m = a W_d^T;  8. y = h + RMS(m) * w_post_mlp
     st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, nullptr, nullptr, tmp, T, D, F,
-                    cs, ds, F32_OUT);
+                    cs, ds, F32_OUT, split);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_DOWN);
     e = launch_norm(t, true, NormIO{tmp, true, hb, true, y, nullptr, ds->err, ds->sms}, w->post_mlp_norm_w, nullptr,

@@ -32,6 +32,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kGemmThreads = 192;
+constexpr int kSplitMinKb = 32;  // k-blocks per segment of a split unit, at least
 
 template <int BN>
 struct GemmCfg {
@@ -44,6 +45,45 @@ struct GemmCfg {
     static constexpr int kSmem = kStages * kStageBytes + 1024 + kBarBytes + kEpiBytes;
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 };
+
+// Work unit v of the persistent loop: unit u over k-blocks [kb0, kb1). Units
+// before split_base run whole; each unit of the last, partial round is
+// split into split_s segments along K, run by otherwise idle CTAs.
+struct Unit {
+    int u, q, kb0, kb1;
+};
+template <bool SPLIT>
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& g, int v, int kb_count) {
+    if (!SPLIT || v < g.split_base) return {v, 0, 0, kb_count};
+    const int t = (v - g.split_base) / g.split_s;
+    const int q = v - g.split_base - t * g.split_s;
+    return {g.split_base + t, q, q * kb_count / g.split_s, (q + 1) * kb_count / g.split_s};
+}
+
+// Sum of a split unit's partial tiles for 32 columns of this thread's row, in
+// segment order (the same order whichever segment finishes last): its own
+// segment's values come from o, the others' from their [column][row]
+// partials.
+template <int BN>
+__device__ __forceinline__ void add_partials(float (&o)[32], const float* part, int part_s,
+                                             int self, int col0, int trow) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    for (int q = 0; q < part_s; ++q) {
+        if (q == self) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] += o[i];
+        } else {
+            const float* p = part + static_cast<size_t>(q) * (kBM * BN) +
+                             static_cast<size_t>(col0) * kBM + trow;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] += __ldcg(p + i * kBM);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = acc[i];
+}
 
 template <typename T>
 __device__ __forceinline__ void store_row32(T* dst, const float (&o)[32], int valid) {
@@ -106,10 +146,11 @@ __device__ __forceinline__ float gelu_tanh_f(float z) {
     return 0.5f * z * (1.0f + tanhf(k0 * (z + 0.044715f * z * z * z)));
 }
 
-template <typename T, int BN, int EPI, int ROT>
+template <typename T, int BN, int EPI, int ROT, bool SPLIT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParams& rp,
                                               uint32_t tbase, int m, int nt, uint32_t stg,
-                                              int lane, int m_base) {
+                                              int lane, int m_base, const float* part, int self,
+                                              int trow) {
     const bool row_ok = m < g.M;
     if constexpr (EPI == EPI_SWIGLU) {
         constexpr int kHalf = BN / 2;
@@ -139,6 +180,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             float o[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            if constexpr (SPLIT)
+                if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
             if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, 32);
             int which, head, dd0;
             if (g.interleaved) {
@@ -183,6 +226,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             float o[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            if constexpr (SPLIT)
+                if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
             if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
             if constexpr (EPI == EPI_GELU) {
 #pragma unroll
@@ -211,7 +256,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
 // from L2 once per pair (a third less L2 traffic per stage). A stage is
 // refilled only after both CTAs' MMAs have released it: each MMA completion
 // arrives on the empty barrier of both CTAs (multicast commit).
-template <typename T, int BN, int EPI, int ROT, int CL>
+template <typename T, int BN, int EPI, int ROT, int CL, bool SPLIT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const GemmArgs g,
@@ -268,15 +313,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int unit0 = static_cast<int>(blockIdx.x) / CL;
     const int unit_step = static_cast<int>(gridDim.x) / CL;
     const int kb_count = (g.K + kBK - 1) / kBK;
+    const int num_work =
+        SPLIT ? g.split_base + (num_units - g.split_base) * g.split_s : num_units;
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = unit0; u < num_units && ok; u += unit_step) {
+            for (int v = unit0; v < num_work && ok; v += unit_step) {
+                const Unit un = decode_unit<SPLIT>(g, v, kb_count);
+                const int u = un.u;
                 const int mt = (g.n_fastest ? u / n_tiles : u % m_units) * CL + rank;
                 const int nt = g.n_fastest ? u % n_tiles : u / m_units;
-                for (int kb = 0; kb < kb_count; ++kb) {
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!mbar_wait(empty(stage), phase ^ 1u, g.err)) {
                         ok = false;
                         break;
@@ -316,13 +365,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int u = unit0; u < num_units && ok; u += unit_step, ++it) {
+            for (int v = unit0; v < num_work && ok; v += unit_step, ++it) {
+                const Unit un = decode_unit<SPLIT>(g, v, kb_count);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!mbar_wait(tempty(acc), acc_phase ^ 1u, g.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < kb_count; ++kb) {
+                for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!mbar_wait(full(stage), phase, g.err)) {
                         ok = false;
                         break;
@@ -332,7 +382,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint64_t bd = db0 + stage * kStageStep;
 #pragma unroll
                     for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_ss(d_tmem, ad + k * 2, bd + k * 2, idesc, (kb | k) != 0 ? 1u : 0u);
+                        tc_mma_ss(d_tmem, ad + k * 2, bd + k * 2, idesc,
+                                  (kb > un.kb0 || k != 0) ? 1u : 0u);
                     if constexpr (CL == 2)
                         tc_commit_multicast(empty(stage), 0x3);
                     else
@@ -350,7 +401,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row = quarter * 32 + lane;
         const uint32_t stg0 = smem_u32(smem) + kStages * Cfg::kStageBytes + Cfg::kBarBytes;
         int it = 0;
-        for (int u = unit0; u < num_units; u += unit_step, ++it) {
+        for (int v = unit0; v < num_work; v += unit_step, ++it) {
+            const Unit un = decode_unit<SPLIT>(g, v, kb_count);
+            const int u = un.u;
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!mbar_wait(tfull(acc), acc_phase, g.err)) break;
@@ -359,9 +412,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int nt = g.n_fastest ? u % n_tiles : u / m_units;
             const uint32_t tbase =
                 tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            epilogue_tile<T, BN, EPI, ROT>(g, rp, tbase, mt * kBM + row, nt,
+            const float* part = nullptr;
+            unsigned* cnt = nullptr;
+            if (SPLIT && v >= g.split_base) {
+                // a segment of a split unit: publish this warp's 32 rows of
+                // the partial tile ([column][row], coalesced per column), then
+                // count the warp in; the warp that arrives last for these
+                // rows sums every segment and runs the epilogue
+                const int t = (v - g.split_base) / g.split_s;
+                float* slot0 = g.split_ws + static_cast<size_t>((t * CL + rank) * g.split_s) *
+                                                (kBM * BN);
+                float* mine = slot0 + static_cast<size_t>(un.q) * (kBM * BN) + row;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        __stcg(mine + (c * 32 + i) * kBM, __uint_as_float(r[i]));
+                }
+                __threadfence();
+                __syncwarp();
+                cnt = g.split_cnt + ((t * CL + rank) * 4 + quarter);
+                unsigned old = 0;
+                if (lane == 0) old = atomicAdd(cnt, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                if (old != static_cast<unsigned>(g.split_s - 1)) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty(acc));
+                    continue;
+                }
+                __threadfence();  // the other segments' partials are visible
+                part = slot0;
+            }
+            epilogue_tile<T, BN, EPI, ROT, SPLIT>(g, rp, tbase, mt * kBM + row, nt,
                                            stg0 + quarter * (32 * 128), lane,
-                                           mt * kBM + quarter * 32);
+                                           mt * kBM + quarter * 32, part, un.q, row);
+            if (cnt && lane == 0) *cnt = 0u;  // every segment has arrived: ready for the next launch
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(acc));
@@ -384,12 +472,18 @@ cudaError_t launch_cl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
                       const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
     using Cfg = GemmCfg<BN>;
     constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
-    auto kern = gemm_kernel<T, BN, EPI, ROT, CL>;
+    // the split instance exists only where a split is possible
+    constexpr bool kCanSplit = EPI != EPI_SWIGLU;
+    auto kern = gemm_kernel<T, BN, EPI, ROT, CL, false>;
+    auto kern_split = gemm_kernel<T, BN, EPI, ROT, CL, kCanSplit>;
     static bool attr_set = false;  // per template instance
     static int max_clusters = 0;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg::kSmem);
+        if (e == cudaSuccess && kCanSplit)
+            e = cudaFuncSetAttribute(kern_split, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::kSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -418,7 +512,30 @@ cudaError_t launch_cl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
     }
     const int64_t grid_units = units < slots ? units : slots;
     cfg.gridDim = dim3(static_cast<unsigned>(grid_units * CL), 1, 1);
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, g, rp);
+    // With scratch, split each unit of a last round that would leave at
+    // least half of the CTAs idle (G units per round, R <= G/2 in the last)
+    // into two halves along K, when each half still has at least
+    // kSplitMinKb k-blocks: the unit that finishes second reads the other's
+    // partial tile back from L2, one round trip per 32 columns, which only a
+    // long mainloop pays for (measured: the down projections gain, shorter
+    // K loses).
+    GemmArgs ga = g;
+    ga.split_s = 1;
+    ga.split_base = 0;
+    if (kCanSplit && g.split_ws && g.split_cnt) {
+        const int64_t G = grid_units;
+        const int64_t rounds = (units + G - 1) / G;
+        const int64_t R = units - (rounds - 1) * G;
+        const int64_t sp = 2;
+        const int64_t kb_count = (g.K + kBK - 1) / kBK;
+        if (rounds >= 2 && R * sp <= G && kb_count >= sp * kSplitMinKb &&
+            R * CL * sp <= kGemmSplitSlots && R * CL * 4 <= kGemmSplitCounters) {
+            ga.split_s = static_cast<int>(sp);
+            ga.split_base = static_cast<int>((rounds - 1) * G);
+            return cudaLaunchKernelEx(&cfg, kern_split, ta, tb, tb2, ga, rp);
+        }
+    }
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, ga, rp);
 }
 
 template <typename T, int BN, int EPI, int ROT = 0>

@@ -65,7 +65,20 @@ struct GemmArgs {
     int S, H, Hk, d, interleaved;
     unsigned* err;
     int n_fastest;        // work-unit order (set by launch_gemm)
+    // split of the last, partial round of work units along K (LINEAR, GELU,
+    // QKV; only with scratch): fp32 partial tiles and per-warp arrival
+    // counters (zero before the launch, left zero after it)
+    float* split_ws;
+    unsigned* split_cnt;
+    int split_s;          // segments per split unit (set by launch_gemm; 1 = none)
+    int split_base;       // first split unit
 };
+// scratch of a split GEMM: kGemmSplitSlots partial 128 x 256 fp32 tiles, then
+// kGemmSplitCounters counters
+constexpr int kGemmSplitSlots = 256;
+constexpr int kGemmSplitCounters = 1024;
+constexpr size_t kGemmSplitBytes =
+    static_cast<size_t>(kGemmSplitSlots) * 128 * 256 * 4 + kGemmSplitCounters * 4;
 // a: [M, K]; b: [N(or N rows of gate), K]; b2: up weights for SWIGLU.
 cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const void* b2,
                         const GemmArgs& args, const RopeParams& rp, int num_sms, cudaStream_t s);

@@ -88,6 +88,26 @@ def test_block_negative_control_full_rotary_diverges():
     assert np.abs(y16 - y64).max() > 0.4
 
 
+def test_block_split_gemm_rounds():
+    """A down projection whose work units end in a partial round on 152 SMs
+    (76 clusters of two): 96 units of 128 k-blocks, the last round's 20 split
+    into two halves along K. The split tiles (rows past 3072 in column tile
+    4, every row in column tile 5) are checked against the oracle, and the
+    result is bit-identical run to run: the partial tiles are summed in
+    segment order whichever half finishes last."""
+    cfg = scaled(BLOCK_CONFIGS["stablelm2_1p6b"], batch=2, seq=2048, hidden=1536, n_heads=24,
+                 n_kv_heads=8, intermediate=8192)
+    x, w = workloads.block_inputs(cfg)
+    y = _gpu_forward(cfg, x, w)
+    y2 = _gpu_forward(cfg, x, w)
+    assert torch.equal(y, y2)
+    rows = np.array(sorted({int(r) for r in workloads.sample_rows(cfg.tokens, 24, seed=cfg.seed)}
+                           | {0, 2047, 2048, 3071, 3072, 4095}))
+    ref = oracle.block_forward(cfg, x, w, rows=rows)["y"]
+    got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
+    check(got, ref, "split GEMM rounds", unit_scale=True, abs_tol=_abs_tol(cfg))
+
+
 @pytest.mark.parametrize("name", ["stablelm2_1p6b", "bloom_560m", "olmo2_1b"])
 def test_block_full_size_sampled_rows(name):
     cfg = BLOCK_CONFIGS[name]
