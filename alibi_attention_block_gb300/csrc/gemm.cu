@@ -31,7 +31,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each with half of the columns
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kSplitMinKb = 32;  // k-blocks per segment of a split unit, at least
 
 template <int BN>
@@ -41,7 +42,7 @@ struct GemmCfg {
     static constexpr int kBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kEpiBytes = 4 * 32 * 128;  // per epilogue warp: 32 rows x 32 fp32
+    static constexpr int kEpiBytes = kEpiWarps * 32 * 128;  // per epilogue warp: 32 rows x 32 fp32
     static constexpr int kSmem = kStages * kStageBytes + 1024 + kBarBytes + kEpiBytes;
     static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
 };
@@ -150,12 +151,15 @@ template <typename T, int BN, int EPI, int ROT, bool SPLIT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParams& rp,
                                               uint32_t tbase, int m, int nt, uint32_t stg,
                                               int lane, int m_base, const float* part, int self,
-                                              int trow) {
+                                              int trow, int half) {
+    // this warp's half of the tile's 32-column chunks
+    constexpr int kChunks = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 32;
+    const int c_begin = half * (kChunks / 2), c_end = c_begin + kChunks / 2;
     const bool row_ok = m < g.M;
     if constexpr (EPI == EPI_SWIGLU) {
         constexpr int kHalf = BN / 2;
 #pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
             uint32_t gr[32], ur[32];
             tmem_ld32(tbase + c * 32, gr);
             tmem_ld32(tbase + kHalf + c * 32, ur);
@@ -172,7 +176,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
         const int b = m / g.S;
         const int s = m - b * g.S;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
             uint32_t r[32];
             tmem_ld32(tbase + c * 32, r);
             const int n0 = nt * BN + c * 32;
@@ -217,7 +221,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
         }
     } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
             uint32_t r[32];
             tmem_ld32(tbase + c * 32, r);
             const int n0 = nt * BN + c * 32;
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull(i), 1);
-            mbar_init(tempty(i), 4);
+            mbar_init(tempty(i), kEpiWarps);
         }
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
@@ -397,7 +401,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
     } else {
+        // epilogue warp ew: TMEM lanes 32 (warp % 4) .. +31 (a warp reaches
+        // only the lane quarter of its index mod 4), columns of half ew / 4
+        const int ew = warp - 2;
         const int quarter = warp & 3;
+        const int half = ew / 4;
         const int row = quarter * 32 + lane;
         const uint32_t stg0 = smem_u32(smem) + kStages * Cfg::kStageBytes + Cfg::kBarBytes;
         int it = 0;
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                                 (kBM * BN);
                 float* mine = slot0 + static_cast<size_t>(un.q) * (kBM * BN) + row;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
                     uint32_t r[32];
                     tmem_ld32(tbase + c * 32, r);
 #pragma unroll
@@ -433,7 +441,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 __threadfence();
                 __syncwarp();
-                cnt = g.split_cnt + ((t * CL + rank) * 4 + quarter);
+                cnt = g.split_cnt + ((t * CL + rank) * kEpiWarps + ew);
                 unsigned old = 0;
                 if (lane == 0) old = atomicAdd(cnt, 1u);
                 old = __shfl_sync(0xffffffffu, old, 0);
@@ -447,8 +455,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 part = slot0;
             }
             epilogue_tile<T, BN, EPI, ROT, SPLIT>(g, rp, tbase, mt * kBM + row, nt,
-                                           stg0 + quarter * (32 * 128), lane,
-                                           mt * kBM + quarter * 32, part, un.q, row);
+                                                  stg0 + ew * (32 * 128), lane,
+                                                  mt * kBM + quarter * 32, part, un.q, row, half);
             if (cnt && lane == 0) *cnt = 0u;  // every segment has arrived: ready for the next launch
             tc_fence_before();
             __syncwarp();
@@ -529,7 +537,7 @@ cudaError_t launch_cl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         const int64_t sp = 2;
         const int64_t kb_count = (g.K + kBK - 1) / kBK;
         if (rounds >= 2 && R * sp <= G && kb_count >= sp * kSplitMinKb &&
-            R * CL * sp <= kGemmSplitSlots && R * CL * 4 <= kGemmSplitCounters) {
+            R * CL * sp <= kGemmSplitSlots && R * CL * kEpiWarps <= kGemmSplitCounters) {
             ga.split_s = static_cast<int>(sp);
             ga.split_base = static_cast<int>((rounds - 1) * G);
             return cudaLaunchKernelEx(&cfg, kern_split, ta, tb, tb2, ga, rp);
