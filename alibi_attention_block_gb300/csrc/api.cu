@@ -706,7 +706,7 @@ blk_status blk_attn_decode(const blk_decode_desc* d, const void* q, const void* 
     a.Hk = static_cast<int>(d->n_kv_heads);
     a.d = static_cast<int>(d->head_dim);
     a.S_max = static_cast<int>(d->max_seq);
-    a.parts = decode_parts(d->batch, d->n_kv_heads, d->max_seq, ds->sms);
+    a.parts = decode_parts(d->batch, d->n_kv_heads, d->max_seq, d->head_dim, ds->sms);
     a.scale = d->softmax_scale > 0.f ? d->softmax_scale
                                      : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
     a.alibi = d->alibi;

@@ -27,28 +27,34 @@ namespace blk {
 
 namespace {
 
-constexpr int kDecThreads = 128;  // 4 warps per block, one part each
+constexpr int kDecThreads = 128;  // combine kernel: 4 warps per block
 constexpr float kLog2eDec = 1.4426950408889634f;
 
+// Ring depth and warps per block: at head_dim 64 a three-stage ring is 24 KB
+// a warp (eight warps per SM); at 128 a three-stage ring would be 48 KB and
+// leave four warps per SM, one per scheduler, with nothing to hide the
+// latencies of its shared-memory loads and shuffles, so there a two-stage
+// ring in two-warp blocks gives six.
 template <int D>
 struct DecCfg {
-    static constexpr int kStages = 3;                    // key blocks in flight per warp
+    static constexpr int kStages = D > 64 ? 2 : 3;       // key blocks in flight per warp
+    static constexpr int kWarps = D > 64 ? 2 : 4;        // warps per block
     static constexpr int kBlockBytes = 32 * D * 2;       // 32 K (or V) rows
     static constexpr int kStageBytes = 2 * kBlockBytes;  // K then V
     static constexpr int kWarpBytes = kStages * kStageBytes;
-    static constexpr int kSmem = 4 * kWarpBytes;
+    static constexpr int kSmem = kWarps * kWarpBytes;
 };
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(DecodeArgs a) {
     using Cfg = DecCfg<D>;
     constexpr int kCols = D / 32;  // output columns per lane
     constexpr int kChunks = D / 8; // 16-byte pieces per row
-    __shared__ float qs[4][G][D];  // this warp's queries, pre-scaled (log2 domain)
+    __shared__ __align__(16) float qs[Cfg::kWarps][G][D];  // each warp's queries, pre-scaled (log2)
     extern __shared__ __align__(128) uint8_t dsm[];
     const int lane = threadIdx.x & 31;
     const int wl = threadIdx.x / 32;
-    const int64_t wid = static_cast<int64_t>(blockIdx.x) * 4 + wl;
+    const int64_t wid = static_cast<int64_t>(blockIdx.x) * Cfg::kWarps + wl;
     const int64_t total = static_cast<int64_t>(a.B) * a.Hk * a.parts;
     if (wid >= total) return;  // whole warps exit together
     const uint32_t ring = smem_u32(dsm) + wl * Cfg::kWarpBytes;
@@ -116,6 +122,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
     for (int i = 0; i < Cfg::kStages - 1; ++i) issue(i);
     __syncwarp();
     const float qpos = static_cast<float>(n - 1);
+    const uint32_t qs_addr = smem_u32(&qs[wl][0][0]);
     for (int i = 0; i < nblk; ++i) {
         issue(i + Cfg::kStages - 1);
         cp_async_wait<Cfg::kStages - 1>();  // block i has landed (this lane's copies)
@@ -124,23 +131,39 @@ __global__ void __launch_bounds__(kDecThreads) decode_partial_kernel(DecodeArgs 
         const int jb = j0 + i * 32;
         const int j = jb + lane;
         const bool valid = j < j1;
-        // scores of key j against the G queries (log2 domain)
-        float sc[G];
+        // scores of key j against the G queries (log2 domain): paired
+        // (f32x2) FMAs over even and odd dims, the queries read 16 bytes at
+        // a time (the same address in every lane: a broadcast)
+        uint64_t sc2[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) sc[h] = 0.f;
+        for (int h = 0; h < G; ++h) sc2[h] = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
             const uint4 kv = ld_shared_u4(st + lane * (D * 2) + ((c ^ (lane & 7)) << 4));
             const uint32_t w4[4] = {kv.x, kv.y, kv.z, kv.w};
+            uint64_t k2[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
                 const float2 kf = dt_traits<T>::unpack2(w4[e2]);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    sc[h] = fmaf(qs[wl][h][c * 8 + 2 * e2], kf.x, sc[h]);
-                    sc[h] = fmaf(qs[wl][h][c * 8 + 2 * e2 + 1], kf.y, sc[h]);
-                }
+                k2[e2] = f2_pack(kf.x, kf.y);
             }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                uint64_t q0, q1, q2, q3;
+                ld_shared_v2_u64(qs_addr + (h * D + c * 8) * 4, q0, q1);
+                ld_shared_v2_u64(qs_addr + (h * D + c * 8 + 4) * 4, q2, q3);
+                ffma2_acc(sc2[h], q0, k2[0]);
+                ffma2_acc(sc2[h], q1, k2[1]);
+                ffma2_acc(sc2[h], q2, k2[2]);
+                ffma2_acc(sc2[h], q3, k2[3]);
+            }
+        }
+        float sc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float lo, hi;
+            f2_unpack(sc2[h], lo, hi);
+            sc[h] = lo + hi;
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
@@ -244,7 +267,8 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    kern<<<static_cast<unsigned>((warps + 3) / 4), kDecThreads, DecCfg<D>::kSmem, s>>>(a);
+    constexpr int kW = DecCfg<D>::kWarps;
+    kern<<<static_cast<unsigned>((warps + kW - 1) / kW), 32 * kW, DecCfg<D>::kSmem, s>>>(a);
     const int64_t cw = static_cast<int64_t>(a.B) * a.H;
     decode_combine_kernel<T, D><<<static_cast<unsigned>((cw + 3) / 4), kDecThreads, 0, s>>>(a);
     return cudaGetLastError();
@@ -277,9 +301,13 @@ int decode_parts_max(int64_t S_max) {
     return static_cast<int>(most < 256 ? most : 256);
 }
 
-int decode_parts(int64_t B, int64_t Hk, int64_t S_max, int num_sms) {
-    // about 16 warps per SM in flight, and at least 64 keys per part
-    const int64_t want = (16LL * num_sms + B * Hk - 1) / (B * Hk);
+int decode_parts(int64_t B, int64_t Hk, int64_t S_max, int64_t head_dim, int num_sms) {
+    // at least 64 keys per part; head_dim 64: about 16 warps per SM in all
+    // (two rounds of the eight resident); head_dim 128: one round of the six
+    // resident warps, each with a longer range, so its two-stage ring stays
+    // full and no partial round is left
+    const int64_t want = head_dim > 64 ? (6LL * num_sms) / (B * Hk)
+                                       : (16LL * num_sms + B * Hk - 1) / (B * Hk);
     const int64_t most = decode_parts_max(S_max);
     int64_t p = want < most ? want : most;
     if (p < 1) p = 1;

@@ -477,6 +477,14 @@ __device__ __forceinline__ void ffma2(float x0, float x1, uint64_t m, uint64_t c
         : "=f"(d0), "=f"(d1)
         : "f"(x0), "f"(x1), "l"(m), "l"(c));
 }
+// acc += a * b, both lanes in one instruction (a, b, acc: packed pairs).
+__device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+// Two 8-byte words from shared memory (16-byte aligned address).
+__device__ __forceinline__ void ld_shared_v2_u64(uint32_t addr, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
 // acc += (x0, x1), both lanes in one instruction.
 __device__ __forceinline__ void fadd2_acc(uint64_t& acc, float x0, float x1) {
     asm("{\n\t.reg .b64 rb;\n\t"

@@ -116,7 +116,7 @@ struct DecodeArgs {
 };
 cudaError_t launch_attention_decode(DType dt, const DecodeArgs& a, cudaStream_t s);
 // number of key ranges per (batch, kv head), and its device-independent bound
-int decode_parts(int64_t B, int64_t Hk, int64_t S_max, int num_sms);
+int decode_parts(int64_t B, int64_t Hk, int64_t S_max, int64_t head_dim, int num_sms);
 int decode_parts_max(int64_t S_max);
 
 // ---- per-device state and error reporting shared with other entry points (api.cu)
