@@ -22,7 +22,8 @@ from ._abi import BlkError  # noqa: F401
 
 __all__ = ["layernorm_bias", "rmsnorm", "qkv_bias_rope_partial", "rope_inplace", "attn_prefill",
            "attn_decode", "attn_decode_workspace_size", "decode_desc",
-           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host", "ForwardGraph", "HostPipe",
+           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host", "ForwardGraph", "HostPipe", "model_desc",
+           "model_workspace_size", "model_forward",
            "check_device_status", "BlkError", "library_path"]
 
 library_path = _abi.LIB_PATH
@@ -245,6 +246,70 @@ def forward(cfg, weights: dict, x, workspace=None, out=None):
     out = torch.empty_like(x) if out is None else out
     _abi.check(_lib().blk_forward(C.byref(desc), C.byref(w), _p(x), _p(out), _p(workspace),
                                   workspace.numel(), _dt(x), _stream()), "blk_forward")
+    return out
+
+
+def model_desc(cfg, batch: int, seq: int, n_layers: int, vocab: int, embed_norm: bool = False,
+               final_norm: str = "layernorm", final_eps: float = 1e-5) -> _abi.ModelDesc:
+    """Descriptor of an n_layers stack of cfg's block between the token
+    embedding and the logits (blk_model_forward)."""
+    return _abi.ModelDesc(block_desc(cfg, batch, seq), n_layers, vocab, 1 if embed_norm else 0,
+                          _abi.BLK_NORM_LAYERNORM if final_norm == "layernorm" else _abi.BLK_NORM_RMS,
+                          final_eps)
+
+
+def model_workspace_size(cfg, batch: int, seq: int, n_layers: int, vocab: int, **kw) -> int:
+    need = C.c_size_t(0)
+    desc = model_desc(cfg, batch, seq, n_layers, vocab, **kw)
+    _abi.check(_lib().blk_model_workspace_size(C.byref(desc), C.byref(need)),
+               "blk_model_workspace_size")
+    return need.value
+
+
+_MODEL_SLOTS = ("embed", "embed_norm_w", "embed_norm_b", "layers", "final_norm_w",
+                "final_norm_b", "lm_head")
+
+
+def model_forward(cfg, model_w: dict, tokens, vocab: int, embed_norm: bool = False,
+                  final_norm: str = "layernorm", final_eps: float = 1e-5, workspace=None,
+                  out=None):
+    """Token ids [B, S] (int32, CUDA) -> logits [B, S, vocab] in the storage
+    dtype, through len(model_w["layers"]) blocks. model_w holds ``embed``
+    [vocab, hidden], optional ``embed_norm_w``/``embed_norm_b``, ``layers``
+    (a list of block weight dicts), ``final_norm_w``, optional
+    ``final_norm_b`` and ``lm_head`` [vocab, hidden]."""
+    unknown = set(model_w) - set(_MODEL_SLOTS)
+    if unknown:
+        raise KeyError(f"unknown model slots: {sorted(unknown)}")
+    if tokens.dtype != torch.int32 or not tokens.is_cuda or tokens.dim() != 2:
+        raise ValueError("tokens must be a CUDA int32 tensor [batch, seq]")
+    B, S = tokens.shape
+    emb = model_w["embed"]
+    layers = model_w.get("layers", [])
+    desc = model_desc(cfg, B, S, len(layers), vocab, embed_norm, final_norm, final_eps)
+    need = model_workspace_size(cfg, B, S, len(layers), vocab, embed_norm=embed_norm,
+                                final_norm=final_norm, final_eps=final_eps)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=tokens.device)
+    arr = (_abi.BlockWeights * max(1, len(layers)))()
+    for i, lw in enumerate(layers):
+        bad = set(lw) - set(_abi.WEIGHT_SLOTS)
+        if bad:
+            raise KeyError(f"unknown weight slots in layer {i}: {sorted(bad)}")
+        for name, t in lw.items():
+            if name != "alibi_slopes":
+                _same(emb, t)
+        arr[i] = _abi.BlockWeights(*[_p(lw.get(n)) for n in _abi.WEIGHT_SLOTS])
+    for n in ("embed_norm_w", "embed_norm_b", "final_norm_w", "final_norm_b", "lm_head"):
+        _same(emb, model_w.get(n))
+    mw = _abi.ModelWeights(_p(emb), _p(model_w.get("embed_norm_w")), _p(model_w.get("embed_norm_b")),
+                           arr, _p(model_w.get("final_norm_w")), _p(model_w.get("final_norm_b")),
+                           _p(model_w.get("lm_head")))
+    out = torch.empty((B, S, vocab), dtype=emb.dtype, device=tokens.device) if out is None else out
+    _same(emb, out)
+    _abi.check(_lib().blk_model_forward(C.byref(desc), C.byref(mw), C.c_void_p(tokens.data_ptr()),
+                                        _p(out), _p(workspace), workspace.numel(), _dt(emb),
+                                        _stream()), "blk_model_forward")
     return out
 
 

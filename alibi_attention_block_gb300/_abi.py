@@ -62,6 +62,17 @@ class BlockWeights(C.Structure):
     _fields_ = [(n, vp) for n in WEIGHT_SLOTS]
 
 
+class ModelDesc(C.Structure):
+    _fields_ = [("block", BlockDesc), ("n_layers", i32), ("vocab", i64), ("embed_norm", i32),
+                ("final_norm", i32), ("final_eps", f32)]
+
+
+class ModelWeights(C.Structure):
+    _fields_ = [("embed", vp), ("embed_norm_w", vp), ("embed_norm_b", vp),
+                ("layers", C.POINTER(BlockWeights)), ("final_norm_w", vp), ("final_norm_b", vp),
+                ("lm_head", vp)]
+
+
 _PROTOS = {
     "blk_status_string": (C.c_char_p, [C.c_int]),
     "blk_last_error": (C.c_char_p, []),
@@ -94,6 +105,9 @@ _PROTOS = {
     "blk_graph_destroy": (C.c_int, [vp]),
     "blk_forward_host": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp, vp,
                                    vp, C.c_size_t, i32, C.c_int, vp]),
+    "blk_model_workspace_size": (C.c_int, [C.POINTER(ModelDesc), C.POINTER(C.c_size_t)]),
+    "blk_model_forward": (C.c_int, [C.POINTER(ModelDesc), C.POINTER(ModelWeights), vp, vp, vp,
+                                    C.c_size_t, C.c_int, vp]),
     "blk_host_pipe_mem_size": (C.c_int, [C.POINTER(BlockDesc), i32, C.POINTER(C.c_size_t)]),
     "blk_host_pipe_create": (C.c_int, [C.POINTER(BlockDesc), i32, C.c_int, vp, C.c_size_t,
                                        C.POINTER(vp)]),

@@ -13,6 +13,7 @@
 
 #include "blk.h"
 #include "internal.h"
+#include "model.h"
 
 namespace blk {
 
@@ -1030,6 +1031,122 @@ blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
     e = cudaEventRecord(ds->ev_done, ds->copy_out);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ds->ev_done, 0);
     return e == cudaSuccess ? BLK_OK : cuda_fail(e, "stream ordering");
+}
+
+namespace {
+
+struct ModelLayout {
+    size_t x0, x1, n, blk, total, blk_bytes;
+};
+
+ModelLayout model_layout(const blk_model_desc* d) {
+    const auto& q = d->block.qkv;
+    const size_t act = align256(static_cast<size_t>(q.batch) * q.seq * q.hidden * 2);
+    ModelLayout L;
+    L.x0 = 0;
+    L.x1 = act;
+    L.n = 2 * act;
+    L.blk = 3 * act;
+    L.blk_bytes = forward_layout(&d->block).total;
+    L.total = L.blk + L.blk_bytes;
+    return L;
+}
+
+blk_status validate_model_desc(const blk_model_desc* d) {
+    BLK_REQUIRE(d != nullptr, "descriptor is NULL");
+    blk_status st = validate_qkv_desc(&d->block.qkv);
+    if (st != BLK_OK) return st;
+    BLK_REQUIRE(d->block.intermediate >= 8 && d->block.intermediate % 8 == 0,
+                "intermediate must be a positive multiple of 8");
+    BLK_REQUIRE(d->n_layers >= 0 && d->n_layers <= 4096, "n_layers must be in [0, 4096]");
+    BLK_REQUIRE(d->vocab >= 8 && d->vocab % 8 == 0 && d->vocab <= kI32,
+                "vocab must be a positive multiple of 8");
+    BLK_REQUIRE(d->embed_norm == 0 || d->embed_norm == 1, "embed_norm must be 0 or 1");
+    BLK_REQUIRE(d->final_norm == BLK_NORM_LAYERNORM || d->final_norm == BLK_NORM_RMS,
+                "unknown final_norm");
+    BLK_REQUIRE(std::isfinite(d->final_eps) && d->final_eps >= 0.f, "final_eps must be >= 0");
+    BLK_REQUIRE(d->block.qkv.hidden <= 16384, "hidden must be <= 16384");
+    return BLK_OK;
+}
+
+}  // namespace
+
+blk_status blk_model_workspace_size(const blk_model_desc* d, size_t* bytes) {
+    BLK_REQUIRE(bytes != nullptr, "NULL argument");
+    blk_status st = validate_model_desc(d);
+    if (st != BLK_OK) return st;
+    *bytes = model_layout(d).total;
+    return BLK_OK;
+}
+
+blk_status blk_model_forward(const blk_model_desc* d, const blk_model_weights* w,
+                             const int32_t* tokens, void* logits, void* workspace,
+                             size_t ws_bytes, blk_dtype dt, blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    blk_status st = validate_model_desc(d);
+    if (st != BLK_OK) return st;
+    BLK_REQUIRE(w != nullptr, "weights is NULL");
+    BLK_REQUIRE(tokens != nullptr, "tokens is NULL");
+    BLK_CHECK_PTR(logits, true);
+    BLK_CHECK_PTR(w->embed, true);
+    BLK_CHECK_PTR(w->lm_head, true);
+    BLK_CHECK_PTR(w->final_norm_w, true);
+    BLK_CHECK_PTR(w->final_norm_b, false);
+    BLK_REQUIRE(d->final_norm == BLK_NORM_LAYERNORM || !w->final_norm_b,
+                "final_norm_b is only read by a LayerNorm final norm");
+    if (d->embed_norm) {
+        BLK_CHECK_PTR(w->embed_norm_w, true);
+        BLK_CHECK_PTR(w->embed_norm_b, false);
+    } else {
+        BLK_REQUIRE(!w->embed_norm_w && !w->embed_norm_b,
+                    "embed_norm weights given but embed_norm is 0");
+    }
+    BLK_REQUIRE(d->n_layers == 0 || w->layers != nullptr, "layers is NULL");
+    for (int32_t l = 0; l < d->n_layers; ++l) {
+        st = validate_block(&d->block, &w->layers[l]);
+        if (st != BLK_OK) return st;
+    }
+    const ModelLayout L = model_layout(d);
+    if (!workspace || ws_bytes < L.total || !aligned16(workspace))
+        return fail(BLK_EWORKSPACE, "workspace needs %zu bytes, 16-byte aligned", L.total);
+    DevState* ds = nullptr;
+    if ((st = dev_state(&ds)) != BLK_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    const DType t = to_dt(dt);
+    const auto& q = d->block.qkv;
+    const int64_t T = q.batch * q.seq;
+    const int D = static_cast<int>(q.hidden);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* xa = ws + L.x0;
+    void* xb = ws + L.x1;
+    void* nb = ws + L.n;
+    // 1. embedding rows of the tokens
+    cudaError_t e = launch_embed_gather(t, tokens, w->embed, xa, T, D, d->vocab, ds->sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "embedding gather launch");
+    // 2. (Bloom) LayerNorm of the embeddings
+    if (d->embed_norm) {
+        e = launch_norm(t, false, NormIO{xa, false, nullptr, false, xb, nullptr, ds->err, ds->sms},
+                        w->embed_norm_w, w->embed_norm_b, T, D, d->block.eps, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "embedding norm launch");
+        void* tmp = xa;
+        xa = xb;
+        xb = tmp;
+    }
+    // 3. the blocks, ping-pong between the two activations
+    for (int32_t l = 0; l < d->n_layers; ++l) {
+        st = blk_forward(&d->block, &w->layers[l], xa, xb, ws + L.blk, L.blk_bytes, dt, s);
+        if (st != BLK_OK) return st;
+        void* tmp = xa;
+        xa = xb;
+        xb = tmp;
+    }
+    // 4. final norm and the vocabulary projection
+    e = launch_norm(t, d->final_norm == BLK_NORM_RMS,
+                    NormIO{xa, false, nullptr, false, nb, nullptr, ds->err, ds->sms},
+                    w->final_norm_w, w->final_norm_b, T, D, d->final_eps, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "final norm launch");
+    return run_linear(t, EPI_LINEAR, nb, w->lm_head, nullptr, nullptr, nullptr, nullptr, logits, T,
+                      d->vocab, D, cs, ds);
 }
 
 constexpr int kMaxPipeDepth = 4;

@@ -262,6 +262,77 @@ def run_attn_sweep(args, rank):
               flush=True)
 
 
+def run_model(args, rank):
+    """The model-level wrap (blk_model_forward) at StableLM-2-1.6B's printed
+    shape: 24 blocks, embedding and untied lm_head over a 100352-token
+    vocabulary (nnterp "stablelm" Printout), B4 S2048 token ids in, bf16
+    logits out. Every layer has its own weights (2.5 GB in all), drawn on the
+    device from a seeded generator; the working set is far above L2."""
+    import alibi_attention_block_gb300 as blk
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    cfg = workloads.BLOCK_CONFIGS["stablelm2_1p6b"]
+    n_layers, vocab = 24, 100352
+    g = torch.Generator(device=dev).manual_seed(1234)
+    dt = workloads.storage_dtype(cfg.dtype)
+    shapes = workloads.weight_shapes(cfg)
+
+    def draw(shape, kind):
+        t = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        if kind != "x":
+            t = t * 0.02
+        if kind == "g":
+            t = t + 1.0
+        return t.to(dt)
+
+    layers = [{n: draw(shape, kind) for n, (shape, kind) in shapes.items()} for _ in range(n_layers)]
+    mw = {"embed": draw((vocab, cfg.hidden), "x"), "layers": layers,
+          "final_norm_w": draw((cfg.hidden,), "g"), "final_norm_b": draw((cfg.hidden,), "b"),
+          "lm_head": draw((vocab, cfg.hidden), "w")}
+    tokens = torch.randint(0, vocab, (cfg.batch, cfg.seq), generator=g, device=dev,
+                           dtype=torch.int32)
+    ws = torch.empty(blk.model_workspace_size(cfg, cfg.batch, cfg.seq, n_layers, vocab),
+                     dtype=torch.uint8, device=dev)
+    logits = torch.empty((cfg.batch, cfg.seq, vocab), dtype=dt, device=dev)
+
+    def step():
+        blk.model_forward(cfg, mw, tokens, vocab, workspace=ws, out=logits)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    blk.check_device_status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as sampler:
+        sampler.mark_start()
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        sampler.mark_end()
+    blk.check_device_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    tokens_n = cfg.batch * cfg.seq
+    work = step_work(cfg)
+    kinds = ("qkv", "attention", "o_proj", "mlp_up", "mlp_down")
+    block_flops = sum(work[k]["flops"] for k in kinds)
+    head_flops = 2.0 * tokens_n * cfg.hidden * vocab
+    flops = n_layers * block_flops + head_flops
+    if rank == 0:
+        print(json.dumps({
+            "metric": "model-level prefill tokens/s (24 blocks + embedding + lm_head)",
+            "value": tokens_n / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic (seeded device draws: N(0,1) embeddings, N(0,0.02) weights)",
+            "config": {"workload": "stablelm2_1p6b 24-layer model prefill", "global_batch": cfg.batch,
+                       "seq_len": cfg.seq, "layers": n_layers, "vocab": vocab,
+                       "l2": "not flushed: 2.5 GB of weights per step"},
+            "model_tflops": flops / (ms / 1e3) / 1e12,
+            "clocks": sampler.summary()}), flush=True)
+
+
 def run_decode(args, rank):
     """Decode-step attention (blk_attn_decode) over KV caches larger than L2:
     HBM bound, reported against the measured copy bandwidth. Algorithmic
@@ -609,6 +680,8 @@ def main():
                          "blk_forward_host (copies overlapped over groups of sequences)")
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="groups of sequences blk_forward_host overlaps copies and compute over")
+    ap.add_argument("--model", action="store_true",
+                    help="time the 24-layer StableLM-2-1.6B model wrap (embedding, blocks, lm_head)")
     ap.add_argument("--decode", action="store_true",
                     help="time decode-step attention over KV caches instead of the block")
     ap.add_argument("--attn-sweep", action="store_true",
@@ -620,6 +693,8 @@ def main():
     dist, rank, world, local_rank = _dist()
     if args.attn_sweep:
         run_attn_sweep(args, rank)
+    elif args.model:
+        run_model(args, rank)
     elif args.decode:
         run_decode(args, rank)
     elif args.impl == "reference":

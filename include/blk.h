@@ -315,6 +315,44 @@ blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
                             void* workspace, size_t ws_bytes, int32_t n_chunks, blk_dtype dt,
                             blk_stream_t s);
 
+/* ---- model-level wrap ------------------------------------------------- */
+
+/* A stack of n_layers blocks of one shape between the token embedding and
+ * the logits: x = embed[tokens]; for Bloom ("Bloom in a sovereign engine",
+ * Contribution (2): a layernorm on the embeddings before the first block)
+ * x = LN(x); x = block_l(x) for l = 0 .. n_layers-1; logits = norm(x)
+ * lm_head^T (nnterp "stablelm" Printout and Config: a final LayerNorm with
+ * bias, then lm_head, tie_word_embeddings False). */
+typedef struct {
+    blk_block_desc block; /* every layer's shapes and variant */
+    int32_t n_layers;     /* >= 0 */
+    int64_t vocab;        /* >= 8, a multiple of 8 */
+    int32_t embed_norm;   /* 1: LayerNorm (bias nullable) on the embeddings before layer 0 */
+    int32_t final_norm;   /* blk_norm_kind of the final norm */
+    float final_eps;
+} blk_model_desc;
+
+typedef struct {
+    const void* embed;                       /* [vocab, hidden] */
+    const void *embed_norm_w, *embed_norm_b; /* embed_norm only (bias nullable) */
+    const blk_block_weights* layers;         /* HOST array of n_layers weight sets */
+    const void *final_norm_w, *final_norm_b; /* final_norm_b: LayerNorm bias, nullable */
+    const void* lm_head;                     /* [vocab, hidden] */
+} blk_model_weights;
+
+/* Workspace bytes blk_model_forward needs: two [batch, seq, hidden]
+ * activations, the final norm's output and one block's workspace. */
+blk_status blk_model_workspace_size(const blk_model_desc* d, size_t* bytes);
+
+/* tokens: device int32 [batch, seq]; logits: device [batch, seq, vocab] in
+ * the storage dtype. Token ids live in device memory, so the host cannot
+ * check them: an id outside [0, vocab) reads row 0 of the embedding (the
+ * kernel clamps the index; nothing outside the table is read). Weights are
+ * validated per layer as blk_forward does; everything runs on stream s. */
+blk_status blk_model_forward(const blk_model_desc* d, const blk_model_weights* w,
+                             const int32_t* tokens, void* logits, void* workspace,
+                             size_t ws_bytes, blk_dtype dt, blk_stream_t s);
+
 /* A pipeline of block forwards over a stream of host batches, for serving:
  * blk_host_pipe_submit enqueues one batch and returns. Batch n is copied in
  * (pinned x_host, [batch, seq, hidden] as in the desc) on a copy stream the

@@ -21,3 +21,4 @@ from .block import (  # noqa: F401
     qk_norm_full_rms, qk_norm_per_head_ln, rope_inv_freq, rope, alibi_slopes,
     attention, attention_decode, silu, gelu_tanh, mlp, block_forward, attention_forward,
 )
+from .model import model_forward  # noqa: F401

@@ -231,6 +231,40 @@ def test_host_pipe_validation(lib):
     assert lib.blk_host_pipe_destroy(None) == _abi.BLK_OK
 
 
+def test_model_validation(lib):
+    """blk_model_*: descriptor and argument checks before any CUDA call."""
+    d = _abi.ModelDesc(_block(), 2, 1000, 0, _abi.BLK_NORM_LAYERNORM, 1e-5)
+    need, blk = C.c_size_t(0), C.c_size_t(0)
+    assert lib.blk_model_workspace_size(C.byref(d), C.byref(need)) == _abi.BLK_OK
+    assert lib.blk_forward_workspace_size(C.byref(d.block), C.byref(blk)) == _abi.BLK_OK
+    q = d.block.qkv
+    act = (q.batch * q.seq * q.hidden * 2 + 255) // 256 * 256
+    assert need.value == 3 * act + blk.value  # two activations, the final norm, one block
+    for bad in (_abi.ModelDesc(_block(), -1, 1000, 0, 0, 1e-5),   # n_layers
+                _abi.ModelDesc(_block(), 2, 1004, 0, 0, 1e-5),    # vocab % 8
+                _abi.ModelDesc(_block(), 2, 1000, 2, 0, 1e-5),    # embed_norm
+                _abi.ModelDesc(_block(), 2, 1000, 0, 7, 1e-5)):   # final_norm
+        assert lib.blk_model_workspace_size(C.byref(bad), C.byref(need)) == _abi.BLK_EINVAL
+    layers = (_abi.BlockWeights * 2)(_weights(), _weights())
+    w = _abi.ModelWeights(FAKE, None, None, layers, FAKE, FAKE, FAKE)
+    args = (C.byref(d), C.byref(w))
+    assert lib.blk_model_forward(*args, None, FAKE, FAKE, 1 << 40, 1, None) == _abi.BLK_EINVAL
+    assert "tokens" in _err(lib)
+    assert lib.blk_model_forward(*args, FAKE, FAKE, FAKE, 16, 1, None) == _abi.BLK_EWORKSPACE
+    no_head = _abi.ModelWeights(FAKE, None, None, layers, FAKE, FAKE, None)
+    assert lib.blk_model_forward(C.byref(d), C.byref(no_head), FAKE, FAKE, FAKE, 1 << 40, 1,
+                                 None) == _abi.BLK_EINVAL
+    stray = _abi.ModelWeights(FAKE, FAKE, None, layers, FAKE, FAKE, FAKE)  # embed_norm is 0
+    assert lib.blk_model_forward(C.byref(d), C.byref(stray), FAKE, FAKE, FAKE, 1 << 40, 1,
+                                 None) == _abi.BLK_EINVAL
+    rms = _abi.ModelDesc(_block(), 2, 1000, 0, _abi.BLK_NORM_RMS, 1e-6)  # RMS has no bias
+    assert lib.blk_model_forward(C.byref(rms), C.byref(w), FAKE, FAKE, FAKE, 1 << 40, 1,
+                                 None) == _abi.BLK_EINVAL
+    empty = _abi.ModelWeights(FAKE, None, None, None, FAKE, FAKE, FAKE)  # layers NULL
+    assert lib.blk_model_forward(C.byref(d), C.byref(empty), FAKE, FAKE, FAKE, 1 << 40, 1,
+                                 None) == _abi.BLK_EINVAL
+
+
 def test_decode_validation(lib):
     """blk_attn_decode: shape rules and workspace size without a GPU."""
     d = _abi.DecodeDesc(4, 2048, 32, 8, 64, -1.0, 0)

@@ -224,6 +224,28 @@ def block_inputs(cfg: BlockConfig, seed: int | None = None):
     return x, weights
 
 
+def model_inputs(cfg: BlockConfig, n_layers: int, vocab: int, embed_norm: bool = False,
+                 final_norm: str = "layernorm", seed: int | None = None):
+    """(tokens, model weights) for the model-level wrap, as CPU tensors:
+    tokens int32 [batch, seq] uniform over the vocabulary; embed [vocab, D]
+    ~ N(0, 1); per layer the block's weights (drawn as ``block_inputs`` does,
+    seed + 1 + layer); norm gains ~ 1 + N(0, 0.02^2), shifts and lm_head
+    ~ N(0, 0.02^2)."""
+    base = cfg.seed if seed is None else seed
+    rng = np.random.Generator(np.random.PCG64(base))
+    tokens = torch.from_numpy(rng.integers(0, vocab, size=(cfg.batch, cfg.seq)).astype(np.int32))
+    mw = {"embed": _to_storage(_draw(rng, (vocab, cfg.hidden), "x"), cfg.dtype)}
+    if embed_norm:
+        mw["embed_norm_w"] = _to_storage(_draw(rng, (cfg.hidden,), "g"), cfg.dtype)
+        mw["embed_norm_b"] = _to_storage(_draw(rng, (cfg.hidden,), "b"), cfg.dtype)
+    mw["layers"] = [block_inputs(cfg, seed=base + 1 + layer)[1] for layer in range(n_layers)]
+    mw["final_norm_w"] = _to_storage(_draw(rng, (cfg.hidden,), "g"), cfg.dtype)
+    if final_norm == "layernorm":
+        mw["final_norm_b"] = _to_storage(_draw(rng, (cfg.hidden,), "b"), cfg.dtype)
+    mw["lm_head"] = _to_storage(_draw(rng, (vocab, cfg.hidden), "w"), cfg.dtype)
+    return tokens, mw
+
+
 def attn_inputs(cfg: AttnConfig, seed: int | None = None):
     """Head-split q [B,H,S,d], k and v [B,Hk,S,d] ~ N(0,1), plus optional biases.
 
