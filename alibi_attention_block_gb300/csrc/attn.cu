@@ -1,10 +1,13 @@
-// K3: causal softmax attention, flash-style, on tcgen05 tensor cores.
+// K3: causal softmax attention, flash-style, on tcgen05 tensor cores: the
+// single-query-tile kernel, which serves head_dim 160 (head_dim 64 and 128
+// run the paired-query-tile kernels of attn_pair.cu and attn_pair128.cu; at
+// 160 two query tiles' O no longer leave TMEM room for S and P), and the
+// dispatch by head_dim.
 //
 // Persistent: each CTA walks (128-query tile, batch, head) items, heaviest
 // (latest) query tiles first, keeping its TMEM and barriers; the next item's
 // Q loads into a second buffer and its first QK^T overlaps the current item's
-// last tile. At head_dim 64 two CTAs share an SM, so one CTA's MMAs run while
-// the other's softmax warps compute. 10 warps:
+// last tile. 10 warps:
 //   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into a
 //               STAGES-deep ring (128-byte swizzle, 64-column boxes). A K
 //               slot is refilled once its QK^T has completed and a V slot once
