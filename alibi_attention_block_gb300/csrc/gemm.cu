@@ -1,17 +1,23 @@
 // K2: C = A B^T on tcgen05 tensor cores, with the block's epilogues fused.
 //
 // A [M, K] (activations) and B [N, K] (a torch-convention weight W[out, in])
-// are both K-major. Persistent kernel, one CTA per SM, 6 warps:
+// are both K-major. Persistent kernel, one CTA per SM, 10 warps:
 //   warp 0      TMA producer: 128x64 A tile and BNx64 B tile per stage
 //               (128-byte swizzle) into a STAGES-deep shared-memory ring
 //   warp 1      TMEM allocator and single-thread MMA issuer:
 //               tcgen05.mma.cta_group::1.kind::f16, M=128, N=BN, K=16 per
 //               instruction, fp32 accumulators in TMEM, double-buffered so
 //               the epilogue of tile i overlaps the mainloop of tile i+1
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per load (one
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (a warp reaches
+//               the quarter of its index mod 4), each with half of the tile's
+//               columns: tcgen05.ld 32 lanes x 32 columns per load (one
 //               thread per output row), fused op, 16-byte global stores per
 //               row; fp32 outputs go through 4 KB of shared memory per warp
 //               so that each store instruction writes whole lines
+// When the work units end in a partial round, the units of that round may
+// be split in two along K (long K only): each half publishes an fp32
+// partial tile and the half that finishes second sums both and runs the
+// epilogue (a separate kernel instance; see launch_cl).
 // Epilogues (the block's steps after each projection):
 //   EPI_LINEAR  + bias, + up to two residuals (o_proj and down_proj residual
 //               adds); residuals and output may be fp32 (the block keeps its

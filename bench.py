@@ -48,17 +48,23 @@ _KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # profiles/gemm_gate_up_and_down_stablelm2_1p6b.md: 81.82 MB read + 62.91 MB written
     "mlp_up": {"kind": "gemm", "bytes": 144739072,
-               "sha256": "aabe8a2ae5a357b0c3a30758a4c96bdfc8850fbdcb6b89c7105767faf67dbc3e"},
+               "sha256": "b3f47797dba85fa5894489f4f83b76662c7f9fcec3fbdec482abb90ae6993f2e"},
 }
 
 
 def _sources_sha(kind: str) -> str:
+    """SHA-256 of the kernel's sources with // comments and blank lines
+    dropped: an edit to a comment does not change the kernel, any edit to code
+    does."""
     import hashlib
     h = hashlib.sha256()
     root = os.path.dirname(os.path.abspath(__file__))
     for rel in _KERNEL_SOURCES[kind]:
-        with open(os.path.join(root, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(root, rel), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 
