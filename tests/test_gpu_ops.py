@@ -9,7 +9,7 @@ import torch
 import alibi_attention_block_gb300 as blk
 import oracle
 import workloads
-from tests.parity import check, f64, to_dev
+from tests.parity import check, f64, row_cosine, to_dev
 from workloads import draw
 
 pytestmark = pytest.mark.gpu
@@ -231,6 +231,65 @@ def test_attention(dt, case):
     ref = oracle.attention(f64(q), f64(k), f64(v), slopes=oracle.alibi_slopes(H) if alibi else None)
     # outputs are convex combinations of unit-scale value rows: unit scale
     check(o, ref.transpose(0, 2, 1, 3), f"attention {case}", unit_scale=True)
+
+
+@pytest.mark.parametrize("name", ["attn_s16384", "attn_12b"])
+def test_attention_sweep_full_size_sampled(name):
+    """The attention sweep at its full sizes (B2 S16384 H32x64 with QKV bias
+    and r16; the 12B shape B2 S4096 H32/Hk8 x160 r40), run as bench.py runs
+    it: bias and rotary in place (blk_rope_inplace), then blk_attn_prefill,
+    on sampled query rows of every (batch, head). Each step is held to its
+    own bar, and the two together to the floor the storage dtype sets:
+    - rotary: within one bf16 ulp of the oracle's bias + rotary;
+    - attention: the usual gate against the oracle on exactly the q/k/v
+      the kernel received;
+    - both: per row, no worse than the oracle's own q/k/v rounded to the
+      storage dtype do against the exact oracle (minus 1e-4), and max abs
+      within 2e-2. That floor falls with the sequence length (min cosine
+      ~0.9995 at S=16384: a late row averages thousands of value rows, and
+      the logit perturbation of bf16 q/k does not average out); any
+      bf16 tensor-core attention shares it."""
+    c = workloads.ATTN_CONFIGS[name]
+    q, k, v, biases = workloads.attn_inputs(c)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    bd = [to_dev(t) for t in biases] if biases else None
+    blk.rope_inplace(qd, bd[0] if bd else None, rotary_span=c.rotary_span, rope_base=c.rope_base)
+    blk.rope_inplace(kd, bd[1] if bd else None, rotary_span=c.rotary_span, rope_base=c.rope_base)
+    if bd:
+        blk.rope_inplace(vd, bd[2], rotary_span=0, rope_base=c.rope_base)
+    o = blk.attn_prefill(qd, kd, vd, alibi=c.alibi)
+    blk.check_device_status()
+    rows = workloads.sample_rows(c.seq, 24, seed=c.seed)
+    H, Hk, d = c.n_heads, c.n_kv_heads, c.head_dim
+    # the oracle's bias + rotary in fp64
+    pos = np.arange(c.seq)
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    if biases is not None:
+        qf = qf + f64(biases[0]).reshape(H, d)[None, :, None, :]
+        kf = kf + f64(biases[1]).reshape(Hk, d)[None, :, None, :]
+        vf = vf + f64(biases[2]).reshape(Hk, d)[None, :, None, :]
+    qf = oracle.rope(qf, pos, c.rotary_span, c.rope_base)
+    kf = oracle.rope(kf, pos, c.rotary_span, c.rope_base)
+    # 1. rotary: one bf16 ulp (2^-7 relative) of the exact value, plus the
+    # fp32 rotation's own absolute error (angles to ~1e-6 rad on unit-scale
+    # inputs) where a rotated value cancels to near zero
+    for gpu_t, ref_t, label in ((qd, qf, "q"), (kd, kf, "k"), (vd, vf, "v")):
+        g = f64(gpu_t)
+        assert (np.abs(g - ref_t) <= 2.0 ** -7 * np.abs(ref_t) + 4e-6).all(), f"{name} rotary {label}"
+    # 2. attention on exactly what the kernel received
+    qg, kg, vg = f64(qd), f64(kd), f64(vd)
+    slopes = oracle.alibi_slopes(H) if c.alibi else None
+    got = f64(o[:, torch.as_tensor(rows, device=o.device)].permute(0, 2, 1, 3))
+    ref_k = oracle.attention(qg[:, :, rows], kg, vg, slopes=slopes, q_positions=rows)
+    check(got, ref_k, f"{name} attention kernel", unit_scale=True)
+    # 3. composition against the exact oracle, at the storage floor
+    exact = oracle.attention(qf[:, :, rows], kf, vf, slopes=slopes, q_positions=rows)
+    bf = lambda a: torch.from_numpy(a).to(qd.dtype).double().numpy()
+    stored = oracle.attention(bf(qf)[:, :, rows], bf(kf), bf(vf), slopes=slopes, q_positions=rows)
+    floor = row_cosine(stored, exact)
+    cos = row_cosine(got, exact)
+    assert (cos >= np.minimum(floor, 0.9999) - 1e-4).all(), f"{name}: below the storage floor"
+    assert np.abs(got - exact).max() <= 2e-2
 
 
 @pytest.mark.parametrize("d", [64, 128])
