@@ -85,6 +85,20 @@ def _peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def _max_over_ranks(dist, ms: float, device) -> float:
+    """The slowest rank's time (MAX all-reduce); the value itself on one rank."""
+    if not dist:
+        return ms
+    t = torch.tensor([ms], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_throughput(world: int, tokens_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_step * steps / (total_ms / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
@@ -541,13 +555,9 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         for j, name in enumerate(step_names):
             per_kind.setdefault(name, []).append(e[j].elapsed_time(e[j + 1]))
     kernel_ms = {k: float(np.mean(v)) for k, v in per_kind.items()}
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = _max_over_ranks(dist, float(sum(step_ms)), dev)
     ms_per_step = total_ms / args.steps
-    value = world * cfg.tokens * args.steps / (total_ms / 1e3)
+    value = _job_throughput(world, cfg.tokens, args.steps, total_ms)
 
     # e2e through the public API, pinned host x -> pinned host y every step:
     # blk_host_pipe_* (default: step n's copy in overlaps step n-1's block, its
@@ -589,11 +599,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
     e2e_end()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, dev)
 
     standalone = standalone_hbm(blk, dev) if rank == 0 else None
     if rank != 0:
