@@ -460,6 +460,31 @@ def run_reference(args, cfg, rank, world, budget_s: float = 150.0):
     print(json.dumps(line), flush=True)
 
 
+def _provenance(cfg, x_cpu, w_cpu, device=None) -> dict:
+    """What the numbers were measured on: the library's source hash, the
+    seeded inputs (seed and a hash of their bytes), the GPU, and the git
+    revision where a checkout is present."""
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    src = hashlib.sha256()
+    csrc = os.path.join(root, "alibi_attention_block_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)) + ["../../include/blk.h"]:
+        with open(os.path.normpath(os.path.join(csrc, name)), "rb") as f:
+            src.update(f.read())
+    inp = hashlib.sha256()
+    for t in [x_cpu] + [w_cpu[n] for n in sorted(w_cpu)]:
+        inp.update(t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32)
+                   .numpy().tobytes())
+    try:
+        rev = subprocess.run(["git", "-C", root, "rev-parse", "HEAD"], capture_output=True,
+                             text=True, timeout=5).stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        rev = None
+    gpu = torch.cuda.get_device_name(device) if device is not None else None
+    return {"sources_sha256": src.hexdigest(), "seed": cfg.seed,
+            "inputs_sha256": inp.hexdigest(), "gpu": gpu, "git_rev": rev}
+
+
 def _config(cfg, l2):
     return {"workload": f"{cfg.name} block prefill", "global_batch": cfg.batch, "seq_len": cfg.seq,
             "hidden": cfg.hidden, "heads": cfg.n_heads, "kv_heads": cfg.n_kv_heads,
@@ -670,6 +695,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
         "wall_s_timed": t_wall,
+        "provenance": _provenance(cfg, x_cpu, w_cpu, dev),
     }
     print(json.dumps(line), flush=True)
 
