@@ -485,6 +485,14 @@ def _provenance(cfg, x_cpu, w_cpu, device=None) -> dict:
             "inputs_sha256": inp.hexdigest(), "gpu": gpu, "git_rev": rev}
 
 
+def _safe_provenance(cfg, x_cpu, w_cpu, device) -> dict:
+    """_provenance, never failing the bench line over a bookkeeping field."""
+    try:
+        return _provenance(cfg, x_cpu, w_cpu, device)
+    except Exception as e:  # noqa: BLE001
+        return {"error": repr(e)}
+
+
 def _config(cfg, l2):
     return {"workload": f"{cfg.name} block prefill", "global_batch": cfg.batch, "seq_len": cfg.seq,
             "hidden": cfg.hidden, "heads": cfg.n_heads, "kv_heads": cfg.n_kv_heads,
@@ -695,7 +703,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
         "wall_s_timed": t_wall,
-        "provenance": _provenance(cfg, x_cpu, w_cpu, dev),
+        "provenance": _safe_provenance(cfg, x_cpu, w_cpu, dev),
     }
     print(json.dumps(line), flush=True)
 
