@@ -26,3 +26,18 @@ def test_oracle_is_deterministic():
     y1 = oracle.block_forward(CFG, x, w)["y"]
     y2 = oracle.block_forward(CFG, x, w)["y"]
     assert np.array_equal(y1, y2)
+
+
+def test_kernel_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """The hash that ties the recorded ncu traffic to the GEMM's sources is
+    blind to comment and blank-line edits and sees any code edit."""
+    import os
+    src = tmp_path / "k.cu"
+    src.write_text("int a = 1;  // first\n\nint b = 2;\n")
+    monkeypatch.setitem(bench._KERNEL_SOURCES, "probe", (os.path.relpath(src, os.path.dirname(
+        os.path.abspath(bench.__file__))),))
+    h0 = bench._sources_sha("probe")
+    src.write_text("// a new comment\nint a = 1;  // changed\nint b = 2;\n\n")
+    assert bench._sources_sha("probe") == h0
+    src.write_text("int a = 1;\nint b = 3;\n")
+    assert bench._sources_sha("probe") != h0
