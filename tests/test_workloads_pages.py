@@ -66,3 +66,26 @@ def test_olmo2_facts():
 def test_slots_are_distinct(name):
     s = weight_shapes(BLOCK_CONFIGS[name])
     assert len(set(s)) == len(s)
+
+
+def test_stablelm2_1p6b_model_facts_match_the_model_bench_and_oracle():
+    """bench.py --model and the model wrap use the printed model shape: 24
+    layers, a 100352-token vocabulary, an untied bias-free lm_head and a
+    final LayerNorm with bias."""
+    import inspect
+
+    import bench
+    import workloads
+    g = _read("stablelm2_1p6b_model.txt")
+    src = inspect.getsource(bench.run_model)
+    assert f"n_layers, vocab = {int(g['num_hidden_layers'])}, {int(g['vocab_size'])}" in src
+    c = BLOCK_CONFIGS["stablelm2_1p6b"]
+    assert c.hidden == int(g["embed_dim"]) and c.eps == float(g["final_norm_eps"])
+    assert g["tie_word_embeddings"] == "False" and g["lm_head_bias"] == "False"
+    # the model inputs draw separate embedding and lm_head tables, a final
+    # LayerNorm with a bias, and no lm_head bias slot
+    _, mw = workloads.model_inputs(workloads.BLOCK_CONFIGS["tiny_stablelm2"], 1, 64)
+    assert mw["embed"].data_ptr() != mw["lm_head"].data_ptr()
+    assert ("final_norm_b" in mw) == (g["final_norm_bias"] == "True")
+    assert not any(k.startswith("lm_head_b") for k in mw)
+
