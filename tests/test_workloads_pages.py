@@ -89,3 +89,18 @@ def test_stablelm2_1p6b_model_facts_match_the_model_bench_and_oracle():
     assert ("final_norm_b" in mw) == (g["final_norm_bias"] == "True")
     assert not any(k.startswith("lm_head_b") for k in mw)
 
+
+def test_bloom_facts():
+    """The Bloom workload follows its page: ALiBi without rotary, the fused
+    QKV in per-head interleaved order, f16, and the embedding LayerNorm in
+    the model wrap's inputs."""
+    import workloads
+    g = _read("bloom_block.txt")
+    c = BLOCK_CONFIGS["bloom_560m"]
+    assert c.alibi == (g["alibi"] == "True")
+    assert (c.rotary_span > 0) == (g["rotary"] == "True")
+    assert (c.qkv_layout == "head_interleaved") == (g["fused_qkv_deinterleave"] == "True")
+    assert c.dtype == "fp16" and g["precision"] == "f16"
+    _, mw = workloads.model_inputs(c, 0, 64, embed_norm=g["embedding_layernorm"] == "True")
+    assert "embed_norm_w" in mw and "embed_norm_b" in mw
+
