@@ -22,3 +22,4 @@ from .block import (  # noqa: F401
     attention, attention_decode, silu, gelu_tanh, mlp, block_forward, attention_forward,
 )
 from .model import model_forward  # noqa: F401
+from .quant import q8_0_quantize, q8_0_dequantize, linear_q8_0  # noqa: F401

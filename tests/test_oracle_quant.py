@@ -1,0 +1,66 @@
+"""Pins of the Q8_0 weight oracle (CPU): closed forms and exact cases."""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+RNG = np.random.Generator(np.random.PCG64(77))
+
+
+def test_error_bound_is_half_a_step_per_block():
+    """|w - d q| <= d / 2 everywhere (round to nearest), and the block's
+    largest |w| maps to |q| = 127 (up to the fp16 rounding of d)."""
+    w = RNG.standard_normal((48, 256)) * 0.02
+    q, d = oracle.q8_0_quantize(w)
+    err = np.abs(w - oracle.q8_0_dequantize(q, d)).reshape(48, 8, 32)
+    df = d.astype(np.float64)
+    assert (err <= df[..., None] / 2 * (1 + 1e-3) + 1e-12).all()
+    top = np.abs(q.reshape(48, 8, 32)).max(axis=-1)
+    assert ((top >= 126) & (top <= 127)).all()
+
+
+def test_exact_round_trip_of_representable_weights():
+    """A weight that is already d * q with |q| <= 127 and an fp16 d comes
+    back bit-exactly (and so does its linear)."""
+    d = np.float16(0.0009765625)          # 2^-10, exact in fp16
+    qv = RNG.integers(-127, 128, size=(16, 64))
+    qv[:, ::32] = 127                     # every block reaches the full range
+    w = qv * float(d)
+    q, dd = oracle.q8_0_quantize(w)
+    assert np.array_equal(q.astype(np.int64), qv) and (dd == d).all()
+    x = RNG.standard_normal((5, 64))
+    np.testing.assert_array_equal(oracle.linear_q8_0(x, q, dd), x @ w.T)
+
+
+def test_zero_block_and_rounding_direction():
+    w = np.zeros((2, 64))
+    w[1, 32:] = np.linspace(-1, 1, 32)
+    q, d = oracle.q8_0_quantize(w)
+    assert d[0, 0] == 0 and d[0, 1] == 0 and d[1, 0] == 0 and not q[0].any() and not q[1, :32].any()
+    # half away from zero: +-0.5 steps round outwards
+    d1 = np.float16(0.5)
+    w2 = np.full((1, 32), 0.25)
+    w2[0, 0] = 63.5                        # absmax -> d = 0.5; 0.25 / 0.5 = 0.5 -> 1
+    q2, dd2 = oracle.q8_0_quantize(w2)
+    assert dd2[0, 0] == d1 and q2[0, 1] == 1 and q2[0, 0] == 127
+    q3, _ = oracle.q8_0_quantize(-w2)
+    assert q3[0, 1] == -1
+
+
+def test_linear_matches_the_library_on_dequantized_weights():
+    """The quantized linear is torch's float64 linear on d * q (a library
+    routine on the dequantized weight)."""
+    w = RNG.standard_normal((40, 96)) * 0.02
+    b = RNG.standard_normal(40) * 0.02
+    x = RNG.standard_normal((7, 96))
+    q, d = oracle.q8_0_quantize(w)
+    ref = F.linear(torch.from_numpy(x), torch.from_numpy(oracle.q8_0_dequantize(q, d)),
+                   torch.from_numpy(b)).numpy()
+    np.testing.assert_allclose(oracle.linear_q8_0(x, q, d, b), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_rejects_widths_not_a_multiple_of_32():
+    with pytest.raises(ValueError):
+        oracle.q8_0_quantize(np.ones((2, 40)))
