@@ -23,3 +23,4 @@ from .block import (  # noqa: F401
 )
 from .model import model_forward  # noqa: F401
 from .quant import q8_0_quantize, q8_0_dequantize, linear_q8_0  # noqa: F401
+from .decode_step import block_decode_step  # noqa: F401
