@@ -100,3 +100,63 @@ def test_planted_mistake_is_caught(i, monkeypatch):
     monkeypatch.setattr(oracle, name, bad, raising=False)
     with pytest.raises((AssertionError, ValueError)):
         pin()
+
+
+# ---- the newer oracles (Q8_0 weights, the whole-block decode step): each
+# mistake is planted in its own module, so the prefill oracle that the
+# decode pin compares against stays the true one
+import oracle.decode_step as ods  # noqa: E402
+import oracle.quant as oq  # noqa: E402
+from tests import test_oracle_decode_step as tds  # noqa: E402
+from tests import test_oracle_quant as tq  # noqa: E402
+
+_Q8 = oq.q8_0_quantize
+
+
+def _q8_scale_over_128(w):
+    w = np.asarray(w, dtype=np.float64)
+    out_f, in_f = w.shape
+    blocks = w.reshape(out_f, in_f // 32, 32)
+    d = (np.abs(blocks).max(axis=-1) / 128.0).astype(np.float16)
+    df = d.astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(df[..., None] > 0, blocks / df[..., None], 0.0)
+    q = np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
+    return q.reshape(out_f, in_f), d
+
+
+def _q8_truncating(w):
+    q, d = _Q8(w)
+    w = np.asarray(w, dtype=np.float64)
+    df = np.repeat(d.astype(np.float64), 32, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(df > 0, w / df, 0.0)
+    return np.clip(np.trunc(r), -127, 127).astype(np.int8), d
+
+
+def _rope_at_next_position(xh, positions, rotary_span, base):
+    return ob.rope(xh, np.asarray(positions) + 1, rotary_span, base)
+
+
+def _attend_without_the_new_token(q, k_cache, v_cache, lens, scale=None, slopes=None):
+    return ob.attention_decode(q, k_cache, v_cache, np.asarray(lens) - 1, scale, slopes)
+
+
+_DECODE_PIN = lambda: tds.test_decode_step_equals_prefill_last_row("stablelm2")  # noqa: E731
+
+MODULE_MUTATIONS = [
+    (oq, "q8_0_quantize", _q8_scale_over_128, tq.test_error_bound_is_half_a_step_per_block),
+    (oq, "q8_0_quantize", _q8_truncating, tq.test_error_bound_is_half_a_step_per_block),
+    (ods, "rope", _rope_at_next_position, _DECODE_PIN),
+    (ods, "attention_decode", _attend_without_the_new_token, _DECODE_PIN),
+]
+
+
+@pytest.mark.parametrize("i", range(len(MODULE_MUTATIONS)))
+def test_planted_mistake_in_a_newer_oracle_is_caught(i, monkeypatch):
+    mod, name, bad, pin = MODULE_MUTATIONS[i]
+    monkeypatch.setattr(mod, name, bad)
+    if mod is oq:
+        monkeypatch.setattr(oracle, name, bad)
+    with pytest.raises((AssertionError, ValueError)):
+        pin()
