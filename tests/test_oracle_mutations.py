@@ -160,3 +160,19 @@ def test_planted_mistake_in_a_newer_oracle_is_caught(i, monkeypatch):
         monkeypatch.setattr(oracle, name, bad)
     with pytest.raises((AssertionError, ValueError)):
         pin()
+
+
+import oracle.model as om  # noqa: E402
+from tests import test_oracle_model as tm  # noqa: E402
+
+
+def _norm_skipped(x, gamma, beta, eps):
+    return np.asarray(x, dtype=np.float64)
+
+
+def test_model_oracle_without_its_norms_fails_its_pin(monkeypatch):
+    """Skipping the embedding / final LayerNorm in the model oracle fails the
+    pin against torch's float64 layer_norm and linear."""
+    monkeypatch.setattr(om, "layer_norm", _norm_skipped)
+    with pytest.raises(AssertionError):
+        tm.test_no_layers_is_norms_and_projection(True, "layernorm")
