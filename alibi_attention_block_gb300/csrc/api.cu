@@ -9,6 +9,8 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <set>
+#include <utility>
 #include <string>
 
 #include "blk.h"
@@ -143,6 +145,19 @@ blk_status current_device_info(int* sms, unsigned** err) {
     *sms = ds->sms;
     *err = ds->err;
     return BLK_OK;
+}
+
+cudaError_t set_smem_attr_once(const void* func, int smem_bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({func, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess) done.insert({func, dev});
+    return e;
 }
 
 blk_status report_error_status(blk_status st, const char* fmt, ...) {

@@ -461,12 +461,9 @@ cudaError_t launch_d(DType dt, const AttnArgs& a, cudaStream_t s) {
         !make_tmap_3d(&tv, dt, a.v, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kBKV))
         return cudaErrorInvalidValue;
     auto kern = attn_kernel<T, D, ALIBI>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    {
+        const cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     const int64_t items = static_cast<int64_t>((a.S + kBQ - 1) / kBQ) * a.B * a.H;
     if (items > 0x7fffffff) return cudaErrorInvalidValue;

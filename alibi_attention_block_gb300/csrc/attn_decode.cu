@@ -260,12 +260,10 @@ template <typename T, int D, int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
     const int64_t warps = static_cast<int64_t>(a.B) * a.Hk * a.parts;
     auto kern = decode_partial_kernel<T, D, G>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             DecCfg<D>::kSmem);
+    {
+        const cudaError_t e =
+            set_smem_attr_once(reinterpret_cast<const void*>(kern), DecCfg<D>::kSmem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     constexpr int kW = DecCfg<D>::kWarps;
     kern<<<static_cast<unsigned>((warps + kW - 1) / kW), 32 * kW, DecCfg<D>::kSmem, s>>>(a);

@@ -484,12 +484,9 @@ cudaError_t launch_pair128_t(DType dt, const AttnArgs& a, cudaStream_t s) {
         !make_tmap_3d(&tv, dt, a.v, static_cast<uint64_t>(a.B) * a.Hk, a.S, D, kTK))
         return cudaErrorInvalidValue;
     auto kern = attn_pair128_kernel<T, ALIBI>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    {
+        const cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     const int64_t nq = (a.S + kTQ - 1) / kTQ;
     const int64_t items = (nq + 1) / 2 * a.B * a.H;

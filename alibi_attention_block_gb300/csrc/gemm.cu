@@ -17,7 +17,7 @@
 // When the work units end in a partial round, the units of that round may
 // be split in two along K (long K only): each half publishes an fp32
 // partial tile and the half that finishes second sums both and runs the
-// epilogue (a separate kernel instance; see launch_cl).
+// epilogue (a separate kernel instance; see launch_cfg).
 // Epilogues (the block's steps after each projection):
 //   EPI_LINEAR  + bias, + up to two residuals (o_proj and down_proj residual
 //               adds); residuals and output may be fp32 (the block keeps its
@@ -260,13 +260,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
     }
 }
 
-// CL = 2: a cluster of two CTAs takes vertically adjacent tiles (2m, n) and
-// (2m+1, n), which share the B tile. Each CTA loads its own A tile and one
-// half of the B tile, multicast into both CTAs' shared memory, so B crosses
-// from L2 once per pair (a third less L2 traffic per stage). A stage is
-// refilled only after both CTAs' MMAs have released it: each MMA completion
-// arrives on the empty barrier of both CTAs (multicast commit).
-template <typename T, int BN, int EPI, int ROT, int CL, bool SPLIT>
+// Every CTA loads its own A and B tiles with plain (per-CTA) TMA loads.
+template <typename T, int BN, int EPI, int ROT, bool SPLIT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const GemmArgs g,
@@ -286,11 +281,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto tempty = [&](int i) { return bar0 + 8u * (2 * kStages + 2 + i); };
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
-    const int rank = CL == 2 ? static_cast<int>(cluster_ctarank()) : 0;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(full(i), 1);
-            mbar_init(empty(i), CL);
+            mbar_init(empty(i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull(i), 1);
@@ -306,22 +300,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    if constexpr (CL == 2)
-        cluster_sync();  // the peer's barriers exist before anything targets them
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int m_tiles = (g.M + kBM - 1) / kBM;
     const int n_tiles = (g.N + kBNOut - 1) / kBNOut;
-    // work units: single tiles, or vertical pairs of tiles for a cluster,
-    // numbered M-fastest (the CTAs running at any time share a few columns
-    // of B and all of A stays in L2) or, when A is too large to stay in L2,
-    // N-fastest (they share rows of A, read from DRAM once; B stays in L2)
-    const int m_units = (m_tiles + CL - 1) / CL;
+    // work units (output tiles), numbered M-fastest (the CTAs running at any
+    // time share a few columns of B and all of A stays in L2) or, when A is
+    // too large to stay in L2, N-fastest (they share rows of A, read from
+    // DRAM once; B stays in L2)
+    const int m_units = m_tiles;
     const int num_units = m_units * n_tiles;
-    const int unit0 = static_cast<int>(blockIdx.x) / CL;
-    const int unit_step = static_cast<int>(gridDim.x) / CL;
+    const int unit0 = static_cast<int>(blockIdx.x);
+    const int unit_step = static_cast<int>(gridDim.x);
     const int kb_count = (g.K + kBK - 1) / kBK;
     const int num_work =
         SPLIT ? g.split_base + (num_units - g.split_base) * g.split_s : num_units;
@@ -333,7 +324,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int v = unit0; v < num_work && ok; v += unit_step) {
                 const Unit un = decode_unit<SPLIT>(g, v, kb_count);
                 const int u = un.u;
-                const int mt = (g.n_fastest ? u / n_tiles : u % m_units) * CL + rank;
+                const int mt = g.n_fastest ? u / n_tiles : u % m_units;
                 const int nt = g.n_fastest ? u % n_tiles : u / m_units;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
                     if (!mbar_wait(empty(stage), phase ^ 1u, g.err)) {
@@ -344,15 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t sb = sa + Cfg::kABytes;
                     mbar_expect_tx(full(stage), Cfg::kStageBytes);
                     tma_load_2d(sa, &tmA, full(stage), kb * kBK, mt * kBM);
-                    if constexpr (CL == 2) {
-                        // this CTA's half of the B tile, into both CTAs
-                        if constexpr (EPI == EPI_SWIGLU)
-                            tma_load_2d_multicast(sb + rank * (BN / 2) * 128, rank ? &tmB2 : &tmB,
-                                                  full(stage), kb * kBK, nt * kBNOut, 0x3);
-                        else
-                            tma_load_2d_multicast(sb + rank * (BN / 2) * 128, &tmB, full(stage),
-                                                  kb * kBK, nt * BN + rank * (BN / 2), 0x3);
-                    } else if constexpr (EPI == EPI_SWIGLU) {
+                    if constexpr (EPI == EPI_SWIGLU) {
                         tma_load_2d(sb, &tmB, full(stage), kb * kBK, nt * kBNOut);
                         tma_load_2d(sb + (BN / 2) * 128, &tmB2, full(stage), kb * kBK, nt * kBNOut);
                     } else {
@@ -394,10 +377,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int k = 0; k < kBK / 16; ++k)
                         tc_mma_ss(d_tmem, ad + k * 2, bd + k * 2, idesc,
                                   (kb > un.kb0 || k != 0) ? 1u : 0u);
-                    if constexpr (CL == 2)
-                        tc_commit_multicast(empty(stage), 0x3);
-                    else
-                        tc_commit(empty(stage));
+                    tc_commit(empty(stage));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -422,7 +402,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!mbar_wait(tfull(acc), acc_phase, g.err)) break;
             tc_fence_after();
-            const int mt = (g.n_fastest ? u / n_tiles : u % m_units) * CL + rank;
+            const int mt = g.n_fastest ? u / n_tiles : u % m_units;
             const int nt = g.n_fastest ? u % n_tiles : u / m_units;
             const uint32_t tbase =
                 tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -434,8 +414,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 // count the warp in; the warp that arrives last for these
                 // rows sums every segment and runs the epilogue
                 const int t = (v - g.split_base) / g.split_s;
-                float* slot0 = g.split_ws + static_cast<size_t>((t * CL + rank) * g.split_s) *
-                                                (kBM * BN);
+                float* slot0 = g.split_ws + static_cast<size_t>(t * g.split_s) * (kBM * BN);
                 float* mine = slot0 + static_cast<size_t>(un.q) * (kBM * BN) + row;
 #pragma unroll 1
                 for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
@@ -447,7 +426,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 __threadfence();
                 __syncwarp();
-                cnt = g.split_cnt + ((t * CL + rank) * kEpiWarps + ew);
+                cnt = g.split_cnt + (t * kEpiWarps + ew);
                 unsigned old = 0;
                 if (lane == 0) old = atomicAdd(cnt, 1u);
                 old = __shfl_sync(0xffffffffu, old, 0);
@@ -469,63 +448,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (lane == 0) mbar_arrive(tempty(acc));
         }
     }
-    // every MMA of this CTA has completed (its epilogue consumed the last
-    // accumulator), so all its arrivals on the peer's barriers have landed
-    if constexpr (CL == 2)
-        cluster_sync();
-    else
-        __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
 }
 
-template <typename T, int BN, int EPI, int ROT, int CL>
-cudaError_t launch_cl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
-                      const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
+template <typename T, int BN, int EPI, int ROT = 0>
+cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                       const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
     using Cfg = GemmCfg<BN>;
     constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
     // the split instance exists only where a split is possible
     constexpr bool kCanSplit = EPI != EPI_SWIGLU;
-    auto kern = gemm_kernel<T, BN, EPI, ROT, CL, false>;
-    auto kern_split = gemm_kernel<T, BN, EPI, ROT, CL, kCanSplit>;
-    static bool attr_set = false;  // per template instance
-    static int max_clusters = 0;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg::kSmem);
-        if (e == cudaSuccess && kCanSplit)
-            e = cudaFuncSetAttribute(kern_split, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     Cfg::kSmem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::kSmem;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const int64_t m_units = ((g.M + kBM - 1) / kBM + CL - 1) / CL;
-    const int64_t units = m_units * ((g.N + kBNOut - 1) / kBNOut);
-    int64_t slots = num_sms / CL;
-    if (CL > 1) {
-        if (max_clusters == 0) {
-            cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CL * CL), 1, 1);
-            if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess ||
-                max_clusters <= 0)
-                max_clusters = num_sms / CL;
-        }
-        slots = max_clusters;
-    }
-    const int64_t grid_units = units < slots ? units : slots;
-    cfg.gridDim = dim3(static_cast<unsigned>(grid_units * CL), 1, 1);
+    auto kern = gemm_kernel<T, BN, EPI, ROT, false>;
+    auto kern_split = gemm_kernel<T, BN, EPI, ROT, kCanSplit>;
+    cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmem);
+    if (e == cudaSuccess && kCanSplit)
+        e = set_smem_attr_once(reinterpret_cast<const void*>(kern_split), Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t units = static_cast<int64_t>((g.M + kBM - 1) / kBM) * ((g.N + kBNOut - 1) / kBNOut);
+    const int64_t grid_units = units < num_sms ? units : num_sms;
+    const dim3 grid(static_cast<unsigned>(grid_units), 1, 1);
     // With scratch, split each unit of a last round that would leave at
     // least half of the CTAs idle (G units per round, R <= G/2 in the last)
     // into two halves along K, when each half still has at least
@@ -543,21 +488,15 @@ cudaError_t launch_cl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
         const int64_t sp = 2;
         const int64_t kb_count = (g.K + kBK - 1) / kBK;
         if (rounds >= 2 && R * sp <= G && kb_count >= sp * kSplitMinKb &&
-            R * CL * sp <= kGemmSplitSlots && R * CL * kEpiWarps <= kGemmSplitCounters) {
+            R * sp <= kGemmSplitSlots && R * kEpiWarps <= kGemmSplitCounters) {
             ga.split_s = static_cast<int>(sp);
             ga.split_base = static_cast<int>((rounds - 1) * G);
-            return cudaLaunchKernelEx(&cfg, kern_split, ta, tb, tb2, ga, rp);
+            kern_split<<<grid, kGemmThreads, Cfg::kSmem, s>>>(ta, tb, tb2, ga, rp);
+            return cudaGetLastError();
         }
     }
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, ga, rp);
-}
-
-template <typename T, int BN, int EPI, int ROT = 0>
-cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
-                       const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
-    if (g.M > kBM)
-        return launch_cl<T, BN, EPI, ROT, 2>(ta, tb, tb2, g, rp, num_sms, s);
-    return launch_cl<T, BN, EPI, ROT, 1>(ta, tb, tb2, g, rp, num_sms, s);
+    kern<<<grid, kGemmThreads, Cfg::kSmem, s>>>(ta, tb, tb2, ga, rp);
+    return cudaGetLastError();
 }
 
 template <typename T>
@@ -565,9 +504,8 @@ cudaError_t launch_t(DType dt, int epi, const void* a, const void* b, const void
                      const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
     constexpr int BN = 256;
     CUtensorMap ta, tb, tb2;
-    // the B box is half a tile whenever the pair of CTAs splits the B tile
-    // (M > 128) or the tile stacks gate and up rows (SWIGLU)
-    const uint32_t b_box = (epi == EPI_SWIGLU || g.M > kBM) ? BN / 2 : BN;
+    // the B box is half a tile when the tile stacks gate and up rows (SWIGLU)
+    const uint32_t b_box = epi == EPI_SWIGLU ? BN / 2 : BN;
     if (!make_tmap_2d(&ta, dt, a, g.M, g.K, kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_2d(&tb, dt, b, g.N, g.K, b_box)) return cudaErrorInvalidValue;
     tb2 = tb;

@@ -122,6 +122,10 @@ int decode_parts_max(int64_t S_max);
 // ---- per-device state and error reporting shared with other entry points (api.cu)
 // SM count and device error word of the current device (set up on first use).
 blk_status current_device_info(int* sms, unsigned** err);
+// Set a kernel's maximum dynamic shared memory on the current device, once
+// per (kernel, device): the attribute belongs to the device's context, so a
+// process that drives several GPUs sets it on each. Thread-safe.
+cudaError_t set_smem_attr_once(const void* func, int smem_bytes);
 // Record a printf-style message for blk_last_error() and return `st`.
 blk_status report_error_status(blk_status st, const char* fmt, ...);
 

@@ -479,11 +479,8 @@ template <typename T, int D, int NU>
 void launch_unit(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s, int64_t warps) {
     using Cfg = UnitCfg<NU>;
     auto kern = qk_unit_kernel<T, D, NU>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
-        attr_set = true;
-    }
+    // a failure here stays the runtime's last error, which the caller returns
+    if (set_smem_attr_once(reinterpret_cast<const void*>(kern), Cfg::kSmem) != cudaSuccess) return;
     // persistent: as many 4-warp blocks as fit (shared memory bound) on every SM
     const int per_sm = (200 * 1024) / Cfg::kSmem > 0 ? (200 * 1024) / Cfg::kSmem : 1;
     int64_t blocks = (warps + 3) / 4;

@@ -39,15 +39,23 @@ def test_links_no_vendor_math_library(lib):
         assert bad not in out.lower(), out
 
 
-def test_sources_use_only_tcgen05_and_local_memory():
+def test_sources_use_only_tcgen05_and_no_multicast():
     """Tensor-core work goes through tcgen05 (no legacy mma.sync / wmma, no
-    Hopper wgmma); multicast is only within a CTA cluster on this GPU (TMA
-    loads and MMA-completion arrivals), never NVLink multimem."""
-    csrc = os.path.join(os.path.dirname(_abi.HERE), "alibi_attention_block_gb300", "csrc")
-    for f in os.listdir(csrc):
-        text = open(os.path.join(csrc, f)).read()
-        assert "wgmma" not in text and "mma.sync" not in text and "wmma" not in text, f
-        assert "multimem" not in text, f
+    Hopper wgmma). No kernel issues a multicast of any kind: every TMA load
+    and every MMA-completion arrival targets the issuing CTA's own shared
+    memory, and nothing uses NVLink multimem, so the same library is safe to
+    run as independent replicas on several GPUs."""
+    root = os.path.dirname(_abi.HERE)
+    dirs = [os.path.join(root, "alibi_attention_block_gb300", "csrc"), os.path.join(root, "include")]
+    seen = 0
+    for d in dirs:
+        for f in os.listdir(d):
+            text = open(os.path.join(d, f)).read()
+            seen += 1
+            assert "wgmma" not in text and "mma.sync" not in text and "wmma" not in text, f
+            assert "multicast" not in text.lower(), f
+            assert "multimem" not in text, f
+    assert seen >= 10
 
 
 def test_status_strings_and_version(lib):
