@@ -134,6 +134,20 @@ def _q8_truncating(w):
     return np.clip(np.trunc(r), -127, 127).astype(np.int8), d
 
 
+def _q8_divides_by_fp16_scale(w):
+    """The order the GGML format does not use: the scale rounded to fp16
+    first, the codes divided by it (and clipped)."""
+    w = np.asarray(w, dtype=np.float64)
+    out_f, in_f = w.shape
+    blocks = w.reshape(out_f, in_f // 32, 32)
+    d = (np.abs(blocks).max(axis=-1) / 127.0).astype(np.float16)
+    df = d.astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(df[..., None] > 0, blocks / df[..., None], 0.0)
+    q = np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
+    return q.reshape(out_f, in_f), d
+
+
 def _rope_at_next_position(xh, positions, rotary_span, base):
     return ob.rope(xh, np.asarray(positions) + 1, rotary_span, base)
 
@@ -147,6 +161,8 @@ _DECODE_PIN = lambda: tds.test_decode_step_equals_prefill_last_row("stablelm2") 
 MODULE_MUTATIONS = [
     (oq, "q8_0_quantize", _q8_scale_over_128, tq.test_error_bound_is_half_a_step_per_block),
     (oq, "q8_0_quantize", _q8_truncating, tq.test_error_bound_is_half_a_step_per_block),
+    (oq, "q8_0_quantize", _q8_divides_by_fp16_scale,
+     tq.test_codes_are_rounded_against_the_float32_scale_not_the_fp16_one),
     (ods, "rope", _rope_at_next_position, _DECODE_PIN),
     (ods, "attention_decode", _attend_without_the_new_token, _DECODE_PIN),
 ]

@@ -10,15 +10,55 @@ RNG = np.random.Generator(np.random.PCG64(77))
 
 
 def test_error_bound_is_half_a_step_per_block():
-    """|w - d q| <= d / 2 everywhere (round to nearest), and the block's
-    largest |w| maps to |q| = 127 (up to the fp16 rounding of d)."""
+    """|w - d q| <= D / 2 + 127 |D - d| everywhere, with D = absmax / 127 the
+    exact scale the codes are rounded against and d its stored fp16 value;
+    the block's largest |w| maps to |q| = 127."""
     w = RNG.standard_normal((48, 256)) * 0.02
+    w = w.astype(np.float32).astype(np.float64)
     q, d = oracle.q8_0_quantize(w)
     err = np.abs(w - oracle.q8_0_dequantize(q, d)).reshape(48, 8, 32)
+    exact = np.abs(w.reshape(48, 8, 32)).max(axis=-1) / 127.0
     df = d.astype(np.float64)
-    assert (err <= df[..., None] / 2 * (1 + 1e-3) + 1e-12).all()
+    # the stored scale is absmax / 127 to fp16 precision (11 significant bits)
+    assert (np.abs(df - exact) <= exact * 2.0 ** -11).all()
+    bound = exact / 2 * (1 + 1e-5) + 127 * np.abs(exact - df)
+    assert (err <= bound[..., None] + 1e-12).all()
     top = np.abs(q.reshape(48, 8, 32)).max(axis=-1)
-    assert ((top >= 126) & (top <= 127)).all()
+    assert (top == 127).all()
+
+
+def test_codes_are_rounded_against_the_float32_scale_not_the_fp16_one():
+    """GGML's order: codes from w * (1 / (absmax / 127)) before the scale is
+    rounded to fp16. With absmax = 1 the exact code of w is round(127 w); a
+    weight at 63.497 / 127 lies 0.003 below the half-step, far outside
+    float32 rounding, so its code is 63. Dividing by the stored fp16 scale
+    instead (1032 * 2^-17, 6e-5 below 1/127) would push it over 63.5 to 64.
+    Every code of a random block is checked against exact rational
+    arithmetic wherever that exact value is not within 1e-4 of a half-step."""
+    from fractions import Fraction
+
+    w = np.zeros((1, 32), dtype=np.float32)
+    w[0, 0] = 1.0
+    w[0, 1] = np.float32(63.497 / 127)
+    w[0, 2] = -np.float32(63.497 / 127)
+    q, d = oracle.q8_0_quantize(w)
+    assert float(d[0, 0]) == 1032 * 2.0 ** -17
+    assert q[0, 0] == 127 and q[0, 1] == 63 and q[0, 2] == -63
+
+    blocks = (RNG.standard_normal((64, 32)) * 0.02).astype(np.float32)
+    qb, _ = oracle.q8_0_quantize(blocks)
+    checked = 0
+    for row in range(64):
+        amax = max(Fraction(float(abs(v))) for v in blocks[row])
+        for j in range(32):
+            r = Fraction(float(blocks[row, j])) * 127 / amax
+            frac = abs(r) - int(abs(r))
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 10000):
+                continue
+            expect = int(abs(r) + Fraction(1, 2)) * (1 if r >= 0 else -1)
+            assert int(qb[row, j]) == expect, (row, j, float(r))
+            checked += 1
+    assert checked > 2000
 
 
 def test_exact_round_trip_of_representable_weights():
