@@ -24,7 +24,8 @@ std::mutex g_scratch_mu;
 
 // Device address of g_mlp_scratch on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device with that device current.
+// per device with that device current, and kept: a device reset in this
+// process (cudaDeviceReset) would leave it stale, which the header forbids.
 blk_status scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

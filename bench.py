@@ -38,18 +38,15 @@ METRIC = "prefill tokens/s per block and attention TFLOP/s (% of GB300 FP16 peak
 
 
 # DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum, one
-# capture of the default workload) for the kernels that can be the roofline's
-# dominant one, with the SHA-256 of the sources the kernel was built from when
-# the counters were taken: a kernel changed since then reports null.
+# capture of the workload) for the kernels that can be a workload's dominant
+# one, with the SHA-256 of the sources the kernel was built from when the
+# counters were taken: a kernel changed since then reports null. Keyed by
+# (workload, block step).
 _KERNEL_SOURCES = {
     "gemm": ("alibi_attention_block_gb300/csrc/gemm.cu", "alibi_attention_block_gb300/csrc/common.cuh",
              "alibi_attention_block_gb300/csrc/internal.h"),
 }
-NCU_TRAFFIC = {
-    # profiles/gemm_gate_up_and_down_stablelm2_1p6b.md: 81.82 MB read + 62.91 MB written
-    "mlp_up": {"kind": "gemm", "bytes": 144739072,
-               "sha256": "b3f47797dba85fa5894489f4f83b76662c7f9fcec3fbdec482abb90ae6993f2e"},
-}
+NCU_TRAFFIC = {}
 
 
 def _sources_sha(kind: str) -> str:
@@ -68,8 +65,8 @@ def _sources_sha(kind: str) -> str:
     return h.hexdigest()
 
 
-def _traffic(step: str):
-    ent = NCU_TRAFFIC.get(step)
+def _traffic(cfg, step: str):
+    ent = NCU_TRAFFIC.get((cfg.name, step))
     if not ent or _sources_sha(ent["kind"]) != ent["sha256"]:
         return None
     return ent["bytes"]
@@ -81,8 +78,9 @@ def _peaks():
         d = json.load(open(p))
         return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
                     bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
-                    source="measured")
-    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+                    sm_max_mhz=d.get("sm_max_mhz"), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                sm_max_mhz=2070.0, source="fallback")
 
 
 def _max_over_ranks(dist, ms: float, device) -> float:
@@ -132,17 +130,64 @@ def step_work(cfg):
 
 
 # ------------------------------------------------------------------ clocks --
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (SM clock,
+    its maximum, power, active clock-event reasons) for one GPU, selected by
+    UUID. None of these calls changes any setting."""
+
+    def __init__(self, device_index: int):
+        import ctypes as C
+        self.C = C
+        self.lib = C.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        self.h = C.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), C.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + uuid)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_sm = self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn):
+        v = self.C.c_uint(0)
+        return float(v.value) if fn(self.h, 1, self.C.byref(v)) == 0 else None  # 1: SM clock
+
+    def sample(self):
+        C = self.C
+        mw, rs = C.c_uint(0), C.c_ulonglong(0)
+        power = mw.value / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.h, C.byref(mw)) == 0 else None
+        bits = rs.value if self.reasons_fn(self.h, C.byref(rs)) == 0 else 0
+        return (time.time(), self._clock(self.lib.nvmlDeviceGetClockInfo), self.max_sm, power,
+                [n for m, n in _NVML_REASONS.items() if bits & m])
+
+
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms; only samples whose timestamps fall
-    inside the timed region (mark_start / mark_end) are summarised."""
+    """SM clock, power and clock-event reasons sampled every millisecond
+    through NVML in a background thread (nvidia-smi every 50 ms where NVML
+    cannot be loaded); only samples whose timestamps fall inside the timed
+    region (mark_start / mark_end) are summarised, so a timed region of a few
+    milliseconds still gets samples."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
-        self.proc = None
+        self.proc = self.thread = None
         self.t0 = self.t1 = None
+        self.samples = []
+        self.source = "nvml"
+        try:
+            self.nvml = _Nvml(device_index)
+        except Exception:  # noqa: BLE001
+            self.nvml = None
+            self.source = "nvidia-smi"
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -152,7 +197,22 @@ class ClockSampler:
         self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                     "-lms", "50", *sel]
 
+    def _loop(self):
+        while not self.stop:
+            try:
+                self.samples.append(self.nvml.sample())
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(0.001)
+
     def __enter__(self):
+        if self.nvml is not None:
+            import threading
+            self.stop = False
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+            time.sleep(0.05)
+            return self
         try:
             self.proc = subprocess.Popen(self.cmd, stdout=self.out, stderr=subprocess.DEVNULL)
         except OSError:
@@ -167,6 +227,9 @@ class ClockSampler:
         self.t1 = time.time()
 
     def __exit__(self, *a):
+        if self.thread is not None:
+            self.stop = True
+            self.thread.join(timeout=5)
         if self.proc:
             self.proc.terminate()
             try:
@@ -184,16 +247,30 @@ class ClockSampler:
                 pass
         return None
 
-    def summary(self):
-        self.out.flush()
+    def _rows(self):
+        """(sm_mhz, sm_max_mhz, power_w, [active reasons]) inside the region,
+        and the count of samples outside it."""
         rows, outside = [], 0
+        if self.nvml is not None:
+            for t, sm, mx, pw, rs in self.samples:
+                if sm is None:
+                    continue
+                if self.t0 is not None and not (self.t0 <= t <= self.t1):
+                    outside += 1
+                    continue
+                rows.append((sm, mx, pw, rs))
+            os.unlink(self.out.name)
+            return rows, outside
+        self.out.flush()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in open(self.out.name):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) != 8:
                 continue
             t = self._epoch(parts[0])
             try:
-                row = (float(parts[1]), float(parts[2]), float(parts[3]), parts[4:])
+                row = (float(parts[1]), float(parts[2]), float(parts[3]),
+                       [names[i] for i, v in enumerate(parts[4:]) if v.lower() == "active"])
             except ValueError:
                 continue
             if t is not None and self.t0 is not None and not (self.t0 <= t <= self.t1):
@@ -201,13 +278,21 @@ class ClockSampler:
                 continue
             rows.append(row)
         os.unlink(self.out.name)
+        return rows, outside
+
+    def summary(self):
+        rows, outside = self._rows()
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({names[i] for *_, r in rows for i, v in enumerate(r) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w": statistics.median(r[2] for r in rows), "reasons": reasons,
-                "samples": len(rows), "samples_outside_timed_region": outside}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({n for *_, rs in rows for n in rs})
+        powers = [r[2] for r in rows if r[2] is not None]
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows if r[1] is not None) if any(
+                    r[1] is not None for r in rows) else None,
+                "power_w": statistics.median(powers) if powers else None, "reasons": reasons,
+                "samples": len(rows), "samples_outside_timed_region": outside,
+                "source": self.source}
 
 
 # ------------------------------------------------------- standalone kernels --
@@ -502,46 +587,65 @@ def _config(cfg, l2):
 
 
 # -------------------------------------------------------------------- ours --
-def run_ours(args, cfg, rank, world, local_rank, dist):
-    import ctypes as C
+# Per-SM dense bf16/fp16 rate of tcgen05: one M=128, N=256, K=16 MMA
+# (2*128*256*16 flops) per 128 clocks; a microbenchmark of back-to-back
+# instructions measured 129 clocks.
+TC_FLOP_PER_CLK_SM = 8192
 
-    import __graft_entry__
-    __graft_entry__.build()
+
+def _spec_peak(dev, peaks) -> dict:
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = peaks.get("sm_max_mhz") or 2070.0
+    tf = sms * TC_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12
+    return {"tflops": tf, "derivation": f"{sms} SMs x {TC_FLOP_PER_CLK_SM} flop/clk/SM x {mhz:.0f} MHz"}
+
+
+class _Block:
+    """One workload's inputs, weights and workspace on the device, and the
+    ctypes arguments of blk_forward_ex."""
+
+    def __init__(self, cfg, dev, lib):
+        import ctypes as C
+
+        import alibi_attention_block_gb300 as blk
+        from alibi_attention_block_gb300 import _abi
+        self.cfg, self.lib, self.C, self._abi = cfg, lib, C, _abi
+        self.x_cpu, self.w_cpu = workloads.block_inputs(cfg)
+        self.x = self.x_cpu.to(dev)
+        self.wd = {k: t.to(dev) for k, t in self.w_cpu.items()}
+        self.y = torch.empty_like(self.x)
+        self.ws_bytes = blk.forward_workspace_size(cfg, cfg.batch, cfg.seq)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.desc = blk.block_desc(cfg, cfg.batch, cfg.seq)
+        self.wstruct = _abi.BlockWeights(*[(self.wd[n].data_ptr() if n in self.wd else None)
+                                           for n in _abi.WEIGHT_SLOTS])
+        self.dt = _abi.BLK_F16 if cfg.dtype == "fp16" else _abi.BLK_BF16
+        self.max_ev = 11
+        self.kinds = (C.c_int32 * 10)()
+        self.nl = C.c_int(0)
+
+    def step(self, stream, events):
+        C = self.C
+        arr = (C.c_void_p * self.max_ev)(*[e.cuda_event for e in events]) if events else None
+        self._abi.check(self.lib.blk_forward_ex(
+            C.byref(self.desc), C.byref(self.wstruct), C.c_void_p(self.x.data_ptr()),
+            C.c_void_p(self.y.data_ptr()), C.c_void_p(self.ws.data_ptr()), self.ws_bytes, self.dt,
+            C.c_void_p(stream.cuda_stream), arr, self.max_ev if events else 0, self.kinds,
+            C.byref(self.nl)), "blk_forward_ex")
+
+
+def _time_steps(bl, args, flush, stream, dist, sampler_index, steps, warmup):
+    """W warm-up and K timed forwards of one workload, L2 flushed before each,
+    with per-launch CUDA events recorded by the library on the launching
+    stream. Returns the per-kernel means, the per-step times and the clocks."""
     import alibi_attention_block_gb300 as blk
     from alibi_attention_block_gb300 import _abi
-
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    lib = _abi.load()
-    x_cpu, w_cpu = workloads.block_inputs(cfg)
-    x = x_cpu.to(dev)
-    wd = {k: t.to(dev) for k, t in w_cpu.items()}
-    y = torch.empty_like(x)
-    ws_bytes = blk.forward_workspace_size(cfg, cfg.batch, cfg.seq)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    desc = blk.block_desc(cfg, cfg.batch, cfg.seq)
-    wstruct = _abi.BlockWeights(*[(wd[n].data_ptr() if n in wd else None) for n in _abi.WEIGHT_SLOTS])
-    dt = _abi.BLK_F16 if cfg.dtype == "fp16" else _abi.BLK_BF16
-    stream = torch.cuda.current_stream()
-    max_ev = 11
-    kinds = (C.c_int32 * 10)()
-    nl = C.c_int(0)
-
-    def one_step(events):
-        arr = (C.c_void_p * max_ev)(*[e.cuda_event for e in events]) if events else None
-        _abi.check(lib.blk_forward_ex(C.byref(desc), C.byref(wstruct), C.c_void_p(x.data_ptr()),
-                                      C.c_void_p(y.data_ptr()), C.c_void_p(ws.data_ptr()), ws_bytes,
-                                      dt, C.c_void_p(stream.cuda_stream), arr,
-                                      max_ev if events else 0, kinds, C.byref(nl)),
-                   "blk_forward_ex")
-
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
-        one_step(None)
+        bl.step(stream, None)
     torch.cuda.synchronize()
     blk.check_device_status()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(max_ev)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(bl.max_ev)] for _ in range(steps)]
     for row in evs:          # torch creates the CUDA event on its first record
         for e in row:
             e.record(stream)
@@ -550,7 +654,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
     if args.launch == "graph":
         # the block's launches recorded once as a CUDA graph; every timed step
         # replays it with its own events (blk_graph_set_events)
-        graph = blk.ForwardGraph(cfg, wd, x, y, ws, events=evs[0])
+        graph = blk.ForwardGraph(bl.cfg, bl.wd, bl.x, bl.y, bl.ws, events=evs[0])
         for _ in range(3):
             flush.zero_()
             graph.launch()
@@ -559,36 +663,108 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         n_launch = graph.n_launches.value
         step_names = [_abi.STEP_NAMES[graph.kinds[i]] for i in range(n_launch)]
     else:
-        n_launch = nl.value
-        step_names = [_abi.STEP_NAMES[kinds[i]] for i in range(n_launch)]
-
+        n_launch = bl.nl.value
+        step_names = [_abi.STEP_NAMES[bl.kinds[i]] for i in range(n_launch)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(sampler_index) as clk:
         clk.mark_start()
         t_wall = time.perf_counter()
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()
             if graph is not None:
                 graph.launch(evs[i])
             else:
-                one_step(evs[i])
+                bl.step(stream, evs[i])
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
         clk.mark_end()
     if dist:
         dist.barrier()
     blk.check_device_status()
-    clocks = clk.summary()
-
     step_ms = [e[0].elapsed_time(e[n_launch]) for e in evs]
     per_kind = {}
     for e in evs:
         for j, name in enumerate(step_names):
             per_kind.setdefault(name, []).append(e[j].elapsed_time(e[j + 1]))
     kernel_ms = {k: float(np.mean(v)) for k, v in per_kind.items()}
-    total_ms = _max_over_ranks(dist, float(sum(step_ms)), dev)
+    return dict(kernel_ms=kernel_ms, step_ms=step_ms, n_launch=n_launch, t_wall=t_wall,
+                clocks=clk.summary(), graph=graph is not None)
+
+
+def _report(cfg, kernel_ms, ms_per_step, timed_s, peaks, spec):
+    """Per-kernel rates, attention against the peaks, and the roofline of the
+    dominant kernel. A kernel timed inside a timed region shorter than a
+    second is held to the measured burst bf16 peak; inside a longer one, to
+    the sustained (power-capped) peak."""
+    work = step_work(cfg)
+    burst = timed_s < 1.0
+    tpeak = peaks["bf16_tflops"] if burst else peaks["bf16_tflops_sustained"]
+    tsrc = (peaks["source"] + (" burst bf16 (timed region %.3f s < 1 s)" if burst else
+                               " sustained bf16 (timed region %.3f s >= 1 s)") % timed_s)
+    dom = max(kernel_ms, key=kernel_ms.get)
+    dw = work[dom]
+    if dw["flops"]:
+        achieved = dw["flops"] / (kernel_ms[dom] / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tpeak,
+                "unit": "TFLOP/s", "frac": achieved / tpeak, "traffic": _traffic(cfg, dom),
+                "peak_source": tsrc, "algorithmic_flops_per_launch": dw["flops"],
+                "frac_of_spec_peak": achieved / spec["tflops"]}
+    else:
+        achieved = dw["bytes"] / (kernel_ms[dom] / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(cfg, dom),
+                "peak_source": peaks["source"] + " copy", "algorithmic_bytes_per_launch": dw["bytes"]}
+    kernels = {}
+    for k, ms in kernel_ms.items():
+        w_ = work[k]
+        ent = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4)}
+        if w_["flops"]:
+            tf = w_["flops"] / (ms / 1e3) / 1e12
+            ent["tflops"] = round(tf, 1)
+            ent["frac_of_peak"] = round(tf / tpeak, 4)
+        else:
+            gbs = w_["bytes"] / (ms / 1e3) / 1e9
+            ent["gbs"] = round(gbs, 1)
+            ent["frac_of_measured_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
+        kernels[k] = ent
+    attn = None
+    if "attention" in kernel_ms:
+        at = work["attention"]["flops"] / (kernel_ms["attention"] / 1e3) / 1e12
+        attn = {"tflops": at, "frac_of_measured_bf16_peak": at / peaks["bf16_tflops"],
+                "frac_of_spec_peak": at / spec["tflops"]}
+    block_tf = sum(work[k]["flops"] for k in kernel_ms) / (ms_per_step / 1e3) / 1e12
+    return dict(kernels=kernels, attention=attn, roofline=roof, block_tflops=block_tf)
+
+
+def _cpu_baseline(cfg, budget_s):
+    v, n_tok, secs, sample = time_oracle(cfg, budget_s=budget_s)
+    return {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{sample} ({secs:.1f} s, fp64 NumPy)"}
+
+
+# the other block workloads reported beside the headline one, each in the
+# same launch configuration and timing
+EXTRA_CONFIGS = ("bloom_560m", "olmo2_1b", "stablelm2_12b")
+
+
+def run_ours(args, cfg, rank, world, local_rank, dist):
+    import __graft_entry__
+    __graft_entry__.build()
+    import alibi_attention_block_gb300 as blk
+    from alibi_attention_block_gb300 import _abi
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = _abi.load()
+    bl = _Block(cfg, dev, lib)
+    x, y, wd, x_cpu, w_cpu = bl.x, bl.y, bl.wd, bl.x_cpu, bl.w_cpu
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    r = _time_steps(bl, args, flush, stream, dist, local_rank, args.steps, args.warmup)
+    kernel_ms, n_launch, t_wall, clocks = r["kernel_ms"], r["n_launch"], r["t_wall"], r["clocks"]
+    total_ms = _max_over_ranks(dist, float(sum(r["step_ms"])), dev)
     ms_per_step = total_ms / args.steps
     value = _job_throughput(world, cfg.tokens, args.steps, total_ms)
 
@@ -597,11 +773,11 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
     # copy out step n+1's; the flush after the last step is inside the timed
     # region) or blk_forward_host (copies overlapped over groups of sequences
     # within one step)
+    ws, ws_bytes = bl.ws, bl.ws_bytes
     x_host = x_cpu.pin_memory()
     y_host = torch.empty_like(x_host).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.e2e_api == "pipe":
-        del ws  # the pipe holds its own staging slots and workspace
         pipe = blk.HostPipe(cfg, cfg.batch, cfg.seq, dtype=x.dtype, depth=2)
 
         def e2e_step():
@@ -633,62 +809,59 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, dev)
+    if args.e2e_api == "pipe":
+        pipe.close()
 
     standalone = standalone_hbm(blk, dev) if rank == 0 else None
     if rank != 0:
         return
     peaks = _peaks()
+    spec = _spec_peak(dev, peaks)
     for v in standalone.values():
         v["frac_of_measured_hbm"] = v["gbs"] / peaks["hbm_gbs"]
-    work = step_work(cfg)
-    dom = max(kernel_ms, key=kernel_ms.get)
-    dw = work[dom]
-    if dw["flops"]:
-        achieved = dw["flops"] / (kernel_ms[dom] / 1e3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"],
-                "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "traffic": _traffic(dom),
-                "peak_source": peaks["source"] + " sustained bf16"}
-    else:
-        achieved = dw["bytes"] / (kernel_ms[dom] / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(dom),
-                "peak_source": peaks["source"] + " copy"}
-    kernels = {}
-    for k, ms in kernel_ms.items():
-        w_ = work[k]
-        ent = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4)}
-        if w_["flops"]:
-            ent["tflops"] = round(w_["flops"] / (ms / 1e3) / 1e12, 1)
-        else:
-            ent["gbs"] = round(w_["bytes"] / (ms / 1e3) / 1e9, 1)
-        kernels[k] = ent
-    attn = None
-    if "attention" in kernel_ms:
-        at = work["attention"]["flops"] / (kernel_ms["attention"] / 1e3) / 1e12
-        attn = {"tflops": at, "frac_of_measured_bf16_peak": at / peaks["bf16_tflops"],
-                "frac_of_nominal_2250": at / 2250.0}
-    cpu = None
-    if not args.no_cpu_baseline:
-        v, n_tok, secs, sample = time_oracle(cfg, budget_s=args.cpu_budget)
-        cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{sample} ({secs:.1f} s, fp64 NumPy)"}
+    rep = _report(cfg, kernel_ms, ms_per_step, sum(r["step_ms"]) / 1e3, peaks, spec)
+    cpu = None if args.no_cpu_baseline else _cpu_baseline(cfg, args.cpu_budget)
+    provenance = _safe_provenance(cfg, x_cpu, w_cpu, dev)
+    e2e_bytes_in, e2e_bytes_out = x.numel() * x.element_size(), y.numel() * y.element_size()
+    del bl, x, y, wd, ws, x_host, y_host
+    torch.cuda.empty_cache()
+
+    # the other block workloads, one after another in the same launch
+    # configuration (L2 flushed before every step, K timed steps after W
+    # warm-up ones); each with its own oracle baseline on the host cores
+    others = {}
+    if not args.no_extra_configs and cfg.name == "stablelm2_1p6b":
+        for name in EXTRA_CONFIGS:
+            c = workloads.BLOCK_CONFIGS[name]
+            b2 = _Block(c, dev, lib)
+            r2 = _time_steps(b2, args, flush, stream, None, local_rank, args.steps, args.warmup)
+            ms2 = float(sum(r2["step_ms"])) / args.steps
+            rep2 = _report(c, r2["kernel_ms"], ms2, sum(r2["step_ms"]) / 1e3, peaks, spec)
+            others[name] = {
+                "config": _config(c, "flushed before every step (512 MiB write)"),
+                "tokens_per_s": c.tokens / (ms2 / 1e3), "ms_per_step": ms2,
+                "dtype": c.dtype, **rep2,
+                "cpu_baseline": None if args.no_cpu_baseline else _cpu_baseline(c, args.cpu_budget / 2),
+                "gpu_launches": r2["n_launch"] * args.steps, "clocks": r2["clocks"]}
+            del b2
+            torch.cuda.empty_cache()
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) inputs, N(0,0.02) weights)",
         "config": dict(_config(cfg, "flushed before every step (512 MiB write)"),
-                       launch="CUDA graph replay" if graph is not None else "direct launches"),
-        "block_tflops": sum(work[k]["flops"] for k in kernel_ms) / (ms_per_step / 1e3) / 1e12,
-        "attention": attn,
-        "kernels": kernels,
-        "roofline": roof,
+                       launch="CUDA graph replay" if r["graph"] else "direct launches"),
+        "block_tflops": rep["block_tflops"],
+        "attention": rep["attention"],
+        "kernels": rep["kernels"],
+        "roofline": rep["roofline"],
+        "spec_peak": spec,
         "cpu_baseline": cpu,
         "e2e": {"value": world * cfg.tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": y.numel() * y.element_size(),
+                "h2d_bytes_per_step": e2e_bytes_in,
+                "d2h_bytes_per_step": e2e_bytes_out,
                 "ms_per_step": e2e_ms,
                 "l2": ("not flushed between steps: a step moves %.2f GB of distinct buffers "
                        "(staging, workspace, weights), %.1fx L2; the device-timed leg writes "
@@ -700,10 +873,11 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
                    {"api": "blk_forward_host (pinned host buffers)",
                     "n_chunks": args.e2e_chunks})},
         "hbm_kernels_standalone": standalone,
+        "other_configs": others,
         "gpu_launches": n_launch * args.steps,
         "clocks": clocks,
         "wall_s_timed": t_wall,
-        "provenance": _safe_provenance(cfg, x_cpu, w_cpu, dev),
+        "provenance": provenance,
     }
     print(json.dumps(line), flush=True)
 
@@ -717,6 +891,8 @@ def main():
     ap.add_argument("--config", default="stablelm2_1p6b", choices=sorted(workloads.BLOCK_CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="report the headline workload only (skip Bloom-560m, OLMo-2-1B, 12B)")
     ap.add_argument("--launch", choices=["direct", "graph"], default="direct",
                     help="timed steps launch the block directly (default), or replay it as a "
                          "CUDA graph; the per-kernel events inside a graph cost more than the "

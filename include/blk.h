@@ -228,7 +228,10 @@ blk_status blk_mlp(const blk_mlp_desc* d, const void* x, const void* w_gate, con
  * fit in it; larger requests return BLK_EWORKSPACE and launch nothing. The
  * call allocates and frees nothing. Its first call on a device looks up the
  * array's device address (cudaGetSymbolAddress), so make that first call
- * before any stream capture. All calls share the one array: calls whose
+ * before any stream capture. That address is kept for the life of the
+ * process: after a cudaDeviceReset (or any reset of the device's primary
+ * context) it is stale, so do not call blk_mlp_noalloc on a device that the
+ * process has reset. All calls share the one array: calls whose
  * kernels overlap on the GPU (other streams, other host threads) race on it.
  * Every element the MLP reads from it is written first in the same call, so
  * nothing has to be cleared between calls. Arguments, results and errors are

@@ -39,3 +39,40 @@ def post_norm_block_with_storage_rounding(cfg, x, w):
     a = _round(oracle.silu(oracle.linear(h16, W["w_gate"])) * oracle.linear(h16, W["w_up"]), dt)
     y = h + oracle.rms_norm(oracle.linear(a, W["w_down"]), W["post_mlp_norm_w"], cfg.eps)
     return _round(y, dt)
+
+
+def post_norm_block_from_stored_qkv(cfg, x, w, q, k, v, rows=None):
+    """y of the reordered post-norm block continued, in float64, from the
+    head-split q, k, v a kernel stored (after qk-norm and rotary, in the
+    storage dtype), with the block's remaining storage roundings: the
+    attention output, the bf16 copy of h that feeds the MLP, the MLP
+    activation and y. ``rows`` (optional): flat token indices into B*S, for
+    which alone the attention and everything after it are evaluated. No
+    rounding decision here depends on a softmax near-tie resolved
+    differently from the kernel, because q and k are the kernel's own."""
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float16
+    W = {kk: as_f64(t) for kk, t in w.items()}
+    X = as_f64(x)
+    B, S, D = X.shape
+    H, d = cfg.n_heads, cfg.head_dim
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    if rows is None:
+        o = oracle.merge_heads(oracle.attention(q, k, v)).reshape(B * S, H * d)
+        xs = X.reshape(B * S, D)
+    else:
+        rows = np.asarray(rows)
+        o = np.empty((len(rows), H * d))
+        for b in range(B):
+            mine = np.nonzero(rows // S == b)[0]
+            if len(mine) == 0:
+                continue
+            qi = rows[mine] % S
+            ob = oracle.attention(q[b:b + 1, :, qi], k[b:b + 1], v[b:b + 1], q_positions=qi)
+            o[mine] = ob[0].transpose(1, 0, 2).reshape(len(mine), H * d)
+        xs = X.reshape(B * S, D)[rows]
+    o = _round(o, dt)
+    h = xs + oracle.rms_norm(oracle.linear(o, W["w_o"]), W["post_attn_norm_w"], cfg.eps)
+    h16 = _round(h, dt)
+    a = _round(oracle.silu(oracle.linear(h16, W["w_gate"])) * oracle.linear(h16, W["w_up"]), dt)
+    y = h + oracle.rms_norm(oracle.linear(a, W["w_down"]), W["post_mlp_norm_w"], cfg.eps)
+    return _round(y, dt)

@@ -3,7 +3,7 @@ allocate device memory (an engine or plugin host that owns all device memory
 after start-up, or latency-bound code that cannot take cudaMalloc's implicit
 synchronisation). Its activation lives in the library's fixed 32 MiB device
 array instead of a caller workspace, so its output must equal blk_mlp's, call
-after call.
+after call, and meet the MLP's parity gate against the fp64 oracle.
 
 This file is collected last on purpose, and passes both on its own in a fresh
 process and after the other GPU tests."""
@@ -12,8 +12,9 @@ import ctypes as C
 import pytest
 import torch
 
+import oracle
 from alibi_attention_block_gb300 import _abi, build
-from tests.parity import check, to_dev
+from tests.parity import check, f64, to_dev
 from workloads import draw
 
 pytestmark = pytest.mark.gpu
@@ -50,6 +51,13 @@ def test_noalloc_mlp_matches_workspace_mlp_twice(act, T, D, F, dt):
     _abi.check(lib.blk_mlp(C.byref(desc), _ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(b_up),
                            _ptr(w_down), _ptr(b_down), _ptr(res), None, _ptr(ref), _ptr(ws),
                            ws_bytes.value, dtc, stream), "blk_mlp")
+    w = {"w_up": f64(w_up), "w_down": f64(w_down), "b_down": f64(b_down)}
+    if act == "swiglu":
+        w["w_gate"] = f64(w_gate)
+    else:
+        w["b_up"] = f64(b_up)
+    _, m = oracle.mlp(f64(x), w, act)
+    exact = m + f64(res)
     for _ in range(2):
         y = torch.full_like(x, float("nan"))
         _abi.check(lib.blk_mlp_noalloc(C.byref(desc), _ptr(x), _ptr(w_gate), _ptr(w_up), _ptr(b_up),
@@ -57,6 +65,7 @@ def test_noalloc_mlp_matches_workspace_mlp_twice(act, T, D, F, dt):
                                        stream), "blk_mlp_noalloc")
         torch.cuda.synchronize()
         check(y, ref.double().cpu().numpy(), f"noalloc {act}")
+        check(y, exact, f"noalloc {act} vs oracle")
     _abi.check(lib.blk_check_device_status(stream), "blk_check_device_status")
 
 
