@@ -83,7 +83,7 @@ constexpr size_t kGemmSplitBytes =
 cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const void* b2,
                         const GemmArgs& args, const RopeParams& rp, int num_sms, cudaStream_t s);
 
-// ---- K3: tcgen05 flash attention (attn.cu)
+// ---- K3: tcgen05 flash attention (dispatch in attn.cu)
 struct AttnArgs {
     const void* q;
     const void* k;
@@ -100,6 +100,8 @@ cudaError_t launch_attention(DType dt, const AttnArgs& a, cudaStream_t s);
 // head_dim 64 / 128: the paired-query-tile kernels (attn_pair.cu, attn_pair128.cu)
 cudaError_t launch_attention_pair64(DType dt, const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_attention_pair128(DType dt, const AttnArgs& a, cudaStream_t s);
+// head_dim 128 / 160: a group's query heads packed into one tile (attn_gqa.cu)
+cudaError_t launch_attention_gqa(DType dt, const AttnArgs& a, cudaStream_t s);
 
 // ---- K6: decode-step attention over a KV cache (attn_decode.cu)
 struct DecodeArgs {

@@ -59,7 +59,8 @@ def _check_post_norm(cfg, x, w, y, rows=None, name=""):
     got = y.reshape(cfg.tokens, cfg.hidden)
     if rows is not None:
         got = got[torch.as_tensor(rows, device=y.device)]
-    check(got, ref, f"{name} post-norm vs oracle on stored q/k/v", unit_scale=True)
+    check(got, ref, f"{name} post-norm vs oracle on stored q/k/v", unit_scale=True,
+          storage=cfg.dtype)
 
 
 def _gpu_forward(cfg, x, w):
@@ -81,7 +82,7 @@ def test_block_small(name):
     x, w = workloads.block_inputs(cfg)
     y = _gpu_forward(cfg, x, w)
     ref = oracle.block_forward(cfg, x, w)["y"]
-    check(y, ref, name, unit_scale=True, abs_tol=_abs_tol(cfg))
+    check(y, ref, name, unit_scale=True, abs_tol=_abs_tol(cfg), storage=cfg.dtype)
     if cfg.norm_place == "post":
         _check_post_norm(cfg, x, w, y, name=name)
 
@@ -133,7 +134,7 @@ def test_block_split_gemm_rounds():
                            | {0, 2047, 2048, 3071, 3072, 4095}))
     ref = oracle.block_forward(cfg, x, w, rows=rows)["y"]
     got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
-    check(got, ref, "split GEMM rounds", unit_scale=True, abs_tol=_abs_tol(cfg))
+    check(got, ref, "split GEMM rounds", unit_scale=True, abs_tol=_abs_tol(cfg), storage=cfg.dtype)
 
 
 @pytest.mark.parametrize("name", ["stablelm2_1p6b", "bloom_560m", "olmo2_1b", "stablelm2_12b"])
@@ -148,7 +149,8 @@ def test_block_full_size_sampled_rows(name):
     rows = workloads.sample_rows(cfg.tokens, 48, seed=cfg.seed)
     ref = oracle.block_forward(cfg, x, w, rows=rows)["y"]
     got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
-    check(got, ref, f"{name} sampled rows", unit_scale=True, abs_tol=_abs_tol(cfg))
+    check(got, ref, f"{name} sampled rows", unit_scale=True, abs_tol=_abs_tol(cfg),
+          storage=cfg.dtype)
     if cfg.norm_place == "post":
         _check_post_norm(cfg, x, w, y, rows=rows, name=name)
     assert torch.isfinite(y).all()

@@ -216,6 +216,14 @@ ATTN_CASES = [
     (1, 4, 4, 256, 128, True),
     (1, 4, 1, 300, 160, False),
     (2, 2, 2, 129, 160, False),
+    # GQA-packed tiles (the group's query heads in the rows of one tile)
+    (1, 8, 2, 300, 128, False),    # 4 heads x 32 positions per tile, ragged S
+    (1, 2, 1, 257, 128, True),     # 2 heads x 64 positions, ALiBi per row's head
+    (2, 32, 8, 520, 160, False),   # the 12B grouping (kv head j serves 4j..4j+3)
+    (1, 6, 2, 200, 160, True),     # 3 heads x 40 positions: 8 padding rows, ALiBi
+    (3, 8, 1, 700, 160, False),    # 8 heads x 16 positions
+    (1, 32, 1, 136, 128, False),   # a group of 32: two chunks of 16 heads x 8 positions
+    (1, 16, 2, 1, 160, False),     # one position
 ]
 
 
@@ -292,7 +300,7 @@ def test_attention_sweep_full_size_sampled(name):
     assert np.abs(got - exact).max() <= 2e-2
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 160])
 def test_attention_growing_logits_rescale(d):
     """Keys scaled up along the sequence make the running row max grow tile
     after tile, so O is rescaled in flight many times."""
@@ -305,6 +313,25 @@ def test_attention_growing_logits_rescale(d):
     o = blk.attn_prefill(to_dev(q), to_dev(k), to_dev(v))
     ref = oracle.attention(f64(q), f64(k), f64(v))
     check(o, ref.transpose(0, 2, 1, 3), f"attention growing logits d={d}", unit_scale=True)
+
+
+def test_gqa_packed_equals_replicated_heads():
+    """Packing a group's query heads into one tile changes only which rows
+    share a tile: at head_dim 160 (where MHA and GQA run the same kernel)
+    the GQA result is bit-identical to MHA with each kv head repeated for
+    its group, and at head_dim 128 it meets the gate against it."""
+    B, H, Hk, S = 2, 8, 2, 333
+    for d in (160, 128):
+        q = draw((B, H, S, d), "bf16", 90 + d)
+        k = draw((B, Hk, S, d), "bf16", 91 + d)
+        v = draw((B, Hk, S, d), "bf16", 92 + d)
+        o = blk.attn_prefill(to_dev(q), to_dev(k), to_dev(v))
+        rep = lambda t: t.repeat_interleave(H // Hk, dim=1).contiguous()  # noqa: E731
+        o_mha = blk.attn_prefill(to_dev(q), to_dev(rep(k)), to_dev(rep(v)))
+        if d == 160:
+            assert torch.equal(o, o_mha)
+        else:
+            check(o, f64(o_mha), "gqa vs replicated d=128", unit_scale=True)
 
 
 def test_attention_explicit_slopes_and_scale():
