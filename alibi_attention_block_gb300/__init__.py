@@ -182,6 +182,31 @@ def linear(x, w, bias=None, res1=None, res2=None, out=None):
     return out
 
 
+def q8_0_quantize(w):
+    """Q8_0 of a weight w [n, k] (k % 32 == 0) on the GPU: (codes int8
+    [n, k], scales fp16 [k/32, n], block-major)."""
+    n, k = w.shape
+    q = torch.empty((n, k), dtype=torch.int8, device=w.device)
+    d = torch.empty((k // 32, n), dtype=torch.float16, device=w.device)
+    _abi.check(_lib().blk_q8_0_quantize(_p(w), n, k, _p(q), _p(d), _dt(w), _stream()),
+               "blk_q8_0_quantize")
+    return q, d
+
+
+def linear_q8_0(x, q, d, bias=None, res1=None, res2=None, out=None):
+    """y = x W^T [+ bias] [+ res1] [+ res2] with W in Q8_0 form (q, d)."""
+    _same(x, bias, res1, res2, out)
+    if q.dtype != torch.int8 or d.dtype != torch.float16:
+        raise TypeError("Q8_0 codes are int8 and scales fp16")
+    k = x.shape[-1]
+    n = q.shape[0]
+    m = x.numel() // k
+    out = torch.empty((*x.shape[:-1], n), dtype=x.dtype, device=x.device) if out is None else out
+    _abi.check(_lib().blk_linear_q8_0(_p(x), _p(q), _p(d), _p(bias), _p(res1), _p(res2), _p(out),
+                                      m, n, k, _dt(x), _stream()), "blk_linear_q8_0")
+    return out
+
+
 def mlp(x, w_up, w_down, w_gate=None, b_up=None, b_down=None, res1=None, res2=None,
         act="swiglu", workspace=None, out=None):
     """SwiGLU or GELU(tanh) MLP with optional biases and residual adds."""
@@ -246,6 +271,41 @@ def forward(cfg, weights: dict, x, workspace=None, out=None):
     out = torch.empty_like(x) if out is None else out
     _abi.check(_lib().blk_forward(C.byref(desc), C.byref(w), _p(x), _p(out), _p(workspace),
                                   workspace.numel(), _dt(x), _stream()), "blk_forward")
+    return out
+
+
+Q8_PROJECTIONS = ("qkv", "o", "gate", "up", "down")
+
+
+def forward_q8_0(cfg, weights: dict, q8: dict, x, workspace=None, out=None):
+    """The block with Q8_0 projection weights (blk_forward_q8_0). weights:
+    the non-projection slots as for ``forward``; q8 maps ``q_<name>`` (int8
+    codes) and ``d_<name>`` (fp16 scales) for name in qkv, o, gate, up, down
+    (gate for SwiGLU only)."""
+    B, S, _ = x.shape
+    desc = block_desc(cfg, B, S)
+    if workspace is None:
+        workspace = torch.empty(forward_workspace_size(cfg, B, S), dtype=torch.uint8,
+                                device=x.device)
+    unknown = set(weights) - set(_abi.WEIGHT_SLOTS)
+    if unknown:
+        raise KeyError(f"unknown weight slots: {sorted(unknown)}")
+    unknown = set(q8) - set(_abi.Q8_SLOTS)
+    if unknown:
+        raise KeyError(f"unknown Q8_0 slots: {sorted(unknown)}")
+    for name, t in weights.items():
+        if name != "alibi_slopes":
+            _same(x, t)
+    for name, t in q8.items():
+        want = torch.int8 if name.startswith("q_") else torch.float16
+        if t.dtype != want or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous CUDA {want} tensor")
+    w = _abi.BlockWeights(*[_p(weights.get(n)) for n in _abi.WEIGHT_SLOTS])
+    qw = _abi.Q8Weights(*[_p(q8.get(n)) for n in _abi.Q8_SLOTS])
+    out = torch.empty_like(x) if out is None else out
+    _abi.check(_lib().blk_forward_q8_0(C.byref(desc), C.byref(w), C.byref(qw), _p(x), _p(out),
+                                       _p(workspace), workspace.numel(), _dt(x), _stream()),
+               "blk_forward_q8_0")
     return out
 
 

@@ -62,6 +62,14 @@ class BlockWeights(C.Structure):
     _fields_ = [(n, vp) for n in WEIGHT_SLOTS]
 
 
+Q8_SLOTS = ("q_qkv", "q_o", "q_gate", "q_up", "q_down", "d_qkv", "d_o", "d_gate", "d_up",
+            "d_down")
+
+
+class Q8Weights(C.Structure):
+    _fields_ = [(n, vp) for n in Q8_SLOTS]
+
+
 class ModelDesc(C.Structure):
     _fields_ = [("block", BlockDesc), ("n_layers", i32), ("vocab", i64), ("embed_norm", i32),
                 ("final_norm", i32), ("final_eps", f32)]
@@ -117,6 +125,10 @@ _PROTOS = {
     "blk_forward_ex": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp,
                                  C.c_size_t, C.c_int, vp, C.POINTER(vp), C.c_int,
                                  C.POINTER(i32), C.POINTER(C.c_int)]),
+    "blk_q8_0_quantize": (C.c_int, [vp, i64, i64, vp, vp, C.c_int, vp]),
+    "blk_linear_q8_0": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, C.c_int, vp]),
+    "blk_forward_q8_0": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights),
+                                   C.POINTER(Q8Weights), vp, vp, vp, C.c_size_t, C.c_int, vp]),
 }
 
 STEP_NAMES = ("input_norm", "qkv", "qk_norm_rope", "attention", "o_proj", "post_attn_norm",

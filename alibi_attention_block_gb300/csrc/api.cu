@@ -186,6 +186,21 @@ bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_2d_plain(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes,
+                        const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                        uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * elem_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_3d(CUtensorMap* m, DType dt, const void* base, uint64_t planes, uint64_t rows,
                   uint64_t cols, uint32_t box_rows) {
     auto fn = encode_fn();
@@ -281,7 +296,8 @@ blk_status validate_attn_desc(const blk_attn_desc* d) {
     return BLK_OK;
 }
 
-blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w) {
+blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w,
+                          const blk_q8_weights* q8 = nullptr) {
     BLK_REQUIRE(d && w, "descriptor or weights is NULL");
     blk_status st = validate_qkv_desc(&d->qkv);
     if (st != BLK_OK) return st;
@@ -311,6 +327,7 @@ blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w) {
     const bool seq_pre = pre && d->residual == BLK_RESIDUAL_SEQUENTIAL;
     const bool ln = d->norm_kind == BLK_NORM_LAYERNORM;
     const bool swiglu = d->act == BLK_ACT_SWIGLU;
+    const bool dense = q8 == nullptr;  // projection weights in the storage dtype
     // Every slot is either used (and then required, except optional biases) or
     // must be NULL: a weight handed to the wrong slot is an error, not ignored.
     struct Slot {
@@ -325,16 +342,16 @@ blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w) {
         {w->mlp_norm_b, "mlp_norm_b", seq_pre && ln, false},
         {w->post_attn_norm_w, "post_attn_norm_w", !pre, !pre},
         {w->post_mlp_norm_w, "post_mlp_norm_w", !pre, !pre},
-        {w->w_qkv, "w_qkv", true, true},
+        {w->w_qkv, "w_qkv", dense && true, dense && true},
         {w->b_qkv, "b_qkv", true, false},
         {w->q_norm_w, "q_norm_w", q.qk_norm != BLK_QKNORM_NONE, q.qk_norm != BLK_QKNORM_NONE},
         {w->k_norm_w, "k_norm_w", q.qk_norm != BLK_QKNORM_NONE, q.qk_norm != BLK_QKNORM_NONE},
-        {w->w_o, "w_o", true, true},
+        {w->w_o, "w_o", dense && true, dense && true},
         {w->b_o, "b_o", true, false},
-        {w->w_gate, "w_gate", swiglu, swiglu},
-        {w->w_up, "w_up", true, true},
+        {w->w_gate, "w_gate", dense && swiglu, dense && swiglu},
+        {w->w_up, "w_up", dense && true, dense && true},
         {w->b_up, "b_up", !swiglu, false},
-        {w->w_down, "w_down", true, true},
+        {w->w_down, "w_down", dense && true, dense && true},
         {w->b_down, "b_down", true, false},
         {w->alibi_slopes, "alibi_slopes", d->alibi != 0, false},
     };
@@ -342,6 +359,23 @@ blk_status validate_block(const blk_block_desc* d, const blk_block_weights* w) {
         if (!s.used && s.p) return fail(BLK_EINVAL, "weight slot %s is not used by this block and must be NULL", s.name);
         if (s.required && !s.p) return fail(BLK_EINVAL, "weight slot %s is required", s.name);
         if (s.p && !aligned16(s.p)) return fail(BLK_EINVAL, "weight slot %s is not 16-byte aligned", s.name);
+    }
+    if (dense) return BLK_OK;
+    // Q8_0 projections: every input width is cut into 32-wide blocks
+    BLK_REQUIRE(q.hidden % 32 == 0 && (q.n_heads * q.head_dim) % 32 == 0 &&
+                    d->intermediate % 32 == 0,
+                "Q8_0 weights need hidden, n_heads * head_dim and intermediate multiples of 32");
+    const Slot qslots[] = {
+        {q8->q_qkv, "q_qkv", true, true},   {q8->d_qkv, "d_qkv", true, true},
+        {q8->q_o, "q_o", true, true},       {q8->d_o, "d_o", true, true},
+        {q8->q_gate, "q_gate", swiglu, swiglu}, {q8->d_gate, "d_gate", swiglu, swiglu},
+        {q8->q_up, "q_up", true, true},     {q8->d_up, "d_up", true, true},
+        {q8->q_down, "q_down", true, true}, {q8->d_down, "d_down", true, true},
+    };
+    for (const Slot& s : qslots) {
+        if (!s.used && s.p) return fail(BLK_EINVAL, "Q8_0 slot %s is not used by this block and must be NULL", s.name);
+        if (s.required && !s.p) return fail(BLK_EINVAL, "Q8_0 slot %s is required", s.name);
+        if (s.p && !aligned16(s.p)) return fail(BLK_EINVAL, "Q8_0 slot %s is not 16-byte aligned", s.name);
     }
     return BLK_OK;
 }
@@ -427,10 +461,19 @@ void set_split(GemmArgs& g, void* split) {
                                               static_cast<size_t>(kGemmSplitSlots) * 128 * 256 * 4);
 }
 
+// A projection weight in Q8_0 form (codes and scales; q2/d2: SwiGLU's up
+// weight beside the gate weight in q/d).
+struct Q8W {
+    const int8_t* q;
+    const void* d;
+    const int8_t* q2;
+    const void* d2;
+};
+
 blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, const void* b_qkv,
                    const void* q_norm_w, const void* k_norm_w, void* q, void* k, void* v,
                    DType dt, cudaStream_t s, DevState* ds, StepLog* log = nullptr,
-                   void* split = nullptr) {
+                   void* split = nullptr, const Q8W* wq = nullptr) {
     // the GEMM epilogue rotates spans of 16 or 32 dims in registers; other
     // spans, and any qk-norm (which must precede the rotary), run in the
     // qk-norm/rotary kernel after the projection
@@ -452,7 +495,9 @@ blk_status run_qkv(const blk_qkv_desc* d, const void* x, const void* w_qkv, cons
     g.interleaved = d->qkv_layout == BLK_QKV_HEAD_INTERLEAVED;
     g.err = ds->err;
     set_split(g, split);
-    cudaError_t e = launch_gemm(dt, EPI_QKV, x, w_qkv, nullptr, g, rp, ds->sms, s);
+    cudaError_t e = wq ? launch_gemm_q8(dt, EPI_QKV, x, wq->q, wq->d, nullptr, nullptr, g, rp,
+                                        ds->sms, s)
+                       : launch_gemm(dt, EPI_QKV, x, w_qkv, nullptr, g, rp, ds->sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "qkv projection launch");
     blk_status st;
     if (log && (st = log->step(BLK_STEP_QKV)) != BLK_OK) return st;
@@ -482,7 +527,7 @@ enum : int { F32_OUT = 1, F32_RES1 = 2, F32_RES2 = 4 };
 blk_status run_linear(DType dt, int epi, const void* x, const void* w, const void* w2,
                       const void* bias, const void* r1, const void* r2, void* y, int64_t m,
                       int64_t n, int64_t k, cudaStream_t s, DevState* ds, int f32 = 0,
-                      void* split = nullptr) {
+                      void* split = nullptr, const Q8W* wq = nullptr) {
     GemmArgs g{};
     set_split(g, split);
     g.out_f32 = (f32 & F32_OUT) != 0;
@@ -497,7 +542,8 @@ blk_status run_linear(DType dt, int epi, const void* x, const void* w, const voi
     g.res2 = r2;
     g.err = ds->err;
     const RopeParams rp = make_rope(0, 0.f);
-    cudaError_t e = launch_gemm(dt, epi, x, w, w2, g, rp, ds->sms, s);
+    cudaError_t e = wq ? launch_gemm_q8(dt, epi, x, wq->q, wq->d, wq->q2, wq->d2, g, rp, ds->sms, s)
+                       : launch_gemm(dt, epi, x, w, w2, g, rp, ds->sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return BLK_OK;
 }
@@ -524,6 +570,12 @@ blk_status run_attn(const blk_attn_desc* d, const void* q, const void* k, const 
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     return BLK_OK;
 }
+
+
+blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
+                        const blk_q8_weights* q8, const void* x, void* y, void* workspace,
+                        size_t ws_bytes, blk_dtype dt, blk_stream_t s, void* const* events,
+                        int n_events, int32_t* step_kinds, int* n_launches);
 
 }  // namespace
 
@@ -770,6 +822,46 @@ blk_status blk_linear(const void* x, const void* w, const void* bias, const void
                       reinterpret_cast<cudaStream_t>(s), ds);
 }
 
+blk_status blk_q8_0_quantize(const void* w, int64_t n, int64_t k, int8_t* q, void* d,
+                             blk_dtype dt, blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    BLK_REQUIRE(n >= 0 && n <= kI32, "n out of range");
+    BLK_REQUIRE(k >= 32 && k % 32 == 0 && k <= kI32, "k must be a positive multiple of 32");
+    BLK_REQUIRE(n * (k / 32) <= kI32 * 256LL, "too many blocks");
+    BLK_CHECK_PTR(w, true);
+    BLK_CHECK_PTR(q, true);
+    BLK_CHECK_PTR(d, true);
+    if (n == 0) return BLK_OK;
+    DevState* ds = nullptr;
+    blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
+    const cudaError_t e = launch_q8_quantize(to_dt(dt), w, n, k, q, d, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? BLK_OK : cuda_fail(e, "q8_0 quantize launch");
+}
+
+blk_status blk_linear_q8_0(const void* x, const int8_t* q, const void* d, const void* bias,
+                           const void* res1, const void* res2, void* y, int64_t m, int64_t n,
+                           int64_t k, blk_dtype dt, blk_stream_t s) {
+    BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
+    BLK_REQUIRE(m >= 0 && m <= kI32, "m out of range");
+    BLK_REQUIRE(n >= 8 && n % 8 == 0 && n <= kI32, "n must be a positive multiple of 8");
+    BLK_REQUIRE(k >= 32 && k % 32 == 0 && k <= kI32, "k must be a positive multiple of 32");
+    BLK_CHECK_PTR(x, true);
+    BLK_CHECK_PTR(q, true);
+    BLK_CHECK_PTR(d, true);
+    BLK_CHECK_PTR(bias, false);
+    BLK_CHECK_PTR(res1, false);
+    BLK_CHECK_PTR(res2, false);
+    BLK_CHECK_PTR(y, true);
+    if (m == 0) return BLK_OK;
+    DevState* ds = nullptr;
+    blk_status st = dev_state(&ds);
+    if (st != BLK_OK) return st;
+    const Q8W wq{q, d, nullptr, nullptr};
+    return run_linear(to_dt(dt), EPI_LINEAR, x, nullptr, nullptr, bias, res1, res2, y, m, n, k,
+                      reinterpret_cast<cudaStream_t>(s), ds, 0, nullptr, &wq);
+}
+
 blk_status blk_mlp_workspace_size(const blk_mlp_desc* d, size_t* bytes) {
     BLK_REQUIRE(d && bytes, "NULL argument");
     BLK_REQUIRE(d->tokens >= 0 && d->intermediate >= 8, "bad sizes");
@@ -835,8 +927,28 @@ blk_status blk_forward(const blk_block_desc* d, const blk_block_weights* w, cons
 blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, const void* x,
                           void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s,
                           void* const* events, int n_events, int32_t* step_kinds, int* n_launches) {
+    return forward_impl(d, w, nullptr, x, y, workspace, ws_bytes, dt, s, events, n_events,
+                        step_kinds, n_launches);
+}
+
+blk_status blk_forward_q8_0(const blk_block_desc* d, const blk_block_weights* w,
+                            const blk_q8_weights* q8, const void* x, void* y, void* workspace,
+                            size_t ws_bytes, blk_dtype dt, blk_stream_t s) {
+    BLK_REQUIRE(q8, "Q8_0 weights are NULL");
+    return forward_impl(d, w, q8, x, y, workspace, ws_bytes, dt, s, nullptr, 0, nullptr, nullptr);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The block's composition for dense (q8 == NULL) or Q8_0 projection weights.
+blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
+                        const blk_q8_weights* q8, const void* x, void* y, void* workspace,
+                        size_t ws_bytes, blk_dtype dt, blk_stream_t s, void* const* events,
+                        int n_events, int32_t* step_kinds, int* n_launches) {
     BLK_REQUIRE(valid_dt(dt), "dtype must be BLK_F16 or BLK_BF16");
-    blk_status st = validate_block(d, w);
+    blk_status st = validate_block(d, w, q8);
     if (st != BLK_OK) return st;
     BLK_CHECK_PTR(x, true);
     BLK_CHECK_PTR(y, true);
@@ -868,6 +980,19 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     const bool pre = d->norm_place == BLK_NORM_PRE;
     const bool parallel = d->residual == BLK_RESIDUAL_PARALLEL;
     const bool swiglu = d->act == BLK_ACT_SWIGLU;
+    // Q8_0 projection weights (NULL handles: the dense slots of w)
+    Q8W wq_qkv{}, wq_o{}, wq_up{}, wq_down{};
+    if (q8) {
+        wq_qkv = Q8W{q8->q_qkv, q8->d_qkv, nullptr, nullptr};
+        wq_o = Q8W{q8->q_o, q8->d_o, nullptr, nullptr};
+        wq_up = swiglu ? Q8W{q8->q_gate, q8->d_gate, q8->q_up, q8->d_up}
+                       : Q8W{q8->q_up, q8->d_up, nullptr, nullptr};
+        wq_down = Q8W{q8->q_down, q8->d_down, nullptr, nullptr};
+    }
+    const Q8W* pq_qkv = q8 ? &wq_qkv : nullptr;
+    const Q8W* pq_o = q8 ? &wq_o : nullptr;
+    const Q8W* pq_up = q8 ? &wq_up : nullptr;
+    const Q8W* pq_down = q8 ? &wq_down : nullptr;
     cudaError_t e;
     StepLog log{events, n_events, step_kinds, n_launches, cs};
     if ((st = log.begin()) != BLK_OK) return st;
@@ -893,7 +1018,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     }
     // 2. projection (+bias), qk-norm, rotary, head split
     st = run_qkv(&q, attn_in, w->w_qkv, w->b_qkv, w->q_norm_w, w->k_norm_w, qb, kb, vb, t, cs, ds,
-                 &log, split);
+                 &log, split, pq_qkv);
     if (st != BLK_OK) return st;
     // 3. causal attention (+ALiBi)
     blk_attn_desc ad{q.batch, q.seq, q.n_heads, q.n_kv_heads, q.head_dim, 0.f, 1, d->alibi};
@@ -905,16 +1030,16 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
         // 4p. attn_out = o W_o^T (+b_o) kept in fp32; mlp on the same normed
         // input; y = x + attn_out + mlp
         st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
-                        cs, ds, F32_OUT, split);
+                        cs, ds, F32_OUT, split, pq_o);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
         st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, attn_in, swiglu ? w->w_gate : w->w_up,
                         swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
-                        split);
+                        split, pq_up);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_UP);
         st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, x, tmp, y, T, D, F, cs,
-                        ds, F32_RES2, split);
+                        ds, F32_RES2, split, pq_down);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
         return log.end();
@@ -923,7 +1048,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     if (pre) {
         // 4. h = x + o W_o^T (+b_o), fp32;  5. n2 = norm(h)
         st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, x, nullptr, hb, T, D, Hd, cs, ds,
-                        F32_OUT, split);
+                        F32_OUT, split, pq_o);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
         e = launch_norm(t, rms, NormIO{hb, true, nullptr, false, n2, nullptr, ds->err, ds->sms}, w->mlp_norm_w,
@@ -936,7 +1061,7 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
         // rounding would be magnified);  5. h = x + RMS(a) * w_post_attn
         // (fp32, and a storage copy for the MLP)
         st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
-                        cs, ds, F32_OUT, split);
+                        cs, ds, F32_OUT, split, pq_o);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
         e = launch_norm(t, true, NormIO{tmp, true, x, false, h16, static_cast<float*>(hb), ds->err, ds->sms},
@@ -948,20 +1073,20 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     // 6. MLP up (+activation)
     st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, mlp_in, swiglu ? w->w_gate : w->w_up,
                     swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
-                        split);
+                    split, pq_up);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_UP);
     if (pre) {
         // 7. y = h + a W_d^T (+b_d)
         st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, hb, nullptr, y, T, D, F, cs,
-                        ds, F32_RES1, split);
+                        ds, F32_RES1, split, pq_down);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
         return log.end();
     }
     // 7. m = a W_d^T;  8. y = h + RMS(m) * w_post_mlp
     st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, nullptr, nullptr, tmp, T, D, F,
-                    cs, ds, F32_OUT, split);
+                    cs, ds, F32_OUT, split, pq_down);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_DOWN);
     e = launch_norm(t, true, NormIO{tmp, true, hb, true, y, nullptr, ds->err, ds->sms}, w->post_mlp_norm_w, nullptr,
@@ -971,6 +1096,10 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
     return log.end();
 #undef BLK_STEP
 }
+
+}  // namespace
+
+extern "C" {
 
 blk_status blk_forward_host(const blk_block_desc* d, const blk_block_weights* w,
                             const void* x_host, void* y_host, void* x_dev, void* y_dev,

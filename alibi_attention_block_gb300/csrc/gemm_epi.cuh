@@ -1,0 +1,226 @@
+// The GEMM kernels' shared pieces (gemm.cu, gemm_q8.cu): tile constants,
+// the persistent work-unit decode with its split last round, and the fused
+// epilogues run on one accumulator tile read from TMEM.
+#pragma once
+
+#include "internal.h"
+
+namespace blk {
+namespace gemm {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each with half of the columns
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+constexpr int kSplitMinKb = 32;  // k-blocks per segment of a split unit, at least
+
+// Work unit v of the persistent loop: unit u over k-blocks [kb0, kb1). Units
+// before split_base run whole; each unit of the last, partial round is
+// split into split_s segments along K, run by otherwise idle CTAs.
+struct Unit {
+    int u, q, kb0, kb1;
+};
+template <bool SPLIT>
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& g, int v, int kb_count) {
+    if (!SPLIT || v < g.split_base) return {v, 0, 0, kb_count};
+    const int t = (v - g.split_base) / g.split_s;
+    const int q = v - g.split_base - t * g.split_s;
+    return {g.split_base + t, q, q * kb_count / g.split_s, (q + 1) * kb_count / g.split_s};
+}
+
+// Sum of a split unit's partial tiles for 32 columns of this thread's row, in
+// segment order (the same order whichever segment finishes last): its own
+// segment's values come from o, the others' from their [column][row]
+// partials.
+template <int BN>
+__device__ __forceinline__ void add_partials(float (&o)[32], const float* part, int part_s,
+                                             int self, int col0, int trow) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    for (int q = 0; q < part_s; ++q) {
+        if (q == self) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] += o[i];
+        } else {
+            const float* p = part + static_cast<size_t>(q) * (kBM * BN) +
+                             static_cast<size_t>(col0) * kBM + trow;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] += __ldcg(p + i * kBM);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = acc[i];
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, const float (&o)[32], int valid) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if (v * 8 < valid) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = o[v * 8 + e];
+            store8(dst + v * 8, f);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void add_row32(const T* src, float (&o)[32], int valid) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        if (v * 8 < valid) {
+            float f[8];
+            load8(src + v * 8, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[v * 8 + e] += f[e];
+        }
+    }
+}
+
+// fp32 write-out of a warp's 32 output rows x 32 columns, held one row per
+// thread (the TMEM lane layout): staged through the warp's 4 KB of shared
+// memory (16-byte chunks XOR-swizzled by row, conflict-free both ways), then
+// stored 4 rows x 128 bytes per instruction, whole lines instead of 16 bytes
+// of each of 32 rows (half-sector writes). Storage-type rows (64 bytes per
+// chunk) are stored directly: there the staging only lengthens the epilogue.
+__device__ __forceinline__ void store_chunk_f32(const GemmArgs& g, uint32_t stg, int lane,
+                                                int m_base, int n0, const float (&o)[32]) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        st_shared_v4(stg + lane * 128 + ((v ^ (lane & 7)) << 4), __float_as_uint(o[4 * v]),
+                     __float_as_uint(o[4 * v + 1]), __float_as_uint(o[4 * v + 2]),
+                     __float_as_uint(o[4 * v + 3]));
+    __syncwarp();
+    const int cq = lane & 7;       // columns 4 cq .. 4 cq + 3 of the chunk
+    const int gcol = n0 + cq * 4;  // N % 8 == 0: four columns are all valid or none
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int rr = p * 4 + (lane >> 3);
+        const float4 v = ld_shared_v4(stg + rr * 128 + ((cq ^ (rr & 7)) << 4));
+        const int grow = m_base + rr;
+        if (grow < g.M && gcol < g.N)
+            *reinterpret_cast<float4*>(static_cast<float*>(g.out) +
+                                       static_cast<int64_t>(grow) * g.N + gcol) = v;
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ float gelu_tanh_f(float z) {
+    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+    return 0.5f * z * (1.0f + tanhf(k0 * (z + 0.044715f * z * z * z)));
+}
+
+template <typename T, int BN, int EPI, int ROT, bool SPLIT>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParams& rp,
+                                              uint32_t tbase, int m, int nt, uint32_t stg,
+                                              int lane, int m_base, const float* part, int self,
+                                              int trow, int half) {
+    // this warp's half of the tile's 32-column chunks
+    constexpr int kChunks = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 32;
+    const int c_begin = half * (kChunks / 2), c_end = c_begin + kChunks / 2;
+    const bool row_ok = m < g.M;
+    if constexpr (EPI == EPI_SWIGLU) {
+        constexpr int kHalf = BN / 2;
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; ++c) {
+            uint32_t gr[32], ur[32];
+            tmem_ld32(tbase + c * 32, gr);
+            tmem_ld32(tbase + kHalf + c * 32, ur);
+            const int n0 = nt * kHalf + c * 32;
+            if (!row_ok || n0 >= g.N) continue;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                o[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+            store_row32(static_cast<T*>(g.out) + static_cast<int64_t>(m) * g.N + n0, o, g.N - n0);
+        }
+    } else if constexpr (EPI == EPI_QKV) {
+        const int d = g.d;
+        const int b = m / g.S;
+        const int s = m - b * g.S;
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            const int n0 = nt * BN + c * 32;
+            if (!row_ok || n0 >= g.N) continue;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            if constexpr (SPLIT)
+                if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
+            if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, 32);
+            int which, head, dd0;
+            if (g.interleaved) {
+                head = n0 / (3 * d);
+                const int w = n0 - head * 3 * d;
+                which = w / d;
+                dd0 = w - which * d;
+            } else {
+                const int hd = g.H * d, kd = g.Hk * d;
+                which = n0 < hd ? 0 : (n0 < hd + kd ? 1 : 2);
+                const int off = which == 0 ? 0 : (which == 1 ? hd : hd + kd);
+                head = (n0 - off) / d;
+                dd0 = n0 - off - head * d;
+            }
+            if constexpr (ROT > 0) {
+                // the span is a compile-time constant so o[] stays in registers
+                if (which < 2 && dd0 == 0) {
+                    constexpr int kHalf = ROT / 2;
+#pragma unroll
+                    for (int j = 0; j < kHalf; ++j) {
+                        float cs, sn;
+                        rope_cos_sin(rp, s, j, cs, sn);
+                        const float x1 = o[j], x2 = o[j + kHalf];
+                        o[j] = x1 * cs - x2 * sn;
+                        o[j + kHalf] = x2 * cs + x1 * sn;
+                    }
+                }
+            }
+            T* base = static_cast<T*>(which == 0 ? g.q : (which == 1 ? g.k : g.v));
+            const int nheads = which == 0 ? g.H : g.Hk;
+            T* dst = base + ((static_cast<int64_t>(b) * nheads + head) * g.S + s) * d + dd0;
+            store_row32(dst, o, 32);
+        }
+    } else {
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            const int n0 = nt * BN + c * 32;
+            if (n0 >= g.N) continue;  // uniform across the warp
+            const int valid = g.N - n0;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            if constexpr (SPLIT)
+                if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
+            if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
+            if constexpr (EPI == EPI_GELU) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
+            }
+            const int64_t off = static_cast<int64_t>(m) * g.N + n0;
+            if (row_ok && g.res1) {
+                if (g.res1_f32) add_row32(static_cast<const float*>(g.res1) + off, o, valid);
+                else add_row32(static_cast<const T*>(g.res1) + off, o, valid);
+            }
+            if (row_ok && g.res2) {
+                if (g.res2_f32) add_row32(static_cast<const float*>(g.res2) + off, o, valid);
+                else add_row32(static_cast<const T*>(g.res2) + off, o, valid);
+            }
+            if (g.out_f32)
+                store_chunk_f32(g, stg, lane, m_base, n0, o);  // all lanes (rows checked inside)
+            else if (row_ok)
+                store_row32(static_cast<T*>(g.out) + off, o, valid);
+        }
+    }
+}
+
+
+}  // namespace gemm
+}  // namespace blk

@@ -83,6 +83,23 @@ constexpr size_t kGemmSplitBytes =
 cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const void* b2,
                         const GemmArgs& args, const RopeParams& rp, int num_sms, cudaStream_t s);
 
+// the same GEMM on CTA pairs (gemm2.cu): 256-row tiles, one tcgen05 MMA of
+// M = 256 per pair of SMs; launch_gemm takes it whenever M > 128
+cudaError_t launch_gemm_pair(DType dt, int epi, const void* a, const void* b, const void* b2,
+                             const GemmArgs& g, const RopeParams& rp, int num_sms,
+                             cudaStream_t s);
+
+// ---- K2q: Q8_0 weights (gemm_q8.cu): codes q int8 [N, K], scales fp16
+// d [K/32, N]; for SWIGLU q/d are the gate weight and q2/d2 the up weight.
+// No split of the last round (the args' split fields are ignored).
+cudaError_t launch_gemm_q8(DType dt, int epi, const void* a, const int8_t* q, const void* d,
+                           const int8_t* q2, const void* d2, const GemmArgs& args,
+                           const RopeParams& rp, int num_sms, cudaStream_t s);
+// w [rows, cols] (storage dtype, cols % 32 == 0) -> codes q [rows, cols],
+// scales d [cols/32, rows] (fp16)
+cudaError_t launch_q8_quantize(DType dt, const void* w, int64_t rows, int64_t cols, int8_t* q,
+                               void* d, cudaStream_t s);
+
 // ---- K3: tcgen05 flash attention (dispatch in attn.cu)
 struct AttnArgs {
     const void* q;
@@ -135,6 +152,11 @@ blk_status report_error_status(blk_status st, const char* fmt, ...);
 // 2D row-major [rows, cols] map with a {64, box_rows} box and 128B swizzle.
 bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uint64_t cols,
                   uint32_t box_rows);
+// 2D row-major [rows, cols] map of any element type, no swizzle, with a
+// {box_cols, box_rows} box.
+bool make_tmap_2d_plain(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes,
+                        const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                        uint32_t box_rows);
 // 3D [planes, rows, cols] map with a {64, box_rows, 1} box and 128B swizzle.
 bool make_tmap_3d(CUtensorMap* m, DType dt, const void* base, uint64_t planes, uint64_t rows,
                   uint64_t cols, uint32_t box_rows);

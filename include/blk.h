@@ -192,6 +192,36 @@ blk_status blk_linear(const void* x, const void* w, const void* bias, const void
                       const void* res2, void* y, int64_t m, int64_t n, int64_t k, blk_dtype dt,
                       blk_stream_t s);
 
+/* ---- Q8_0 weights ------------------------------------------------------ */
+
+/* The q8/int8 weight path that the pages report as a secondary precision
+ * ("StableLM-2: partial RoPE ...", section 3 Results: q8 prefill-logit
+ * cosine 0.998910, 11/12 argmax; "OLMo-2: reordered (post) normalization
+ * ...", section 4: int8 cosine 0.998700), in the one format they name: Q8_0
+ * ("RoFormer HIP FP32 layout optimization": BS-RoFormer Q8_0), the GGML
+ * format. A weight W[n, k] (torch convention, k % 32 == 0) is stored as
+ *   q  int8 [n, k] row-major: one code per weight;
+ *   d  fp16 [k/32, n]: one scale per row and 32-input block, block-major
+ *      (the scale of row r, inputs 32j .. 32j+31 is d[j * n + r]).
+ * Both pointers 16-byte aligned, owned by the caller. */
+
+/* Quantize w [n, k] (dt) to Q8_0 on the GPU, with the float32 arithmetic of
+ * GGML's reference quantizer: d = absmax / 127 per block, codes
+ * round(w * (1 / d)) half away from zero (0 where d = 0), and d rounded to
+ * fp16 only after the codes are taken. Bit-exact: the same w gives the same
+ * q and d as any IEEE float32 implementation of those steps.
+ * BLK_EINVAL: k not a positive multiple of 32, NULL or misaligned pointers. */
+blk_status blk_q8_0_quantize(const void* w, int64_t n, int64_t k, int8_t* q, void* d,
+                             blk_dtype dt, blk_stream_t s);
+
+/* y = x W^T [+ bias] [+ res1] [+ res2] with W given as Q8_0 (q, d): blk_linear
+ * with each weight element q * d rounded once to dt on chip (a W8A16 tcgen05
+ * GEMM). x [m, k], bias [n], res1/res2/y [m, n] in dt; n % 8 == 0,
+ * k % 32 == 0. Errors as blk_linear. */
+blk_status blk_linear_q8_0(const void* x, const int8_t* q, const void* d, const void* bias,
+                           const void* res1, const void* res2, void* y, int64_t m, int64_t n,
+                           int64_t k, blk_dtype dt, blk_stream_t s);
+
 typedef struct {
     int64_t tokens, hidden, intermediate;
     int32_t act; /* blk_act */
@@ -301,6 +331,23 @@ typedef enum {
 blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, const void* x,
                           void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s,
                           void* const* events, int n_events, int32_t* step_kinds, int* n_launches);
+
+/* The block with Q8_0 projection weights (the q8 rows of "StableLM-2: partial
+ * RoPE ...", section 3 Results and "OLMo-2 ...", section 4; format above):
+ * blk_forward with every projection (QKV, output, MLP gate/up, down) run as
+ * a W8A16 GEMM on its codes and scales. w holds the norms, biases, qk-norm
+ * weights and ALiBi slopes as for blk_forward; its five projection slots
+ * (w_qkv, w_o, w_gate, w_up, w_down) must be NULL, and q8 gives them, with
+ * the same shapes ([out, in] codes, [in/32, out] scales; q_gate/d_gate NULL
+ * unless the MLP is SwiGLU). hidden, n_heads * head_dim and intermediate must
+ * be multiples of 32. Workspace, errors and everything else as blk_forward. */
+typedef struct {
+    const int8_t *q_qkv, *q_o, *q_gate, *q_up, *q_down;  /* codes */
+    const void *d_qkv, *d_o, *d_gate, *d_up, *d_down;    /* fp16 scales */
+} blk_q8_weights;
+blk_status blk_forward_q8_0(const blk_block_desc* d, const blk_block_weights* w,
+                            const blk_q8_weights* q8, const void* x, void* y, void* workspace,
+                            size_t ws_bytes, blk_dtype dt, blk_stream_t s);
 
 /* blk_forward on host buffers, with the copies overlapped with the compute.
  * x_host and y_host are [batch, seq, hidden] in pinned host memory; x_dev and

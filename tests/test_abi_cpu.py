@@ -290,3 +290,44 @@ def test_decode_validation(lib):
     ali = _abi.DecodeDesc(1, 16, 12, 12, 64, -1.0, 1)  # standard slopes need 2^k heads
     assert lib.blk_attn_decode(C.byref(ali), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 1 << 30, 1,
                                None) == _abi.BLK_EUNSUPPORTED
+
+
+def test_q8_validation(lib):
+    st = lib.blk_q8_0_quantize(FAKE, 16, 48, FAKE, FAKE, _abi.BLK_BF16, None)
+    assert st == _abi.BLK_EINVAL and "multiple of 32" in _err(lib)
+    st = lib.blk_q8_0_quantize(FAKE, 16, 64, None, FAKE, _abi.BLK_BF16, None)
+    assert st == _abi.BLK_EINVAL and "q is NULL" in _err(lib)
+    assert lib.blk_q8_0_quantize(FAKE, 0, 64, FAKE, FAKE, _abi.BLK_BF16, None) == _abi.BLK_OK
+    st = lib.blk_linear_q8_0(FAKE, FAKE, FAKE, None, None, None, FAKE, 4, 64, 40, _abi.BLK_BF16, None)
+    assert st == _abi.BLK_EINVAL and "multiple of 32" in _err(lib)
+    st = lib.blk_linear_q8_0(FAKE, FAKE, FAKE + 8, None, None, None, FAKE, 4, 64, 64, _abi.BLK_BF16, None)
+    assert st == _abi.BLK_EINVAL and "aligned" in _err(lib)
+    assert lib.blk_linear_q8_0(FAKE, FAKE, FAKE, None, None, None, FAKE, 0, 64, 64,
+                               _abi.BLK_F16, None) == _abi.BLK_OK
+
+
+def test_q8_block_slot_rules(lib):
+    """blk_forward_q8_0 takes its projections from the Q8_0 struct only: a
+    dense projection slot is rejected, a missing Q8_0 slot too, and widths
+    must be multiples of 32."""
+    import workloads
+    from alibi_attention_block_gb300 import block_desc
+    cfg = workloads.scaled(workloads.BLOCK_CONFIGS["stablelm2_1p6b"], batch=1, seq=64, hidden=256,
+                           n_heads=4, n_kv_heads=4, intermediate=704)
+    desc = block_desc(cfg, 1, 64)
+    dense = {n: FAKE for n in ("attn_norm_w", "attn_norm_b", "mlp_norm_w", "mlp_norm_b", "b_qkv")}
+    q8 = {n: FAKE for n in _abi.Q8_SLOTS}
+    w = _abi.BlockWeights(*[dense.get(n) for n in _abi.WEIGHT_SLOTS])
+    qw = _abi.Q8Weights(*[q8.get(n) for n in _abi.Q8_SLOTS])
+    ws = C.c_size_t(0)
+    assert lib.blk_forward_workspace_size(C.byref(desc), C.byref(ws)) == _abi.BLK_OK
+    call = lambda w_, q_: lib.blk_forward_q8_0(C.byref(desc), C.byref(w_), C.byref(q_), FAKE,  # noqa: E731
+                                               FAKE + 4096, FAKE, ws.value, _abi.BLK_BF16, None)
+    w2 = _abi.BlockWeights(*[dict(dense, w_o=FAKE).get(n) for n in _abi.WEIGHT_SLOTS])
+    assert call(w2, qw) == _abi.BLK_EINVAL and "w_o" in _err(lib)
+    q2 = _abi.Q8Weights(*[dict(q8, d_down=None).get(n) for n in _abi.Q8_SLOTS])
+    assert call(w, q2) == _abi.BLK_EINVAL and "d_down" in _err(lib)
+    odd = block_desc(workloads.scaled(cfg, intermediate=688), 1, 64)
+    assert lib.blk_forward_q8_0(C.byref(odd), C.byref(w), C.byref(qw), FAKE, FAKE + 4096, FAKE,
+                                1 << 30, _abi.BLK_BF16, None) == _abi.BLK_EINVAL
+    assert "multiples of 32" in _err(lib)

@@ -59,7 +59,8 @@ def test_norm_in_place():
 # ----------------------------------------------------------------- linear --
 @pytest.mark.parametrize("dt", DTYPES)
 @pytest.mark.parametrize("m,n,k", [(128, 256, 256), (200, 264, 688), (1000, 2048, 2048),
-                                   (37, 8, 8), (300, 768, 5632), (513, 1024, 64)])
+                                   (37, 8, 8), (300, 768, 5632), (513, 1024, 64),
+                                   (129, 512, 256), (257, 256, 4096)])
 def test_linear(dt, m, n, k):
     seed = m + n + k
     x = draw((m, k), dt, seed)
@@ -220,7 +221,8 @@ ATTN_CASES = [
     (1, 8, 2, 300, 128, False),    # 4 heads x 32 positions per tile, ragged S
     (1, 2, 1, 257, 128, True),     # 2 heads x 64 positions, ALiBi per row's head
     (2, 32, 8, 520, 160, False),   # the 12B grouping (kv head j serves 4j..4j+3)
-    (1, 6, 2, 200, 160, True),     # 3 heads x 40 positions: 8 padding rows, ALiBi
+    (1, 6, 2, 200, 160, False),    # 3 heads x 40 positions: 8 padding rows
+    (1, 8, 2, 200, 160, True),     # ALiBi with each row's own head slope
     (3, 8, 1, 700, 160, False),    # 8 heads x 16 positions
     (1, 32, 1, 136, 128, False),   # a group of 32: two chunks of 16 heads x 8 positions
     (1, 16, 2, 1, 160, False),     # one position

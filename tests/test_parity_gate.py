@@ -19,9 +19,17 @@ def test_half_ulp_bounds_the_storage_rounding(storage, dtype):
 
 
 def test_storage_allowance_is_on_top_of_the_tolerance():
-    ref = np.array([[9.0, 1.0, -12.0, 0.5]])
-    ok = ref + np.array([[0.031 + 0.019, 0.0039 + 0.019, -0.031 - 0.019, 0.0]])
+    ref = np.array([[0.5, 1.0, -1.5, 0.2]])                      # rms < 1: scale 1
+    hu = half_ulp(ref, "bf16")
+    ok = ref + np.sign(ref) * (hu + 0.019)
     check(ok, ref, "within", unit_scale=True, storage="bf16", cos_min=0.99)
-    bad = ref + np.array([[0.0, 0.03, 0.0, 0.0]])
+    bad = ref + np.array([[0.0, 0.03, 0.0, 0.0]])                # 0.026 past half an ulp
     with pytest.raises(AssertionError):
         check(bad, ref, "beyond", unit_scale=True, storage="bf16", cos_min=0.99)
+
+
+def test_outputs_larger_than_unit_scale_scale_the_tolerance():
+    ref = np.array([[3.0, -3.0, 3.0, -3.0]])                     # rms 3
+    check(ref + 0.055, ref, "within", unit_scale=True, cos_min=0.99)
+    with pytest.raises(AssertionError):
+        check(ref + 0.065, ref, "beyond", unit_scale=True, cos_min=0.99)
