@@ -129,6 +129,9 @@ _PROTOS = {
     "blk_linear_q8_0": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, C.c_int, vp]),
     "blk_forward_q8_0": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights),
                                    C.POINTER(Q8Weights), vp, vp, vp, C.c_size_t, C.c_int, vp]),
+    "blk_forward_q8_0_ex": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights),
+                                      C.POINTER(Q8Weights), vp, vp, vp, C.c_size_t, C.c_int, vp,
+                                      C.POINTER(vp), C.c_int, C.POINTER(i32), C.POINTER(C.c_int)]),
 }
 
 STEP_NAMES = ("input_norm", "qkv", "qk_norm_rope", "attention", "o_proj", "post_attn_norm",

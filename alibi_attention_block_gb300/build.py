@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libblk.so")
-SOURCES = ("api.cu", "norm.cu", "rope.cu", "gemm.cu", "gemm_q8.cu", "attn.cu", "attn_pair.cu", "attn_pair128.cu", "attn_gqa.cu", "attn_decode.cu", "noalloc.cu", "model.cu")
+SOURCES = ("api.cu", "norm.cu", "rope.cu", "gemm.cu", "gemm2.cu", "gemm_q8.cu", "attn.cu", "attn_pair.cu", "attn_pair128.cu", "attn_gqa.cu", "attn_decode.cu", "noalloc.cu", "model.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

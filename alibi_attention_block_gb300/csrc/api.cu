@@ -934,8 +934,18 @@ blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, c
 blk_status blk_forward_q8_0(const blk_block_desc* d, const blk_block_weights* w,
                             const blk_q8_weights* q8, const void* x, void* y, void* workspace,
                             size_t ws_bytes, blk_dtype dt, blk_stream_t s) {
+    return blk_forward_q8_0_ex(d, w, q8, x, y, workspace, ws_bytes, dt, s, nullptr, 0, nullptr,
+                               nullptr);
+}
+
+blk_status blk_forward_q8_0_ex(const blk_block_desc* d, const blk_block_weights* w,
+                               const blk_q8_weights* q8, const void* x, void* y, void* workspace,
+                               size_t ws_bytes, blk_dtype dt, blk_stream_t s,
+                               void* const* events, int n_events, int32_t* step_kinds,
+                               int* n_launches) {
     BLK_REQUIRE(q8, "Q8_0 weights are NULL");
-    return forward_impl(d, w, q8, x, y, workspace, ws_bytes, dt, s, nullptr, 0, nullptr, nullptr);
+    return forward_impl(d, w, q8, x, y, workspace, ws_bytes, dt, s, events, n_events, step_kinds,
+                        n_launches);
 }
 
 }  // extern "C"

@@ -326,6 +326,7 @@ cudaError_t launch_gemm(DType dt, int epi, const void* a, const void* b, const v
     const double a_bytes = 2.0 * args.M * args.K;
     const double b_bytes = 2.0 * args.N * args.K * (epi == EPI_SWIGLU ? 2 : 1);
     g.n_fastest = a_bytes > 48.0 * (1 << 20) && a_bytes > b_bytes;
+    if (g.M > kBM) return launch_gemm_pair(dt, epi, a, b, b2, g, rp, num_sms, s);
     if (dt == DType::F16) return launch_t<__half>(dt, epi, a, b, b2, g, rp, num_sms, s);
     return launch_t<__nv_bfloat16>(dt, epi, a, b, b2, g, rp, num_sms, s);
 }

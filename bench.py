@@ -600,11 +600,15 @@ def _spec_peak(dev, peaks) -> dict:
     return {"tflops": tf, "derivation": f"{sms} SMs x {TC_FLOP_PER_CLK_SM} flop/clk/SM x {mhz:.0f} MHz"}
 
 
+_PROJ_SLOTS = {"qkv": "w_qkv", "o": "w_o", "gate": "w_gate", "up": "w_up", "down": "w_down"}
+
+
 class _Block:
     """One workload's inputs, weights and workspace on the device, and the
-    ctypes arguments of blk_forward_ex."""
+    ctypes arguments of blk_forward_ex (or, with q8, of blk_forward_q8_0_ex:
+    the projection weights quantized to Q8_0 on the device before timing)."""
 
-    def __init__(self, cfg, dev, lib):
+    def __init__(self, cfg, dev, lib, q8=False):
         import ctypes as C
 
         import alibi_attention_block_gb300 as blk
@@ -613,6 +617,15 @@ class _Block:
         self.x_cpu, self.w_cpu = workloads.block_inputs(cfg)
         self.x = self.x_cpu.to(dev)
         self.wd = {k: t.to(dev) for k, t in self.w_cpu.items()}
+        self.q8 = None
+        if q8:
+            q8w = {}
+            for name, slot in _PROJ_SLOTS.items():
+                if slot in self.wd:
+                    q8w["q_" + name], q8w["d_" + name] = blk.q8_0_quantize(self.wd.pop(slot))
+            self.q8_tensors = q8w
+            self.q8 = _abi.Q8Weights(*[(q8w[n].data_ptr() if n in q8w else None)
+                                       for n in _abi.Q8_SLOTS])
         self.y = torch.empty_like(self.x)
         self.ws_bytes = blk.forward_workspace_size(cfg, cfg.batch, cfg.seq)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
@@ -627,11 +640,17 @@ class _Block:
     def step(self, stream, events):
         C = self.C
         arr = (C.c_void_p * self.max_ev)(*[e.cuda_event for e in events]) if events else None
-        self._abi.check(self.lib.blk_forward_ex(
-            C.byref(self.desc), C.byref(self.wstruct), C.c_void_p(self.x.data_ptr()),
-            C.c_void_p(self.y.data_ptr()), C.c_void_p(self.ws.data_ptr()), self.ws_bytes, self.dt,
-            C.c_void_p(stream.cuda_stream), arr, self.max_ev if events else 0, self.kinds,
-            C.byref(self.nl)), "blk_forward_ex")
+        common = (C.c_void_p(self.x.data_ptr()), C.c_void_p(self.y.data_ptr()),
+                  C.c_void_p(self.ws.data_ptr()), self.ws_bytes, self.dt,
+                  C.c_void_p(stream.cuda_stream), arr, self.max_ev if events else 0, self.kinds,
+                  C.byref(self.nl))
+        if self.q8 is not None:
+            self._abi.check(self.lib.blk_forward_q8_0_ex(
+                C.byref(self.desc), C.byref(self.wstruct), C.byref(self.q8), *common),
+                "blk_forward_q8_0_ex")
+            return
+        self._abi.check(self.lib.blk_forward_ex(C.byref(self.desc), C.byref(self.wstruct),
+                                                *common), "blk_forward_ex")
 
 
 def _time_steps(bl, args, flush, stream, dist, sampler_index, steps, warmup):
@@ -745,8 +764,9 @@ def _cpu_baseline(cfg, budget_s):
 
 
 # the other block workloads reported beside the headline one, each in the
-# same launch configuration and timing
-EXTRA_CONFIGS = ("bloom_560m", "olmo2_1b", "stablelm2_12b")
+# same launch configuration and timing; "+q8_0": the same block with Q8_0
+# projection weights (W8A16 GEMMs)
+EXTRA_CONFIGS = ("bloom_560m", "olmo2_1b", "stablelm2_12b", "stablelm2_1p6b+q8_0")
 
 
 def run_ours(args, cfg, rank, world, local_rank, dist):
@@ -832,16 +852,23 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
     others = {}
     if not args.no_extra_configs and cfg.name == "stablelm2_1p6b":
         for name in EXTRA_CONFIGS:
-            c = workloads.BLOCK_CONFIGS[name]
-            b2 = _Block(c, dev, lib)
+            q8 = name.endswith("+q8_0")
+            c = workloads.BLOCK_CONFIGS[name.split("+")[0]]
+            b2 = _Block(c, dev, lib, q8=q8)
             r2 = _time_steps(b2, args, flush, stream, None, local_rank, args.steps, args.warmup)
             ms2 = float(sum(r2["step_ms"])) / args.steps
             rep2 = _report(c, r2["kernel_ms"], ms2, sum(r2["step_ms"]) / 1e3, peaks, spec)
             others[name] = {
-                "config": _config(c, "flushed before every step (512 MiB write)"),
+                "config": dict(_config(c, "flushed before every step (512 MiB write)"),
+                               weights="Q8_0 (int8 codes, fp16 scales per 32 inputs)" if q8
+                               else c.dtype),
                 "tokens_per_s": c.tokens / (ms2 / 1e3), "ms_per_step": ms2,
                 "dtype": c.dtype, **rep2,
-                "cpu_baseline": None if args.no_cpu_baseline else _cpu_baseline(c, args.cpu_budget / 2),
+                # the oracle of the Q8_0 block is the same block on the
+                # dequantized weights: the headline's baseline, not re-timed
+                "cpu_baseline": (None if args.no_cpu_baseline else
+                                 dict(cpu, sample=cpu["sample"] + " (the same oracle block)") if q8
+                                 else _cpu_baseline(c, args.cpu_budget / 2)),
                 "gpu_launches": r2["n_launch"] * args.steps, "clocks": r2["clocks"]}
             del b2
             torch.cuda.empty_cache()

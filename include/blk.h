@@ -348,6 +348,12 @@ typedef struct {
 blk_status blk_forward_q8_0(const blk_block_desc* d, const blk_block_weights* w,
                             const blk_q8_weights* q8, const void* x, void* y, void* workspace,
                             size_t ws_bytes, blk_dtype dt, blk_stream_t s);
+/* blk_forward_q8_0 with per-launch events, as blk_forward_ex. */
+blk_status blk_forward_q8_0_ex(const blk_block_desc* d, const blk_block_weights* w,
+                               const blk_q8_weights* q8, const void* x, void* y, void* workspace,
+                               size_t ws_bytes, blk_dtype dt, blk_stream_t s,
+                               void* const* events, int n_events, int32_t* step_kinds,
+                               int* n_launches);
 
 /* blk_forward on host buffers, with the copies overlapped with the compute.
  * x_host and y_host are [batch, seq, hidden] in pinned host memory; x_dev and
