@@ -8,8 +8,8 @@
 // instruction each CTA holds and TMA-loads only its own 128 rows of A and
 // its own half (128 rows) of B, so per SM the operand reads and the TMA
 // writes per k-block fall by a third while the MMA work per SM stays the
-// same. Nothing is multicast: every TMA load lands in the issuing CTA's own
-// shared memory. Only barrier signals cross between the two CTAs:
+// same. Every TMA load lands in the issuing CTA's own shared memory; only
+// barrier signals cross between the two CTAs:
 //   - each CTA's TMA loads of a stage count their bytes on the even CTA's
 //     "full" barrier (cta_group::2 completion), whose single arrival (with
 //     the whole stage's byte count) comes from the even CTA's producer;
