@@ -260,18 +260,28 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 const uint32_t sq = sbase + st * kTmaStageBytes + kABytes;
                 const uint32_t sd = sq + kCodeBytes;
                 const uint32_t sb = sbase + kOffB + bs * kBTileBytes;
-#pragma unroll 2
-                for (int i = 0; i < (BN * kBK / 16) / (32 * kConvWarps); ++i) {
-                    const int c = i * (32 * kConvWarps) + tid;
-                    const int r = c >> 2;    // B row
-                    const int c16 = c & 3;   // 16 codes: k = 16 c16 .. 16 c16 + 15
-                    const uint4 w = ld_shared_u4(sq + r * kBK + c16 * 16);
+                // all of this thread's loads first, then the arithmetic and
+                // stores: one converter warp per scheduler has nothing else to
+                // hide shared-memory latency behind
+                constexpr int kIters = (BN * kBK / 16) / (32 * kConvWarps);
+                const int c16 = tid & 3;   // 16 codes: k = 16 c16 .. 16 c16 + 15
+                uint4 w[kIters];
+                uint32_t dh[kIters];
+#pragma unroll
+                for (int i = 0; i < kIters; ++i) {
+                    const int r = (i * (32 * kConvWarps) + tid) >> 2;  // B row
+                    w[i] = ld_shared_u4(sq + r * kBK + c16 * 16);
                     // scale of 32-input block c16 / 2 of row r ([half][block][128] fp16)
-                    const uint32_t dh = ld_shared_u16(
+                    dh[i] = ld_shared_u16(
                         sd + ((r >> 7) * (kScaleBytes / 4) + (c16 >> 1) * 128 + (r & 127)) * 2);
-                    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(dh)));
+                }
+#pragma unroll
+                for (int i = 0; i < kIters; ++i) {
+                    const int r = (i * (32 * kConvWarps) + tid) >> 2;
+                    const float d =
+                        __half2float(__ushort_as_half(static_cast<unsigned short>(dh[i])));
                     uint32_t o[8];
-                    expand16<T>(w, d, o);
+                    expand16<T>(w[i], d, o);
                     const uint32_t rb = sb + r * 128;
                     st_shared_v4(rb + (((2 * c16) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
                     st_shared_v4(rb + (((2 * c16 + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);

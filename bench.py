@@ -43,10 +43,15 @@ METRIC = "prefill tokens/s per block and attention TFLOP/s (% of GB300 FP16 peak
 # counters were taken: a kernel changed since then reports null. Keyed by
 # (workload, block step).
 _KERNEL_SOURCES = {
-    "gemm": ("alibi_attention_block_gb300/csrc/gemm.cu", "alibi_attention_block_gb300/csrc/common.cuh",
+    "gemm": ("alibi_attention_block_gb300/csrc/gemm.cu", "alibi_attention_block_gb300/csrc/gemm2.cu",
+             "alibi_attention_block_gb300/csrc/gemm_epi.cuh",
+             "alibi_attention_block_gb300/csrc/common.cuh",
              "alibi_attention_block_gb300/csrc/internal.h"),
 }
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # gate/up SwiGLU GEMM on CTA pairs: 80.76 MB read + 63.03 MB written
+    ("stablelm2_1p6b", "mlp_up"): {"kind": "gemm", "bytes": 143783424, "sha256": "38a2ea0835f7d4c48d02d226c51ad48292d293c154c3b31ed416d400280d1ccb"},
+}
 
 
 def _sources_sha(kind: str) -> str:
@@ -473,6 +478,43 @@ def run_decode(args, rank):
         print(json.dumps({"metric": "decode-step attention over a KV cache (GB/s)",
                           "unit": "GB/s", "peak_source": peaks["source"] + " copy",
                           "decode": res}), flush=True)
+
+
+def run_q8(args, rank):
+    """Q8_0 weights at the StableLM-2-1.6B block's projection shapes: the
+    W8A16 GEMM (blk_linear_q8_0) beside the bf16 GEMM (blk_linear) on the
+    same activations, and the quantizer (blk_q8_0_quantize) on the weights.
+    Compute-bound GEMMs, timed back to back."""
+    import alibi_attention_block_gb300 as blk
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    peaks = _peaks()
+    T, D, F, QKV = 8192, 2048, 5632, 6144
+    res = {}
+    for name, (m, n, k) in {"qkv": (T, QKV, D), "o_proj": (T, D, D), "up": (T, F, D),
+                            "down": (T, D, F)}.items():
+        x = workloads.draw((m, k), "bf16", 300 + n + k).to(dev)
+        w = workloads.draw((n, k), "bf16", 301 + n + k, "w").to(dev)
+        q, d = blk.q8_0_quantize(w)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        t_q8 = _time_back_to_back(lambda: blk.linear_q8_0(x, q, d, out=y), reps=20)
+        t_bf = _time_back_to_back(lambda: blk.linear(x, w, out=y), reps=20)
+        t_qz = _time_back_to_back(lambda: blk.q8_0_quantize(w), reps=20)
+        flops = 2.0 * m * n * k
+        res[name] = {"m": m, "n": n, "k": k,
+                     "q8_ms": t_q8, "q8_tflops": flops / (t_q8 / 1e3) / 1e12,
+                     "bf16_ms": t_bf, "bf16_tflops": flops / (t_bf / 1e3) / 1e12,
+                     "q8_frac_of_measured_bf16_peak": flops / (t_q8 / 1e3) / 1e12 / peaks["bf16_tflops"],
+                     "weight_bytes_q8": n * k * (1 + 2 / 32), "weight_bytes_bf16": 2 * n * k,
+                     "quantize_ms": t_qz,
+                     "quantize_gbs": (2 * n * k + n * k + 2 * n * k / 32) / (t_qz / 1e3) / 1e9}
+        del x, w, q, d, y
+        torch.cuda.empty_cache()
+    blk.check_device_status()
+    if rank == 0:
+        print(json.dumps({"metric": "Q8_0 W8A16 GEMM vs bf16 GEMM at the StableLM-2-1.6B projections",
+                          "peak_source": peaks["source"] + " burst bf16", "q8": res}), flush=True)
 
 
 # ----------------------------------------------------------------- oracle --
@@ -935,6 +977,8 @@ def main():
                     help="time decode-step attention over KV caches instead of the block")
     ap.add_argument("--attn-sweep", action="store_true",
                     help="time the attention-only workloads instead of the block")
+    ap.add_argument("--q8", action="store_true",
+                    help="time the Q8_0 W8A16 GEMM and quantizer at the block's projection shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -942,6 +986,8 @@ def main():
     dist, rank, world, local_rank = _dist()
     if args.attn_sweep:
         run_attn_sweep(args, rank)
+    elif args.q8:
+        run_q8(args, rank)
     elif args.model:
         run_model(args, rank)
     elif args.decode:
