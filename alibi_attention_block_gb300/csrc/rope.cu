@@ -684,6 +684,166 @@ bool launch_head_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_
     return true;
 }
 
+// Row-group path at head_dim 160 (StableLM-2-12B): bias, per-head LayerNorm
+// (or none) and rotary over the first ROT <= 40 dims, in place. A plane
+// (b, head) of q or k is [S, 160] contiguous, so 8 consecutive rows are
+// 2560 contiguous bytes: one warp takes them, 4 lanes per row and 40
+// elements (five 16-byte vectors) per lane, every access a whole line of
+// the warp's block. The row statistics are two shuffle steps over a row's
+// 4 lanes. The rotary span lies within each row's first lane (dims 0..39):
+// the row's 4 lanes compute 5 of its ROT/2 (cos, sin) pairs each and hand
+// them to the first lane by shuffle. Persistent warps over blocks, the next
+// block's rows loaded before this one is computed.
+constexpr int kRgWarps = 8;
+template <typename T, int ROT>
+__global__ void __launch_bounds__(kRgWarps * 32) qk_rowgroup_kernel(QkNormRopeArgs a,
+                                                                    RopeParams rp) {
+    constexpr int D = 160, VL = 5;  // vectors per lane
+    constexpr int kPairs = ROT / 2;
+    static_assert(ROT % 2 == 0 && ROT <= 8 * VL, "the rotary span must lie in a row's first lane");
+    const int lane = threadIdx.x & 31;
+    const int r = lane >> 2;    // row of the block
+    const int sub = lane & 3;   // which 40 dims of the row
+    const int rblocks = (a.S + 7) / 8;
+    const int64_t q_items = static_cast<int64_t>(a.B) * a.H * rblocks;
+    const int64_t items = q_items + static_cast<int64_t>(a.B) * a.Hk * rblocks;
+    const int64_t wstep = static_cast<int64_t>(gridDim.x) * kRgWarps;
+    const bool ln = a.mode == QKN_LN_PER_HEAD;
+    auto locate = [&](int64_t it, T*& row, int& head, bool& isq, int& pos) {
+        isq = it < q_items;
+        const int64_t local = isq ? it : it - q_items;
+        const int64_t plane = local / rblocks;
+        const int rb = static_cast<int>(local - plane * rblocks);
+        const int nh = isq ? a.H : a.Hk;
+        head = static_cast<int>(plane % nh);
+        pos = rb * 8 + r;
+        row = static_cast<T*>(isq ? a.q : a.k) + (plane * a.S + pos) * D + sub * 8 * VL;
+    };
+    int64_t it = static_cast<int64_t>(blockIdx.x) * kRgWarps + (threadIdx.x >> 5);
+    uint4 nxt[VL];
+    T* nrow = nullptr;
+    int nhead = 0, npos = 0;
+    bool nisq = true;
+    if (it < items) {
+        locate(it, nrow, nhead, nisq, npos);
+#pragma unroll
+        for (int v = 0; v < VL; ++v)
+            nxt[v] = npos < a.S ? reinterpret_cast<const uint4*>(nrow)[v] : make_uint4(0, 0, 0, 0);
+    }
+    for (; it < items; it += wstep) {
+        uint4 cur[VL];
+#pragma unroll
+        for (int v = 0; v < VL; ++v) cur[v] = nxt[v];
+        T* row = nrow;
+        const int head = nhead, pos = npos;
+        const bool isq = nisq;
+        if (it + wstep < items) {
+            locate(it + wstep, nrow, nhead, nisq, npos);
+#pragma unroll
+            for (int v = 0; v < VL; ++v)
+                nxt[v] = npos < a.S ? reinterpret_cast<const uint4*>(nrow)[v]
+                                    : make_uint4(0, 0, 0, 0);
+        }
+        float x[8 * VL];
+#pragma unroll
+        for (int v = 0; v < VL; ++v) {
+            const uint32_t w[4] = {cur[v].x, cur[v].y, cur[v].z, cur[v].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = dt_traits<T>::unpack2(w[e]);
+                x[v * 8 + 2 * e] = f.x;
+                x[v * 8 + 2 * e + 1] = f.y;
+            }
+        }
+        const int col0 = sub * 8 * VL;
+        const T* bias = static_cast<const T*>(isq ? a.q_bias : a.k_bias);
+        if (bias) {
+#pragma unroll
+            for (int v = 0; v < VL; ++v) {
+                float b[8];
+                load8(bias + head * D + col0 + v * 8, b);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[v * 8 + e] += b[e];
+            }
+        }
+        if (ln) {
+            float s1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8 * VL; ++e) s1 += x[e];
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+            const float mean = s1 * (1.0f / D);
+            float s2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8 * VL; ++e) {
+                const float c = x[e] - mean;
+                s2 = fmaf(c, c, s2);
+            }
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+            const float rstd = rsqrtf(s2 * (1.0f / D) + a.eps);
+            const T* gam = static_cast<const T*>(isq ? a.q_w : a.k_w) + head * D + col0;
+#pragma unroll
+            for (int v = 0; v < VL; ++v) {
+                float gv[8];
+                load8(gam + v * 8, gv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[v * 8 + e] = (x[v * 8 + e] - mean) * rstd * gv[e];
+            }
+        }
+        if constexpr (kPairs > 0) {
+            // the row's lanes each compute every 4th (cos, sin) pair
+            constexpr int kPer = (kPairs + 3) / 4;
+            float cs[kPer], sn[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int j = i * 4 + sub;
+                cs[i] = 1.f;
+                sn[i] = 0.f;
+                if (j < kPairs) rope_cos_sin(rp, pos, j, cs[i], sn[i]);
+            }
+#pragma unroll
+            for (int j = 0; j < kPairs; ++j) {
+                const int src = (lane & ~3) | (j & 3);
+                const float c = __shfl_sync(0xffffffffu, cs[j >> 2], src);
+                const float sv = __shfl_sync(0xffffffffu, sn[j >> 2], src);
+                if (sub == 0) {
+                    const float x1 = x[j], x2 = x[j + kPairs];
+                    x[j] = x1 * c - x2 * sv;
+                    x[j + kPairs] = x2 * c + x1 * sv;
+                }
+            }
+        }
+        if (pos < a.S) {
+#pragma unroll
+            for (int v = 0; v < VL; ++v)
+                store8(row + v * 8, *reinterpret_cast<const float(*)[8]>(&x[v * 8]));
+        }
+    }
+}
+
+template <typename T>
+bool launch_rowgroup_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
+    if (a.d != 160 || a.mode == QKN_RMS_FULL || a.num_sms <= 0) return false;
+    const int64_t items = static_cast<int64_t>(a.B) * (a.H + a.Hk) * ((a.S + 7) / 8);
+    if (items > (static_cast<int64_t>(1) << 40)) return false;
+    auto kern = rp.span == 0 ? qk_rowgroup_kernel<T, 0>
+              : rp.span == 16 ? qk_rowgroup_kernel<T, 16>
+              : rp.span == 32 ? qk_rowgroup_kernel<T, 32>
+              : rp.span == 40 ? qk_rowgroup_kernel<T, 40> : nullptr;
+    if (!kern) return false;
+    // persistent: as many blocks as are resident at once
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRgWarps * 32, 0) !=
+            cudaSuccess || per_sm <= 0)
+        per_sm = 1;
+    int64_t blocks = (items + kRgWarps - 1) / kRgWarps;
+    const int64_t cap = static_cast<int64_t>(per_sm) * a.num_sms;
+    if (blocks > cap) blocks = cap;
+    kern<<<static_cast<unsigned>(blocks), kRgWarps * 32, 0, s>>>(a, rp);
+    return true;
+}
+
 template <typename T>
 bool launch_warp_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
     const int vph = a.d / 8;
@@ -709,6 +869,9 @@ cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopePar
     if (tokens == 0) return cudaSuccess;
     if (dt == DType::F16 ? launch_unit_path<__half>(a, rp, s)
                          : launch_unit_path<__nv_bfloat16>(a, rp, s))
+        return cudaGetLastError();
+    if (dt == DType::F16 ? launch_rowgroup_path<__half>(a, rp, s)
+                         : launch_rowgroup_path<__nv_bfloat16>(a, rp, s))
         return cudaGetLastError();
     if (dt == DType::F16 ? launch_warp_path<__half>(a, rp, s)
                          : launch_warp_path<__nv_bfloat16>(a, rp, s))
