@@ -684,21 +684,21 @@ bool launch_head_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_
     return true;
 }
 
-// Row-group path at head_dim 160 (StableLM-2-12B): bias, per-head LayerNorm
-// (or none) and rotary over the first ROT <= 40 dims, in place. A plane
-// (b, head) of q or k is [S, 160] contiguous, so 8 consecutive rows are
-// 2560 contiguous bytes: one warp takes them, 4 lanes per row and 40
-// elements (five 16-byte vectors) per lane, every access a whole line of
-// the warp's block. The row statistics are two shuffle steps over a row's
-// 4 lanes. The rotary span lies within each row's first lane (dims 0..39):
-// the row's 4 lanes compute 5 of its ROT/2 (cos, sin) pairs each and hand
-// them to the first lane by shuffle. Persistent warps over blocks, the next
-// block's rows loaded before this one is computed.
+// Row-group path at head_dim D = 64, 128 or 160 (StableLM-2-12B's 160, the
+// attention sweep's 64): bias, per-head LayerNorm (or none) and rotary over
+// the first ROT <= D/4 dims, in place. A plane (b, head) of q or k is [S, D]
+// contiguous, so 8 consecutive rows are 16 D contiguous bytes: one warp takes
+// them, 4 lanes per row and D/4 elements (D/32 16-byte vectors) per lane.
+// The row statistics are two shuffle steps over a row's 4 lanes. The rotary
+// span lies within each row's first lane: the row's 4 lanes compute every
+// 4th of its ROT/2 (cos, sin) pairs and hand them to the first lane by
+// shuffle. Persistent warps over blocks, the next block's rows loaded before
+// this one is computed.
 constexpr int kRgWarps = 8;
-template <typename T, int ROT>
+template <typename T, int D, int ROT>
 __global__ void __launch_bounds__(kRgWarps * 32) qk_rowgroup_kernel(QkNormRopeArgs a,
                                                                     RopeParams rp) {
-    constexpr int D = 160, VL = 5;  // vectors per lane
+    constexpr int VL = D / 32;  // 16-byte vectors per lane
     constexpr int kPairs = ROT / 2;
     static_assert(ROT % 2 == 0 && ROT <= 8 * VL, "the rotary span must lie in a row's first lane");
     const int lane = threadIdx.x & 31;
@@ -824,13 +824,24 @@ __global__ void __launch_bounds__(kRgWarps * 32) qk_rowgroup_kernel(QkNormRopeAr
 
 template <typename T>
 bool launch_rowgroup_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s) {
-    if (a.d != 160 || a.mode == QKN_RMS_FULL || a.num_sms <= 0) return false;
+    if (a.mode == QKN_RMS_FULL || a.num_sms <= 0) return false;
     const int64_t items = static_cast<int64_t>(a.B) * (a.H + a.Hk) * ((a.S + 7) / 8);
     if (items > (static_cast<int64_t>(1) << 40)) return false;
-    auto kern = rp.span == 0 ? qk_rowgroup_kernel<T, 0>
-              : rp.span == 16 ? qk_rowgroup_kernel<T, 16>
-              : rp.span == 32 ? qk_rowgroup_kernel<T, 32>
-              : rp.span == 40 ? qk_rowgroup_kernel<T, 40> : nullptr;
+    using K = void (*)(QkNormRopeArgs, RopeParams);
+    K kern = nullptr;
+    if (a.d == 64) {
+        kern = rp.span == 0 ? qk_rowgroup_kernel<T, 64, 0>
+             : rp.span == 16 ? qk_rowgroup_kernel<T, 64, 16> : nullptr;
+    } else if (a.d == 128) {
+        kern = rp.span == 0 ? qk_rowgroup_kernel<T, 128, 0>
+             : rp.span == 16 ? qk_rowgroup_kernel<T, 128, 16>
+             : rp.span == 32 ? qk_rowgroup_kernel<T, 128, 32> : nullptr;
+    } else if (a.d == 160) {
+        kern = rp.span == 0 ? qk_rowgroup_kernel<T, 160, 0>
+             : rp.span == 16 ? qk_rowgroup_kernel<T, 160, 16>
+             : rp.span == 32 ? qk_rowgroup_kernel<T, 160, 32>
+             : rp.span == 40 ? qk_rowgroup_kernel<T, 160, 40> : nullptr;
+    }
     if (!kern) return false;
     // persistent: as many blocks as are resident at once
     int per_sm = 0;
@@ -867,11 +878,11 @@ cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopePar
                                 cudaStream_t s) {
     const int64_t tokens = static_cast<int64_t>(a.B) * a.S;
     if (tokens == 0) return cudaSuccess;
-    if (dt == DType::F16 ? launch_unit_path<__half>(a, rp, s)
-                         : launch_unit_path<__nv_bfloat16>(a, rp, s))
-        return cudaGetLastError();
     if (dt == DType::F16 ? launch_rowgroup_path<__half>(a, rp, s)
                          : launch_rowgroup_path<__nv_bfloat16>(a, rp, s))
+        return cudaGetLastError();
+    if (dt == DType::F16 ? launch_unit_path<__half>(a, rp, s)
+                         : launch_unit_path<__nv_bfloat16>(a, rp, s))
         return cudaGetLastError();
     if (dt == DType::F16 ? launch_warp_path<__half>(a, rp, s)
                          : launch_warp_path<__nv_bfloat16>(a, rp, s))
