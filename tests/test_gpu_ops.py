@@ -125,6 +125,11 @@ QKV_CASES = {
     "ln_per_head_d128_r32": (1, 140, 256, 4, 2, 128, "stacked", "ln_per_head", 32, 1e4, True),
     "rms_full_d64_r16_gqa": (2, 100, 256, 8, 2, 64, "stacked", "rms_full", 16, 1e4, False),
     "rms_full_d96_r24": (1, 90, 192, 2, 2, 96, "stacked", "rms_full", 24, 1e4, True),
+    # the position-block path: bias, a partial span, 32 query heads (8 units
+    # per thread) beside 8 kv heads, ragged last block
+    "rms_full_d128_r64_bias": (1, 77, 256, 4, 4, 128, "stacked", "rms_full", 64, 1e4, True),
+    "rms_full_h32_d128_bias": (1, 43, 256, 32, 8, 128, "stacked", "rms_full", 128, 5e5, True),
+    "rms_full_d64_r0": (2, 33, 256, 4, 2, 64, "stacked", "rms_full", 0, 1e4, False),
     "ln_per_head_d96_r24_bias": (1, 90, 192, 2, 1, 96, "stacked", "ln_per_head", 24, 1e4, True),
 }
 
