@@ -20,7 +20,9 @@
 //   warp 0      TMA: the item's Q tile (G boxes of R rows per 64-column
 //               slice), then K tiles one ahead of V tiles (each 128 keys,
 //               128-byte swizzle, zero fill past S), K and V in rings of
-//               their own
+//               their own; K and V load with an evict-last L2 policy (other
+//               position blocks of the group read the same key prefix), Q
+//               evict-first
 //   warp 1      TMEM allocator and single-thread MMA issuer, in the order
 //               S(0), S(1), PV(0), S(2), PV(1), ...: S is double-buffered in
 //               TMEM, so the next tile's scores are computed while the
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            const uint64_t pol_kv = l2_evict_last_policy(), pol_q = l2_evict_first_policy();
             GqaCursor c;
             c.start(a, pk, nblk, n_items);
             int gk = 0, gv = 0;  // K and V tiles loaded so far (ring positions)
@@ -189,8 +192,8 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
                 mbar_expect_tx(k_full(st), Cfg::kTileBytes);
 #pragma unroll
                 for (int sub = 0; sub < Cfg::kSub; ++sub)
-                    tma_load_3d(sK + st * Cfg::kTileBytes + sub * kTK * 128, &tmK, k_full(st),
-                                sub * 64, j * kTK, c.b * a.Hk + c.g);
+                    tma_load_3d_hint(sK + st * Cfg::kTileBytes + sub * kTK * 128, &tmK, k_full(st),
+                                sub * 64, j * kTK, c.b * a.Hk + c.g, pol_kv);
                 ++gk;
                 return true;
             };
@@ -200,8 +203,8 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
                 mbar_expect_tx(v_full(st), Cfg::kTileBytes);
 #pragma unroll
                 for (int sub = 0; sub < Cfg::kSub; ++sub)
-                    tma_load_3d(sV + st * Cfg::kTileBytes + sub * kTK * 128, &tmV, v_full(st),
-                                sub * 64, j * kTK, c.b * a.Hk + c.g);
+                    tma_load_3d_hint(sV + st * Cfg::kTileBytes + sub * kTK * 128, &tmV, v_full(st),
+                                sub * 64, j * kTK, c.b * a.Hk + c.g, pol_kv);
                 ++gv;
                 return true;
             };
@@ -216,9 +219,9 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
                 for (int i = 0; i < nh; ++i) {
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d(sQ + qb * Cfg::kTileBytes + sub * kTQ * 128 + i * R * 128,
+                        tma_load_3d_hint(sQ + qb * Cfg::kTileBytes + sub * kTQ * 128 + i * R * 128,
                                     &tmQ, q_full(qb), sub * 64, c.p0,
-                                    c.b * a.H + c.g * G + c.hc * pk.Gt + i);
+                                    c.b * a.H + c.g * G + c.hc * pk.Gt + i, pol_q);
                 }
                 // consumption order: K(0), then K(j+1) ahead of V(j)
                 ok = load_k(0);

@@ -14,7 +14,9 @@
 // thread, in that order). 12 warps:
 //   warp 0      TMA: both Q tiles of an item (double-buffered across items),
 //               then K and V tiles of 128 keys into a four-stage ring
-//               (128-byte swizzle, 64-column boxes, zero fill past S).
+//               (128-byte swizzle, 64-column boxes, zero fill past S). K
+//               and V load with an evict-last L2 policy (the head's other
+//               query-tile pairs read the same key prefix), Q evict-first.
 //   warps 1, 2  one MMA-issuing thread per query tile (M=128, K=16 per
 //               instruction): S (N=128) from Q and K in shared memory, PV
 //               (N=64) from P in TMEM and V in shared memory (V MN-major).
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         setmaxnreg_dec<kRegsControl>();
     if (warp == 0) {
         if (lane == 0) {
+            const uint64_t pol_kv = l2_evict_last_policy(), pol_q = l2_evict_first_policy();
             PairCursor c;
             c.start(a, nq, np, n_items);
             int gkv = 0;  // K/V tiles loaded so far (ring position)
@@ -199,8 +202,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 for (int x = 0; x < (c.nB ? 2 : 1); ++x) {
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d(sQ + (2 * qb + x) * Cfg::kQBytes + sub * kTQ * 128, &tmQ,
-                                    q_full(qb), sub * 64, (2 * c.i + x) * kTQ, c.b * a.H + c.h);
+                        tma_load_3d_hint(sQ + (2 * qb + x) * Cfg::kQBytes + sub * kTQ * 128, &tmQ,
+                                    q_full(qb), sub * 64, (2 * c.i + x) * kTQ, c.b * a.H + c.h, pol_q);
                 }
                 const int nkv = c.n_kv();
                 for (int j = 0; j < nkv; ++j, ++gkv) {
@@ -214,8 +217,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     mbar_expect_tx(k_full(st), Cfg::kKVBytes);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
-                                    c.b * a.Hk + c.g);
+                        tma_load_3d_hint(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
+                                    c.b * a.Hk + c.g, pol_kv);
                     if (!mbar_wait_inl(v_empty(st), ph ^ 1u, a.err)) {
                         ok = false;
                         break;
@@ -223,8 +226,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     mbar_expect_tx(v_full(st), Cfg::kKVBytes);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d(sK + Cfg::kKVBytes + sub * kTK * 128, &tmV, v_full(st),
-                                    sub * 64, j * kTK, c.b * a.Hk + c.g);
+                        tma_load_3d_hint(sK + Cfg::kKVBytes + sub * kTK * 128, &tmV, v_full(st),
+                                    sub * 64, j * kTK, c.b * a.Hk + c.g, pol_kv);
                 }
                 c.next(a, nq, np, n_items);
             }

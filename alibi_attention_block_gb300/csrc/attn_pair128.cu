@@ -15,7 +15,9 @@
 //   warp 0      TMA: each query tile's Q (its own buffer, reloaded once the
 //               tile's last QK^T of the item has completed), K and V tiles of
 //               128 keys into a two-stage ring (128-byte swizzle, 64-column
-//               boxes, zero fill past S).
+//               boxes, zero fill past S). K and V load with an evict-last L2
+//               policy (the head's other query-tile pairs read the same key
+//               prefix), Q evict-first.
 //   warp 1      TMEM allocator and MMA issuer: S (M=128, N=128, K=128: Q and
 //               K K-major in shared memory), PV (N=128: P from TMEM, V
 //               MN-major).
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(kP128Threads, 1)
     if (warp < 4) {
         setmaxnreg_dec<kRegsControl>();
         if (warp == 0 && lane == 0) {
+            const uint64_t pol_kv = l2_evict_last_policy(), pol_q = l2_evict_first_policy();
             PairCursor c;
             c.start(a, nq, np, n_items);
             int gkv = 0;
@@ -168,8 +171,8 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                     mbar_expect_tx(q_full(x), Cfg::kQBytes);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d(sQ + x * Cfg::kQBytes + sub * kTQ * 128, &tmQ, q_full(x),
-                                    sub * 64, (2 * c.i + x) * kTQ, c.b * a.H + c.h);
+                        tma_load_3d_hint(sQ + x * Cfg::kQBytes + sub * kTQ * 128, &tmQ, q_full(x),
+                                    sub * 64, (2 * c.i + x) * kTQ, c.b * a.H + c.h, pol_q);
                     ++itq[x];
                 }
                 const int nkv = c.n_kv();
@@ -184,8 +187,8 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                     mbar_expect_tx(k_full(st), Cfg::kKVBytes);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
-                                    c.b * a.Hk + c.g);
+                        tma_load_3d_hint(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
+                                    c.b * a.Hk + c.g, pol_kv);
                     if (!mbar_wait_inl(v_empty(st), ph ^ 1u, a.err)) {
                         ok = false;
                         break;
@@ -193,8 +196,8 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                     mbar_expect_tx(v_full(st), Cfg::kKVBytes);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d(sK + Cfg::kKVBytes + sub * kTK * 128, &tmV, v_full(st),
-                                    sub * 64, j * kTK, c.b * a.Hk + c.g);
+                        tma_load_3d_hint(sK + Cfg::kKVBytes + sub * kTK * 128, &tmV, v_full(st),
+                                    sub * 64, j * kTK, c.b * a.Hk + c.g, pol_kv);
                 }
                 c.next(a, nq, np, n_items);
             }
