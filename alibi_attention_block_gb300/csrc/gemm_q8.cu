@@ -14,16 +14,20 @@
 //
 // The GEMM (A bf16/fp16 [M, K], both operands K-major) is the K2 kernel with
 // its B operand built on chip: TMA brings the A tile, the int8 code tile and
-// the fp16 scales of one 64-wide k-block into a 3-stage ring; four converter
-// warps expand the codes to the storage type (q * d exactly in fp32, one
-// rounding to the storage type) and write them in the 128-byte-swizzled
-// K-major layout the MMA reads, into a 2-stage ring of B tiles. 14 warps:
+// the fp16 scales of one 64-wide k-block into a 3-stage ring; eight
+// converter warps expand the codes to the storage type (q * d exactly in
+// fp32, one rounding to the storage type) and write them in the
+// 128-byte-swizzled K-major layout the MMA reads, into a 2-stage ring of B
+// tiles. The conversion, not the tensor core, sets the pace: eight converter
+// warps (two per scheduler) measured 6-11% faster than four with eight
+// epilogue warps. 14 warps:
 //   warp 0       TMA producer (A, codes, scales)
 //   warp 1       TMEM allocator and single-thread MMA issuer (M=128, N=256,
 //                K=16, fp32 accumulators double-buffered in TMEM)
-//   warps 2..9   epilogue (the K2 epilogues: bias, residuals, SwiGLU, GELU,
-//                QKV scatter with rotary)
-//   warps 10..13 converters
+//   warps 2..5   epilogue (the K2 epilogues: bias, residuals, SwiGLU, GELU,
+//                QKV scatter with rotary), each warp both column halves of
+//                its TMEM lane quarter
+//   warps 6..13  converters
 // Weight bytes per output element fall from 2 to 1 + 1/16 (codes + scales).
 #include "gemm_epi.cuh"
 
@@ -34,8 +38,9 @@ namespace {
 using namespace gemm;
 
 constexpr int kQBN = 256;                  // B tile rows (output columns, or gate|up rows)
-constexpr int kConvWarps = 4;
-constexpr int kQ8Threads = 64 + 32 * kEpiWarps + 32 * kConvWarps;
+constexpr int kConvWarps = 8;
+constexpr int kQ8EpiWarps = 4;  // each takes both column halves of its lane quarter
+constexpr int kQ8Threads = 64 + 32 * kQ8EpiWarps + 32 * kConvWarps;
 constexpr int kTmaStages = 3;
 constexpr int kBStages = 2;
 constexpr int kABytes = kBM * kBK * 2;            // 16 KB
@@ -46,7 +51,7 @@ constexpr int kBTileBytes = kQBN * kBK * 2;       // 32 KB, 128-byte swizzled
 constexpr int kOffB = kTmaStages * kTmaStageBytes;
 constexpr int kOffBar = kOffB + kBStages * kBTileBytes;
 constexpr int kOffEpi = kOffBar + 256;
-constexpr int kQ8Smem = kOffEpi + kEpiWarps * 32 * 128 + 1024;
+constexpr int kQ8Smem = kOffEpi + kQ8EpiWarps * 32 * 128 + 1024;
 static_assert(kScaleBytes <= 1024, "scales exceed their slot");
 static_assert(kTmaStageBytes % 1024 == 0 && kOffB % 1024 == 0, "tiles must stay 1 KB aligned");
 
@@ -120,7 +125,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull(i), 1);
-            mbar_init(tempty(i), kEpiWarps);
+            mbar_init(tempty(i), kQ8EpiWarps);
         }
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
@@ -222,10 +227,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 if (ok) tc_commit(tfull(acc));
             }
         }
-    } else if (warp < 2 + kEpiWarps) {
+    } else if (warp < 2 + kQ8EpiWarps) {
         const int ew = warp - 2;
         const int quarter = warp & 3;
-        const int half = ew / 4;
         const int row = quarter * 32 + lane;
         const uint32_t stg0 = sbase + kOffEpi;
         int it = 0;
@@ -237,17 +241,20 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
             tile_of(u, mt, nt);
             const uint32_t tbase =
                 tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-            epilogue_tile<T, BN, EPI, ROT, false>(g, rp, tbase, mt * kBM + row, nt,
-                                                  stg0 + ew * (32 * 128), lane,
-                                                  mt * kBM + quarter * 32, nullptr, 0, row, half);
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half)
+                epilogue_tile<T, BN, EPI, ROT, false>(g, rp, tbase, mt * kBM + row, nt,
+                                                      stg0 + ew * (32 * 128), lane,
+                                                      mt * kBM + quarter * 32, nullptr, 0, row,
+                                                      half);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(acc));
         }
     } else {
-        // converters: 1024 16-byte chunks of codes per k-block, 8 per thread;
+        // converters: 1024 16-byte chunks of codes per k-block, 4 per thread;
         // a warp's 32 chunks are 8 rows x 64 contiguous bytes
-        const int tid = threadIdx.x - (64 + 32 * kEpiWarps);
+        const int tid = threadIdx.x - (64 + 32 * kQ8EpiWarps);
         int st = 0, bs = 0;
         uint32_t ph = 0, bph = 0;
         bool ok = true;
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
                 const uint32_t sd = sq + kCodeBytes;
                 const uint32_t sb = sbase + kOffB + bs * kBTileBytes;
                 // all of this thread's loads first, then the arithmetic and
-                // stores: one converter warp per scheduler has nothing else to
+                // stores: two converter warps per scheduler have little else to
                 // hide shared-memory latency behind
                 constexpr int kIters = (BN * kBK / 16) / (32 * kConvWarps);
                 const int c16 = tid & 3;   // 16 codes: k = 16 c16 .. 16 c16 + 15
