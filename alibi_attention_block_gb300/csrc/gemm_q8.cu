@@ -14,7 +14,7 @@
 //
 // The GEMM (A bf16/fp16 [M, K], both operands K-major) is the K2 kernel with
 // its B operand built on chip: TMA brings the A tile, the int8 code tile and
-// the fp16 scales of one 64-wide k-block into a 3-stage ring; eight
+// the fp16 scales of one 64-wide k-block into a 4-stage ring; eight
 // converter warps expand the codes to the storage type (q * d exactly in
 // fp32, one rounding to the storage type) and write them in the
 // 128-byte-swizzled K-major layout the MMA reads, into a 2-stage ring of B
@@ -41,7 +41,7 @@ constexpr int kQBN = 256;                  // B tile rows (output columns, or ga
 constexpr int kConvWarps = 8;
 constexpr int kQ8EpiWarps = 4;  // each takes both column halves of its lane quarter
 constexpr int kQ8Threads = 64 + 32 * kQ8EpiWarps + 32 * kConvWarps;
-constexpr int kTmaStages = 3;
+constexpr int kTmaStages = 4;
 constexpr int kBStages = 2;
 constexpr int kABytes = kBM * kBK * 2;            // 16 KB
 constexpr int kCodeBytes = kQBN * kBK;            // 16 KB of int8 codes
