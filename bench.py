@@ -696,16 +696,16 @@ class _Block:
 
 
 def _time_steps(bl, args, flush, stream, dist, sampler_index, steps, warmup):
-    """W warm-up forwards of one workload, then two passes of K forwards, L2
-    flushed before each. Pass 1 is the timed region: a CUDA event at each
-    step's two ends only, bracketed by a barrier and a synchronize, with the
-    clocks sampled during it. Pass 2 runs the same K steps with an event
-    recorded by the library after every launch (on the launching stream), for
-    the per-kernel times. The step times come from pass 1 because those
-    intermediate records are not free: on GB300 each adds about 1.6 us to the
-    step (StableLM-2-1.6B block: 649.7 us with them, 638.2 without).
-    Returns the per-kernel means (pass 2), the per-step times of both passes,
-    the clocks and pass 1's wall time."""
+    """W warm-up forwards of one workload, then K timed steps, L2 flushed
+    before every forward. Each timed step is a forward with a CUDA event at
+    its two ends only, followed by the same forward with an event recorded by
+    the library after every launch (on the launching stream) for the
+    per-kernel times. The step times come from the first kind because the
+    intermediate records are not free: on GB300 each adds about 1.6 us to
+    the step (StableLM-2-1.6B block: 649.7 us with them, 638.2 without). The
+    region is bracketed by a barrier and a synchronize, with the clocks
+    sampled during it. Returns the per-kernel means, the per-step times of
+    both kinds, the clocks and the region's wall time."""
     import alibi_attention_block_gb300 as blk
     from alibi_attention_block_gb300 import _abi
     for _ in range(warmup):
@@ -742,7 +742,10 @@ def _time_steps(bl, args, flush, stream, dist, sampler_index, steps, warmup):
     else:
         n_launch = bl.nl.value
         step_names = [_abi.STEP_NAMES[bl.kinds[i]] for i in range(n_launch)]
-    # pass 1: the timed region
+    # the timed region: K steps timed at their two ends, each followed by
+    # the same step with per-launch events, so that both see the same clocks
+    # and power state (a pass of each, one after the other, drifted apart by
+    # 8% on the heaviest block)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -757,20 +760,16 @@ def _time_steps(bl, args, flush, stream, dist, sampler_index, steps, warmup):
             else:
                 bl.step(stream, None)
             ends[i][1].record(stream)
+            flush.zero_()
+            if graph is not None:
+                graph.launch(evs[i])
+            else:
+                bl.step(stream, evs[i])
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
         clk.mark_end()
     if dist:
         dist.barrier()
-    blk.check_device_status()
-    # pass 2: the same steps with per-launch events
-    for i in range(steps):
-        flush.zero_()
-        if graph is not None:
-            graph.launch(evs[i])
-        else:
-            bl.step(stream, evs[i])
-    torch.cuda.synchronize()
     blk.check_device_status()
     step_ms = [a.elapsed_time(b) for a, b in ends]
     step_ms_ev = [e[0].elapsed_time(e[n_launch]) for e in evs]
@@ -915,7 +914,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
     for v in standalone.values():
         v["frac_of_measured_hbm"] = v["gbs"] / peaks["hbm_gbs"]
     ms_ev = float(np.mean(r["step_ms_launch_events"]))
-    rep = _report(cfg, kernel_ms, ms_per_step, sum(r["step_ms"]) / 1e3, peaks, spec, ms_ev)
+    rep = _report(cfg, kernel_ms, ms_per_step, r["t_wall"], peaks, spec, ms_ev)
     cpu = None if args.no_cpu_baseline else _cpu_baseline(cfg, args.cpu_budget)
     provenance = _safe_provenance(cfg, x_cpu, w_cpu, dev)
     e2e_bytes_in, e2e_bytes_out = x.numel() * x.element_size(), y.numel() * y.element_size()
@@ -934,7 +933,7 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
             r2 = _time_steps(b2, args, flush, stream, None, local_rank, args.steps, args.warmup)
             ms2 = float(sum(r2["step_ms"])) / args.steps
             ms2_ev = float(np.mean(r2["step_ms_launch_events"]))
-            rep2 = _report(c, r2["kernel_ms"], ms2, sum(r2["step_ms"]) / 1e3, peaks, spec, ms2_ev)
+            rep2 = _report(c, r2["kernel_ms"], ms2, r2["t_wall"], peaks, spec, ms2_ev)
             others[name] = {
                 "config": dict(_config(c, "flushed before every step (512 MiB write)"),
                                weights="Q8_0 (int8 codes, fp16 scales per 32 inputs)" if q8
@@ -962,9 +961,9 @@ def run_ours(args, cfg, rank, world, local_rank, dist):
         "block_tflops": rep["block_tflops"],
         "attention": rep["attention"],
         "kernels": rep["kernels"],
-        "kernel_times": ("a second pass of the same steps with a CUDA event after every launch; "
-                         "its step time, %.4f ms, exceeds the timed pass's by the event records"
-                         % ms_ev),
+        "kernel_times": ("each timed step is followed by the same step with a CUDA event after "
+                         "every launch; those steps take %.4f ms, more than the timed ones by "
+                         "the event records" % ms_ev),
         "roofline": rep["roofline"],
         "spec_peak": spec,
         "cpu_baseline": cpu,
