@@ -1321,6 +1321,9 @@ struct blk_host_pipe {
     cudaEvent_t ev_in[kMaxPipeDepth] = {}, ev_fwd[kMaxPipeDepth] = {}, ev_out[kMaxPipeDepth] = {};
     int64_t n = 0;            // submits since create or the last flush
     cudaStream_t s = nullptr;  // their stream
+    // slot k's forward as a CUDA graph, and the weight pointers it reads
+    blk_graph* g[kMaxPipeDepth] = {};
+    blk_block_weights gw[kMaxPipeDepth] = {};
 };
 
 namespace {
@@ -1335,6 +1338,8 @@ blk_status pipe_release(blk_host_pipe* p) {
         if (first == cudaSuccess && e != cudaSuccess) first = e;
     };
     for (int k = 0; k < kMaxPipeDepth; ++k) {
+        if (p->g[k] && blk_graph_destroy(p->g[k]) != BLK_OK && first == cudaSuccess)
+            first = cudaErrorUnknown;
         if (p->ev_in[k]) keep(cudaEventDestroy(p->ev_in[k]));
         if (p->ev_fwd[k]) keep(cudaEventDestroy(p->ev_fwd[k]));
         if (p->ev_out[k]) keep(cudaEventDestroy(p->ev_out[k]));
@@ -1434,7 +1439,20 @@ blk_status blk_host_pipe_submit(blk_host_pipe* p, const blk_block_weights* w, co
     e = cudaStreamWaitEvent(cs, p->ev_in[k], 0);
     if (e == cudaSuccess && p->n >= p->depth) e = cudaStreamWaitEvent(cs, p->ev_out[k], 0);
     if (e != cudaSuccess) return cuda_fail(e, "stream ordering");
-    st = blk_forward(&p->d, w, p->x_dev[k], p->y_dev[k], p->ws, p->ws_bytes, p->dt, s);
+    // the forward: slot k's graph, recorded on its first use and again when
+    // the weight pointers differ from the recorded ones
+    if (!p->g[k] || std::memcmp(&p->gw[k], w, sizeof(*w)) != 0) {
+        if (p->g[k]) {
+            st = blk_graph_destroy(p->g[k]);
+            p->g[k] = nullptr;
+            if (st != BLK_OK) return st;
+        }
+        st = blk_forward_graph_create(&p->d, w, p->x_dev[k], p->y_dev[k], p->ws, p->ws_bytes,
+                                      p->dt, nullptr, 0, nullptr, nullptr, &p->g[k]);
+        if (st != BLK_OK) return st;
+        p->gw[k] = *w;
+    }
+    st = blk_graph_launch(p->g[k], s);
     if (st != BLK_OK) return st;
     e = cudaEventRecord(p->ev_fwd[k], cs);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->copy_out, p->ev_fwd[k], 0);

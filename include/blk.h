@@ -422,7 +422,11 @@ blk_status blk_model_forward(const blk_model_desc* d, const blk_model_weights* w
  *  - y_host of a batch is complete once s has passed a later
  *    blk_host_pipe_flush.
  * All submits between two flushes use the same stream s (BLK_EINVAL
- * otherwise). The pipe is not thread-safe. dev_mem (blk_host_pipe_mem_size
+ * otherwise). Each slot's forward is recorded as a CUDA graph on the slot's
+ * first submit (and again when the weight pointers differ from the ones it
+ * was recorded with) and replayed by later submits; the graph reads the
+ * weights through those pointers, so their contents may change between
+ * submits. The pipe is not thread-safe. dev_mem (blk_host_pipe_mem_size
  * bytes, 16-byte aligned, caller-owned) holds the staging slots and the
  * forward's workspace; it must stay valid until the submitted work has
  * completed. destroy does not wait for that work. */

@@ -211,24 +211,30 @@ def test_host_pipe_matches_device_forward(name, depth):
     """Five batches through a host pipe (copies of one batch overlapping the
     neighbouring batches' forwards, staging slots reused): each y_host equals
     blk_forward on that batch bit for bit, and a second round after a flush
-    still does."""
+    still does (the slots' recorded graphs replayed). A third round with
+    other weight tensors (one projection halved) follows those weights: the
+    slots record their forwards again."""
     cfg = SMALL[name]
     x, w = workloads.block_inputs(cfg)
     wd = {k: to_dev(t) for k, t in w.items()}
+    wd2 = {k: t.clone() for k, t in wd.items()}
+    wd2["w_o"] = (wd2["w_o"].float() * 0.5).to(wd2["w_o"].dtype)
     B, S, _ = x.shape
     xs = [(x.double() * (1.0 - 0.3 * i)).to(x.dtype) for i in range(5)]
     refs = [blk.forward(cfg, wd, to_dev(xi)).cpu() for xi in xs]
+    refs2 = [blk.forward(cfg, wd2, to_dev(xi)).cpu() for xi in xs]
     pipe = blk.HostPipe(cfg, B, S, dtype=x.dtype, depth=depth)
     xh = [xi.pin_memory() for xi in xs]
-    for _ in range(2):
+    for weights, want in ((wd, refs), (wd, refs), (wd2, refs2)):
         yh = [torch.empty_like(xi).pin_memory() for xi in xs]
         for a, b in zip(xh, yh):
-            pipe.submit(wd, a, b)
+            pipe.submit(weights, a, b)
         pipe.flush()
         torch.cuda.current_stream().synchronize()
         blk.check_device_status()
-        for i, (got, ref) in enumerate(zip(yh, refs)):
+        for i, (got, ref) in enumerate(zip(yh, want)):
             assert torch.equal(got, ref), f"batch {i}"
+    assert not torch.equal(refs2[0], refs[0])
     pipe.close()
 
 
