@@ -528,6 +528,8 @@ blk_status run_linear(DType dt, int epi, const void* x, const void* w, const voi
                       const void* bias, const void* r1, const void* r2, void* y, int64_t m,
                       int64_t n, int64_t k, cudaStream_t s, DevState* ds, int f32 = 0,
                       void* split = nullptr, const Q8W* wq = nullptr) {
+    // an fp32 output is written through the LINEAR epilogue only
+    if ((f32 & F32_OUT) && epi != EPI_LINEAR) return BLK_EUNSUPPORTED;
     GemmArgs g{};
     set_split(g, split);
     g.out_f32 = (f32 & F32_OUT) != 0;

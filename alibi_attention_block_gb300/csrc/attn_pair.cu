@@ -77,7 +77,12 @@ struct PairCfg {
     static constexpr int kStages = 4;
     static constexpr int kOffKV = kQBufs * 2 * kQBytes;
     static constexpr int kOffBar = kOffKV + kStages * 2 * kKVBytes;
-    static constexpr int kSmem = kOffBar + 256 + 1024;  // + barriers + alignment slack
+    // ALiBi: per softmax warpgroup an mbarrier (its four warps' arrivals)
+    // and two 128-float tables slope*log2(e)*i (i = key column within a
+    // tile), one per item parity
+    static constexpr int kOffTabBar = kOffBar + 256;
+    static constexpr int kOffBias = kOffTabBar + 16;
+    static constexpr int kSmem = kOffBias + 2 * 2 * kTK * 4 + 1024;  // + alignment slack
     static constexpr uint32_t kColP = 256;              // P_x at kColP + 64 x
     static constexpr uint32_t kColO = 384;              // O_x at kColO + D x
     static constexpr uint32_t kTmemCols = 512;
@@ -126,6 +131,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                      const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
     using Cfg = PairCfg<D>;
     constexpr int kStages = Cfg::kStages;
+    // With ALiBi the key tiles are walked from the diagonal down: the bias
+    // +slope*j is largest there, so the row max is set by the first tile and
+    // the O rescale (max grown past 2^8) stays rare; walked upwards, the max
+    // rises by slope*128*log2(e) per tile, past 2^8 on most tiles for
+    // slopes above 1/23.
+    constexpr bool kRev = ALIBI;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const uint32_t sQ = smem_u32(smem);      // Q[buf][x] at (2 buf + x) tiles
@@ -162,6 +173,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             mbar_init(q_full(x), 1);
             mbar_init(q_empty(x), 2);
         }
+        if (ALIBI)
+            for (int x = 0; x < 2; ++x) mbar_init(sQ + Cfg::kOffTabBar + 8u * x, 4);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(k_full(i), 1);
             mbar_init(v_full(i), 1);
@@ -207,6 +220,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
                 const int nkv = c.n_kv();
                 for (int j = 0; j < nkv; ++j, ++gkv) {
+                    const int kt = kRev ? nkv - 1 - j : j;  // key tile of shared step j
                     const int st = gkv % kStages;
                     const uint32_t ph = (gkv / kStages) & 1;
                     const uint32_t sK = sKV + (2 * st) * Cfg::kKVBytes;
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     mbar_expect_tx(k_full(st), Cfg::kKVBytes);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d_hint(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
+                        tma_load_3d_hint(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, kt * kTK,
                                     c.b * a.Hk + c.g, pol_kv);
                     if (!mbar_wait_inl(v_empty(st), ph ^ 1u, a.err)) {
                         ok = false;
@@ -227,7 +241,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
                         tma_load_3d_hint(sK + Cfg::kKVBytes + sub * kTK * 128, &tmV, v_full(st),
-                                    sub * 64, j * kTK, c.b * a.Hk + c.g, pol_kv);
+                                    sub * 64, kt * kTK, c.b * a.Hk + c.g, pol_kv);
                 }
                 c.next(a, nq, np, n_items);
             }
@@ -286,38 +300,42 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             while (ok && c.valid) {
                 const int qb = c.it & 1;
                 const int nx = x ? c.nB : c.nA, nkv = c.n_kv();
+                // this tile's shared steps [lo, hi): the first nx in key order,
+                // the last nx when the walk runs down from the diagonal
+                const int lo = kRev ? nkv - nx : 0, hi = kRev ? nkv : nx;
+                const int qlast = nx > 0 ? hi - 1 : 0;  // Q_x is released after this step's S
                 if (!mbar_wait_inl(q_full(qb), (c.it >> 1) & 1, a.err)) break;
                 const uint64_t dq = dq0 + (2 * qb) * kQStep;
-                // S of key tile 0
+                // S of step 0
                 {
                     const int st = gkv % kStages;
                     if (!mbar_wait_inl(k_full(st), (gkv / kStages) & 1, a.err)) break;
-                    if (nx > 0 && !issue_s(dq, dk0 + st * kStageStep)) break;
+                    if (lo == 0 && nx > 0 && !issue_s(dq, dk0 + st * kStageStep)) break;
                     tc_commit(k_empty(st));
-                    if (nx <= 1) tc_commit(q_empty(qb));
+                    if (qlast == 0) tc_commit(q_empty(qb));
                 }
                 for (int j = 0; j < nkv; ++j) {
                     const int gj = gkv + j;
                     const int stj = gj % kStages;
                     if (j + 1 < nkv) {
-                        // S of key tile j+1 ahead of PV of tile j
+                        // S of step j+1 ahead of PV of step j
                         const int stn = (gj + 1) % kStages;
                         if (!mbar_wait_inl(k_full(stn), ((gj + 1) / kStages) & 1, a.err)) {
                             ok = false;
                             break;
                         }
-                        if (j + 1 < nx && !issue_s(dq, dk0 + stn * kStageStep)) {
+                        if (j + 1 >= lo && j + 1 < hi && !issue_s(dq, dk0 + stn * kStageStep)) {
                             ok = false;
                             break;
                         }
                         tc_commit(k_empty(stn));
-                        if (j + 2 == nx) tc_commit(q_empty(qb));
+                        if (j + 1 == qlast) tc_commit(q_empty(qb));
                     }
                     if (!mbar_wait_inl(v_full(stj), (gj / kStages) & 1, a.err)) {
                         ok = false;
                         break;
                     }
-                    if (j < nx && !issue_pv(dv0 + stj * kStageStep, j == 0)) {
+                    if (j >= lo && j < hi && !issue_pv(dv0 + stj * kStageStep, j == lo)) {
                         ok = false;
                         break;
                     }
@@ -351,6 +369,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         bool pend = false;  // an item's O is still in TMEM
         float pend_l = 0.f;
         int64_t pend_row = -1;  // output row (b * S + qpos) * H + h, or -1 past S
+        int n_done = 0;         // items this warpgroup has started (ALiBi table parity)
         while (ok && c.valid) {
             const int nx = x ? c.nB : c.nA;
             if (nx == 0) {
@@ -362,12 +381,28 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             float m_used = -INFINITY;  // running max, log2 domain
             float l = 0.f;
             float slope_l2 = 0.f;
+            uint32_t bias_tab = 0;
             if constexpr (ALIBI) {
                 const float slope = a.slopes ? a.slopes[c.h]
                                              : exp2f(-8.0f * static_cast<float>(c.h + 1) /
                                                      static_cast<float>(a.H));
                 slope_l2 = slope * kLog2e;
+                // the item's column bias table, in the buffer the warpgroup's
+                // previous item did not use (its last readers may still be on
+                // that item); each warp's arrival publishes its 32 entries,
+                // and no warp reads before all four have arrived
+                const int off = Cfg::kOffBias + (2 * x + (n_done & 1)) * kTK * 4;
+                reinterpret_cast<float*>(smem + off)[row] = slope_l2 * static_cast<float>(row);
+                bias_tab = sQ + off;
+                const uint32_t tab_bar = sQ + Cfg::kOffTabBar + 8u * x;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tab_bar);
+                if (!mbar_wait_inl(tab_bar, n_done & 1, a.err)) {
+                    ok = false;
+                    break;
+                }
             }
+            ++n_done;
             for (int j = 0; j < nx; ++j, ++g) {
                 if (!mbar_wait_inl(s_full(x), g & 1, a.err)) {
                     ok = false;
@@ -379,15 +414,29 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_free(x));
-                const int kbase = j * kTK;
+                const int kt = kRev ? nx - 1 - j : j;  // key tile of this step
+                const int kbase = kt * kTK;
+                // ALiBi: u = s*scale*log2(e) + slope*log2(e)*i, one paired FMA
+                // per two scores from the column table; the tile's uniform
+                // part slope*log2(e)*kbase joins the max and the exponent
+                const float sk = ALIBI ? slope_l2 * static_cast<float>(kbase) : 0.f;
                 if constexpr (ALIBI) {
-                    const float sk = slope_l2 * static_cast<float>(kbase);
+                    const uint64_t sc2 = f2_pack(scale_l2, scale_l2);
 #pragma unroll
-                    for (int i = 0; i < kTK; ++i)
-                        r[i] = __float_as_uint(fmaf(__uint_as_float(r[i]), scale_l2,
-                                                    fmaf(slope_l2, static_cast<float>(i), sk)));
+                    for (int i = 0; i < kTK; i += 4) {
+                        uint64_t c01, c23;
+                        ld_shared_v2_u64(bias_tab + i * 4, c01, c23);
+                        float u0, u1, u2, u3;
+                        ffma2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), sc2, c01, u0, u1);
+                        ffma2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]), sc2, c23, u2,
+                              u3);
+                        r[i] = __float_as_uint(u0);
+                        r[i + 1] = __float_as_uint(u1);
+                        r[i + 2] = __float_as_uint(u2);
+                        r[i + 3] = __float_as_uint(u3);
+                    }
                 }
-                if (j == qt || kbase + kTK > a.S) {
+                if (kt == qt || kbase + kTK > a.S) {
                     const int lim = min(qpos, a.S - 1) - kbase;  // keys <= lim are visible
 #pragma unroll
                     for (int i = 0; i < kTK; ++i)
@@ -403,6 +452,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 }
                 float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
                 if constexpr (!ALIBI) mx *= scale_l2;  // scale > 0: max commutes with it
+                if constexpr (ALIBI) mx += sk;
                 float corr = 1.f;
                 if (mx > m_used + kRescaleThreshold) {
                     corr = ex2_approx(m_used - mx);
@@ -411,7 +461,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 // p = 2^(logit - m) in the storage type, and the row sum; P is
                 // held in registers until the previous PV has read P_x
                 const uint64_t mul2 = f2_pack(ALIBI ? 1.f : scale_l2, ALIBI ? 1.f : scale_l2);
-                const uint64_t neg2 = f2_pack(-m_used, -m_used);
+                const uint64_t neg2 = f2_pack(sk - m_used, sk - m_used);
                 uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
                 uint32_t pk[kTK / 2];
 #pragma unroll

@@ -213,7 +213,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 if (g.res2_f32) add_row32(static_cast<const float*>(g.res2) + off, o, valid);
                 else add_row32(static_cast<const T*>(g.res2) + off, o, valid);
             }
-            if (g.out_f32)
+            // fp32 output (LINEAR only: the other epilogues' kernels keep no
+            // staging room in shared memory)
+            if (EPI == EPI_LINEAR && g.out_f32)
                 store_chunk_f32(g, stg, lane, m_base, n0, o);  // all lanes (rows checked inside)
             else if (row_ok)
                 store_row32(static_cast<T*>(g.out) + off, o, valid);
