@@ -170,6 +170,15 @@ blk_status report_error_status(blk_status st, const char* fmt, ...) {
     return st;
 }
 
+bool pdl_allowed(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        (void)cudaGetLastError();  // not the launch's error: launch plainly
+        return false;
+    }
+    return st == cudaStreamCaptureStatusNone;
+}
+
 bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uint64_t cols,
                   uint32_t box_rows) {
     auto fn = encode_fn();
@@ -1538,10 +1547,14 @@ blk_status blk_forward_graph_create(const blk_block_desc* d, const blk_block_wei
         if ((e = cudaGraphNodeGetType(node, &type)) != cudaSuccess) break;
         if (type == cudaGraphNodeTypeEventRecord && g->n_events < kMaxForwardEvents)
             g->ev_nodes[g->n_events++] = node;
-        size_t n_next = 0;
-        if ((e = cudaGraphNodeGetDependentNodes(node, nullptr, nullptr, &n_next)) != cudaSuccess) break;
-        if (n_next != 1) break;
-        e = cudaGraphNodeGetDependentNodes(node, &node, nullptr, &n_next);
+        // edges between kernels launched for programmatic dependent launch
+        // carry edge data, which the query must return (it refuses as lossy
+        // otherwise); room for two dependents tells a chain link (one) apart
+        cudaGraphNode_t next[2] = {};
+        cudaGraphEdgeData edge[2] = {};
+        size_t n_next = 2;
+        if ((e = cudaGraphNodeGetDependentNodes(node, next, edge, &n_next)) != cudaSuccess) break;
+        node = n_next == 1 ? next[0] : nullptr;
     }
     if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, graph, 0);
     if (e != cudaSuccess) {

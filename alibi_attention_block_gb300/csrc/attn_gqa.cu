@@ -178,6 +178,10 @@ __global__ void __launch_bounds__(kGqaThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();  // inputs written by the previous kernel are visible from here on
+        pdl_launch_dependents();
+    }
 
     if (warp == 0) {
         if (lane == 0) {
@@ -506,7 +510,10 @@ cudaError_t launch_gqa_d(DType dt, const AttnArgs& a, const GqaPack& pk, cudaStr
     const int64_t items = static_cast<int64_t>((a.S + R - 1) / R) * a.B * a.Hk * pk.nhc;
     if (items > 0x7fffffff) return cudaErrorInvalidValue;
     const int64_t grid = items < a.num_sms ? items : a.num_sms;
-    kern<<<static_cast<unsigned>(grid), kGqaThreads, Cfg::kSmem, s>>>(tq, tk, tv, a, pk);
+    AttnArgs ap = a;
+    ap.pdl = pdl_allowed(s);
+    (void)launch_pdl(ap.pdl != 0, kern, dim3(static_cast<unsigned>(grid)), dim3(kGqaThreads), Cfg::kSmem, s,
+                     tq, tk, tv, ap, pk);
     return cudaGetLastError();
 }
 

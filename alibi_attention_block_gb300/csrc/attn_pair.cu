@@ -194,6 +194,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();  // inputs written by the previous kernel are visible from here on
+        pdl_launch_dependents();
+    }
     // registers: the launch gives every thread kLaunchRegs; warpgroup 0 (TMA,
     // MMA issue) gives most of its share to the two softmax warpgroups, which
     // hold a row's 128 scores and 64 packed probabilities at once
@@ -578,7 +582,10 @@ cudaError_t launch_pair(DType dt, const AttnArgs& a, cudaStream_t s) {
     const int64_t items = (nq + 1) / 2 * a.B * a.H;
     if (items > 0x7fffffff) return cudaErrorInvalidValue;
     const int64_t grid = items < a.num_sms ? items : a.num_sms;
-    kern<<<static_cast<unsigned>(grid), kPairThreads, Cfg::kSmem, s>>>(tq, tk, tv, a);
+    AttnArgs ap = a;
+    ap.pdl = pdl_allowed(s);
+    (void)launch_pdl(ap.pdl != 0, kern, dim3(static_cast<unsigned>(grid)), dim3(kPairThreads), Cfg::kSmem, s,
+                     tq, tk, tv, ap);
     return cudaGetLastError();
 }
 

@@ -151,6 +151,10 @@ __global__ void __launch_bounds__(kP128Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();  // inputs written by the previous kernel are visible from here on
+        pdl_launch_dependents();
+    }
     static_assert(4 * kRegsControl + 8 * kRegsSoftmax <= 12 * kLaunchRegs,
                   "register split exceeds the launch's registers");
     if (warp < 4) {
@@ -495,7 +499,10 @@ cudaError_t launch_pair128_t(DType dt, const AttnArgs& a, cudaStream_t s) {
     const int64_t items = (nq + 1) / 2 * a.B * a.H;
     if (items > 0x7fffffff) return cudaErrorInvalidValue;
     const int64_t grid = items < a.num_sms ? items : a.num_sms;
-    kern<<<static_cast<unsigned>(grid), kP128Threads, Cfg::kSmem, s>>>(tq, tk, tv, a);
+    AttnArgs ap = a;
+    ap.pdl = pdl_allowed(s);
+    (void)launch_pdl(ap.pdl != 0, kern, dim3(static_cast<unsigned>(grid)), dim3(kP128Threads), Cfg::kSmem, s,
+                     tq, tk, tv, ap);
     return cudaGetLastError();
 }
 

@@ -260,6 +260,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
 // L2 eviction priority for TMA loads (createpolicy): evict_last for tiles that
 // other CTAs read again soon (an attention head's K/V prefix), evict_first for
 // tiles read once (the query tiles).
+// Programmatic dependent launch. A kernel launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization may start while the
+// previous kernel on its stream is still running; pdl_wait() returns once
+// every grid it depends on has completed and their writes are visible (at
+// once for a kernel launched without the attribute). The hot-path kernels
+// call it after their shared-memory / TMEM set-up and before their first
+// global load or store. pdl_launch_dependents() lets the stream's next
+// kernel be scheduled before this grid ends: that kernel is placed only once
+// every block of this grid has started, so its blocks, which take SM room
+// while they wait, never keep a block of this grid from being placed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));

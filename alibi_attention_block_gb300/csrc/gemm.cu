@@ -92,6 +92,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (g.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();  // inputs written by the previous kernel are visible from here on
+        pdl_launch_dependents();
+    }
     const int m_tiles = (g.M + kBM - 1) / kBM;
     const int n_tiles = (g.N + kBNOut - 1) / kBNOut;
     // work units (output tiles), numbered M-fastest (the CTAs running at any
@@ -270,6 +274,8 @@ cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     GemmArgs ga = g;
     ga.split_s = 1;
     ga.split_base = 0;
+    const bool pdl = pdl_allowed(s);
+    ga.pdl = pdl;
     if (kCanSplit && g.split_ws && g.split_cnt) {
         const int64_t G = grid_units;
         const int64_t rounds = (units + G - 1) / G;
@@ -280,11 +286,11 @@ cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
             R * sp <= kGemmSplitSlots && R * kEpiWarps <= kGemmSplitCounters) {
             ga.split_s = static_cast<int>(sp);
             ga.split_base = static_cast<int>((rounds - 1) * G);
-            kern_split<<<grid, kGemmThreads, Cfg::kSmem, s>>>(ta, tb, tb2, ga, rp);
+            (void)launch_pdl(pdl, kern_split, dim3(grid), dim3(kGemmThreads), Cfg::kSmem, s, ta, tb, tb2, ga, rp);
             return cudaGetLastError();
         }
     }
-    kern<<<grid, kGemmThreads, Cfg::kSmem, s>>>(ta, tb, tb2, ga, rp);
+    (void)launch_pdl(pdl, kern, dim3(grid), dim3(kGemmThreads), Cfg::kSmem, s, ta, tb, tb2, ga, rp);
     return cudaGetLastError();
 }
 

@@ -90,6 +90,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     cluster_sync();  // both CTAs' barriers and TMEM exist before any signal crosses
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (g.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();  // inputs written by the previous kernel are visible from here on
+        pdl_launch_dependents();
+    }
     const int m_units = (g.M + kPM - 1) / kPM;
     const int n_tiles = (g.N + kBNOut - 1) / kBNOut;
     const int num_units = m_units * n_tiles;
@@ -278,24 +282,31 @@ cudaError_t launch_pair_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const 
         e = set_smem_attr_once(reinterpret_cast<const void*>(kern_split), kPairSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start (set-up only) while the previous kernel drains, outside
+    // graph capture (pdl_allowed)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = kPairSmem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query below sees the cluster shape only
     const int64_t units =
         static_cast<int64_t>((g.M + 2 * kBM - 1) / (2 * kBM)) * ((g.N + kBNOut - 1) / kBNOut);
     const int64_t slots = max_pairs(reinterpret_cast<const void*>(kern), cfg, num_sms);
+    const bool pdl = pdl_allowed(s);
+    cfg.numAttrs = pdl ? 2 : 1;
     const int64_t pairs = units < slots ? units : slots;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     GemmArgs ga = g;
     ga.split_s = 1;
     ga.split_base = 0;
+    ga.pdl = pdl;
     // the split of a last, partial round along K, as in gemm.cu (each CTA of
     // a pair publishes its own 128-row partial tiles)
     if (kCanSplit && g.split_ws && g.split_cnt) {

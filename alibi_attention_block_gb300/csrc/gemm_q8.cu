@@ -144,6 +144,10 @@ __global__ void __launch_bounds__(kQ8Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (g.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();  // inputs written by the previous kernel are visible from here on
+        pdl_launch_dependents();
+    }
     const int m_tiles = (g.M + kBM - 1) / kBM;
     const int n_tiles = (g.N + kBNOut - 1) / kBNOut;
     const int num_units = m_tiles * n_tiles;
@@ -327,7 +331,10 @@ cudaError_t launch_q8_cfg(const CUtensorMap& ta, const Q8Maps& qm, const GemmArg
     const int64_t units =
         static_cast<int64_t>((g.M + kBM - 1) / kBM) * ((g.N + kBNOut - 1) / kBNOut);
     const int64_t grid = units < num_sms ? units : num_sms;
-    kern<<<static_cast<unsigned>(grid), kQ8Threads, kQ8Smem, s>>>(ta, qm, g, rp);
+    GemmArgs gp = g;
+    gp.pdl = pdl_allowed(s);
+    (void)launch_pdl(gp.pdl != 0, kern, dim3(static_cast<unsigned>(grid)), dim3(kQ8Threads), kQ8Smem,
+                     s, ta, qm, gp, rp);
     return cudaGetLastError();
 }
 

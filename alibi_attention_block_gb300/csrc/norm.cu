@@ -44,8 +44,12 @@ __global__ void __launch_bounds__(kNormThreads) norm_kernel(const TX* x,
                                                             const T* __restrict__ beta,
                                                             T* y,
                                                             float* __restrict__ y32, int64_t rows,
-                                                            int cols, float eps) {
+                                                            int cols, float eps, int pdl) {
     __shared__ float red[kNormThreads / 32];
+    if (pdl) {  // launched for programmatic dependent launch
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     constexpr int kRowsPerBlock = kNormThreads / TPR;
     const int sub = threadIdx.x % TPR;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + threadIdx.x / TPR;
@@ -123,16 +127,15 @@ cudaError_t launch_tv(bool rms, const NormIO& io, const void* g, const void* b, 
     constexpr int kRowsPerBlock = kNormThreads / TPR;
     const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    const bool pdl = pdl_allowed(s);
     auto go = [&](auto kern) {
-        kern<<<static_cast<unsigned>(blocks), kNormThreads, 0, s>>>(
-            static_cast<const TX*>(io.x), static_cast<const TR*>(io.res), static_cast<const T*>(g),
-            static_cast<const T*>(b), static_cast<T*>(io.y), io.y32, rows, cols, eps);
+        return launch_pdl(pdl, kern, dim3(static_cast<unsigned>(blocks)), dim3(kNormThreads), 0, s,
+                          static_cast<const TX*>(io.x), static_cast<const TR*>(io.res),
+                          static_cast<const T*>(g), static_cast<const T*>(b),
+                          static_cast<T*>(io.y), io.y32, rows, cols, eps, pdl ? 1 : 0);
     };
-    if (rms)
-        go(norm_kernel<T, TX, TR, TPR, VPT, true>);
-    else
-        go(norm_kernel<T, TX, TR, TPR, VPT, false>);
-    return cudaGetLastError();
+    return rms ? go(norm_kernel<T, TX, TR, TPR, VPT, true>)
+               : go(norm_kernel<T, TX, TR, TPR, VPT, false>);
 }
 
 template <typename T, typename TX, typename TR>

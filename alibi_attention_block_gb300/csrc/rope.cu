@@ -37,6 +37,10 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 template <typename T>
 __global__ void __launch_bounds__(kRopeThreads, 5) qk_norm_rope_kernel(QkNormRopeArgs a,
                                                                        RopeParams rp) {
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     extern __shared__ float buf[];  // (H + Hk) * d floats, then cos[r/2], sin[r/2]
     __shared__ float red[kRopeThreads / 32];
     const int token = blockIdx.x;
@@ -180,6 +184,10 @@ __global__ void __launch_bounds__(kRopeThreads, 5) qk_norm_rope_kernel(QkNormRop
 // the lane's vector slot within the head, so each lane evaluates them once.
 template <typename T, int NV>
 __global__ void __launch_bounds__(128) qk_warp_kernel(QkNormRopeArgs a, RopeParams rp) {
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     const int lane = threadIdx.x & 31;
     const int wid = blockIdx.x * 4 + threadIdx.x / 32;
     const int parts = a.Hk > 0 ? 2 : 1;
@@ -308,6 +316,10 @@ struct UnitCfg {
 
 template <typename T, int D, int NU>
 __global__ void __launch_bounds__(128) qk_unit_kernel(QkNormRopeArgs a, RopeParams rp) {
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     using Cfg = UnitCfg<NU>;
     constexpr int kLph = D / 16;  // lanes per head
     extern __shared__ __align__(128) uint8_t usm[];
@@ -486,7 +498,7 @@ void launch_unit(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_t s, 
     int64_t blocks = (warps + 3) / 4;
     const int64_t cap = static_cast<int64_t>(per_sm < 8 ? per_sm : 8) * a.num_sms;
     if (blocks > cap) blocks = cap;
-    kern<<<static_cast<unsigned>(blocks), 128, Cfg::kSmem, s>>>(a, rp);
+    (void)launch_pdl(a.pdl != 0, kern, dim3(static_cast<unsigned>(blocks)), dim3(128), Cfg::kSmem, s, a, rp);
 }
 
 template <typename T, int D>
@@ -525,6 +537,10 @@ constexpr int kHeadWarps = 8;
 template <typename T, int HM>
 __global__ void __launch_bounds__(kHeadWarps * 32) qk_head_kernel(QkNormRopeArgs a,
                                                                   RopeParams rp) {
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     __shared__ float cs_tab[2 * kMaxRotaryPairs];  // cos[r/2], then sin[r/2]
     extern __shared__ __align__(16) uint8_t rows[];  // (H + Hk) rows of d values
     const int token = blockIdx.x;
@@ -660,7 +676,7 @@ void launch_head(unsigned grid, size_t smem, const QkNormRopeArgs& a, const Rope
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
-    kern<<<grid, kHeadWarps * 32, smem, s>>>(a, rp);
+    (void)launch_pdl(a.pdl != 0, kern, dim3(grid), dim3(kHeadWarps * 32), smem, s, a, rp);
 }
 
 template <typename T>
@@ -698,6 +714,10 @@ constexpr int kRgWarps = 8;
 template <typename T, int D, int ROT>
 __global__ void __launch_bounds__(kRgWarps * 32) qk_rowgroup_kernel(QkNormRopeArgs a,
                                                                     RopeParams rp) {
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     constexpr int VL = D / 32;  // 16-byte vectors per lane
     constexpr int kPairs = ROT / 2;
     static_assert(ROT % 2 == 0 && ROT <= 8 * VL, "the rotary span must lie in a row's first lane");
@@ -851,7 +871,7 @@ bool launch_rowgroup_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStr
     int64_t blocks = (items + kRgWarps - 1) / kRgWarps;
     const int64_t cap = static_cast<int64_t>(per_sm) * a.num_sms;
     if (blocks > cap) blocks = cap;
-    kern<<<static_cast<unsigned>(blocks), kRgWarps * 32, 0, s>>>(a, rp);
+    (void)launch_pdl(a.pdl != 0, kern, dim3(static_cast<unsigned>(blocks)), dim3(kRgWarps * 32), 0, s, a, rp);
     return true;
 }
 
@@ -865,17 +885,19 @@ bool launch_warp_path(const QkNormRopeArgs& a, const RopeParams& rp, cudaStream_
     const int64_t blocks = (warps + 3) / 4;
     if (blocks > 0x7fffffff) return false;
     const unsigned g = static_cast<unsigned>(blocks);
-    if (nvec <= 32) qk_warp_kernel<T, 1><<<g, 128, 0, s>>>(a, rp);
-    else if (nvec <= 64) qk_warp_kernel<T, 2><<<g, 128, 0, s>>>(a, rp);
-    else if (nvec <= 128) qk_warp_kernel<T, 4><<<g, 128, 0, s>>>(a, rp);
-    else qk_warp_kernel<T, 8><<<g, 128, 0, s>>>(a, rp);
+    if (nvec <= 32) (void)launch_pdl(a.pdl != 0, qk_warp_kernel<T, 1>, dim3(g), dim3(128), 0, s, a, rp);
+    else if (nvec <= 64) (void)launch_pdl(a.pdl != 0, qk_warp_kernel<T, 2>, dim3(g), dim3(128), 0, s, a, rp);
+    else if (nvec <= 128) (void)launch_pdl(a.pdl != 0, qk_warp_kernel<T, 4>, dim3(g), dim3(128), 0, s, a, rp);
+    else (void)launch_pdl(a.pdl != 0, qk_warp_kernel<T, 8>, dim3(g), dim3(128), 0, s, a, rp);
     return true;
 }
 
 }  // namespace
 
-cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopeParams& rp,
+cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& args, const RopeParams& rp,
                                 cudaStream_t s) {
+    QkNormRopeArgs a = args;
+    a.pdl = pdl_allowed(s);
     const int64_t tokens = static_cast<int64_t>(a.B) * a.S;
     if (tokens == 0) return cudaSuccess;
     if (dt == DType::F16 ? launch_rowgroup_path<__half>(a, rp, s)
@@ -897,12 +919,12 @@ cudaError_t launch_qk_norm_rope(DType dt, const QkNormRopeArgs& a, const RopePar
         auto k = qk_norm_rope_kernel<__half>;
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        k<<<static_cast<unsigned>(tokens), kRopeThreads, smem, s>>>(a, rp);
+        (void)launch_pdl(a.pdl != 0, k, dim3(static_cast<unsigned>(tokens)), dim3(kRopeThreads), smem, s, a, rp);
     } else {
         auto k = qk_norm_rope_kernel<__nv_bfloat16>;
         if (smem > 48 * 1024)
             cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        k<<<static_cast<unsigned>(tokens), kRopeThreads, smem, s>>>(a, rp);
+        (void)launch_pdl(a.pdl != 0, k, dim3(static_cast<unsigned>(tokens)), dim3(kRopeThreads), smem, s, a, rp);
     }
     return cudaGetLastError();
 }
