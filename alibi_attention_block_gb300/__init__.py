@@ -22,7 +22,7 @@ from ._abi import BlkError  # noqa: F401
 
 __all__ = ["layernorm_bias", "rmsnorm", "qkv_bias_rope_partial", "rope_inplace", "attn_prefill",
            "attn_decode", "attn_decode_workspace_size", "decode_desc",
-           "linear", "mlp", "block_desc", "forward_workspace_size", "forward", "forward_host", "ForwardGraph", "HostPipe", "model_desc",
+           "linear", "mlp", "block_desc", "forward_workspace_size", "forward_q8_0_workspace_size", "forward", "forward_host", "ForwardGraph", "HostPipe", "model_desc",
            "model_workspace_size", "model_forward",
            "check_device_status", "BlkError", "library_path"]
 
@@ -277,15 +277,26 @@ def forward(cfg, weights: dict, x, workspace=None, out=None):
 Q8_PROJECTIONS = ("qkv", "o", "gate", "up", "down")
 
 
+def forward_q8_0_workspace_size(cfg, batch: int, seq: int) -> int:
+    """Workspace bytes of blk_forward_q8_0's dequantize-once path."""
+    desc = block_desc(cfg, batch, seq)
+    need = C.c_size_t(0)
+    _abi.check(_lib().blk_forward_q8_0_workspace_size(C.byref(desc), C.byref(need)),
+               "blk_forward_q8_0_workspace_size")
+    return need.value
+
+
 def forward_q8_0(cfg, weights: dict, q8: dict, x, workspace=None, out=None):
     """The block with Q8_0 projection weights (blk_forward_q8_0). weights:
     the non-projection slots as for ``forward``; q8 maps ``q_<name>`` (int8
     codes) and ``d_<name>`` (fp16 scales) for name in qkv, o, gate, up, down
-    (gate for SwiGLU only)."""
+    (gate for SwiGLU only). workspace: ``forward_q8_0_workspace_size`` bytes
+    (allocated here when None) take the dequantize-once path from 512 tokens
+    on; ``forward_workspace_size`` bytes keep the W8A16 GEMMs."""
     B, S, _ = x.shape
     desc = block_desc(cfg, B, S)
     if workspace is None:
-        workspace = torch.empty(forward_workspace_size(cfg, B, S), dtype=torch.uint8,
+        workspace = torch.empty(forward_q8_0_workspace_size(cfg, B, S), dtype=torch.uint8,
                                 device=x.device)
     unknown = set(weights) - set(_abi.WEIGHT_SLOTS)
     if unknown:
@@ -480,7 +491,7 @@ class ForwardGraph:
         if events:
             ev = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
             n_ev = len(events)
-        self.kinds = (C.c_int32 * 10)()
+        self.kinds = (C.c_int32 * 12)()  # a block makes at most 12 launches
         self.n_launches = C.c_int(0)
         handle = C.c_void_p()
         _abi.check(_lib().blk_forward_graph_create(C.byref(self.desc), C.byref(self.w), _p(x), _p(y),

@@ -100,6 +100,7 @@ _PROTOS = {
     "blk_mlp_noalloc": (C.c_int, [C.POINTER(MlpDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_int,
                                   vp]),
     "blk_forward_workspace_size": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(C.c_size_t)]),
+    "blk_forward_q8_0_workspace_size": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(C.c_size_t)]),
     "blk_forward": (C.c_int, [C.POINTER(BlockDesc), C.POINTER(BlockWeights), vp, vp, vp,
                               C.c_size_t, C.c_int, vp]),
     "blk_attn_decode_workspace_size": (C.c_int, [C.POINTER(DecodeDesc), C.POINTER(C.c_size_t)]),
@@ -135,7 +136,7 @@ _PROTOS = {
 }
 
 STEP_NAMES = ("input_norm", "qkv", "qk_norm_rope", "attention", "o_proj", "post_attn_norm",
-              "mlp_norm", "mlp_up", "mlp_down", "post_mlp_norm")
+              "mlp_norm", "mlp_up", "mlp_down", "post_mlp_norm", "q8_dequant")
 
 _lib = None
 

@@ -1,6 +1,7 @@
 // C ABI of the block library (include/blk.h): argument validation (before any
 // CUDA call, so a rejected call has no side effects), TMA descriptor set-up,
 // kernel dispatch and the blk_forward step sequence.
+#include <algorithm>
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -419,6 +420,42 @@ FwdLayout forward_layout(const blk_block_desc* d) {
     return L;
 }
 
+// The dequantize-once Q8_0 path: from this many tokens on, expanding a
+// projection's weights once (3 bytes of traffic per weight) costs less than
+// the W8A16 kernel's expansion of every weight tile per 128-row tile of x.
+constexpr int64_t kQ8DequantMinTokens = 512;
+
+// The projections of a block as (rows, cols) of their weights: QKV, output,
+// gate (SwiGLU only), up, down; *n receives how many.
+void q8_shapes(const blk_block_desc* d, int64_t (*rc)[2], int* n) {
+    const auto& q = d->qkv;
+    const int64_t D = q.hidden, Hd = q.n_heads * q.head_dim, Kd = q.n_kv_heads * q.head_dim;
+    const int64_t F = d->intermediate;
+    int i = 0;
+    auto put = [&](int64_t r, int64_t c) {
+        rc[i][0] = r;
+        rc[i][1] = c;
+        ++i;
+    };
+    put(Hd + 2 * Kd, D);
+    put(D, Hd);
+    if (d->act == BLK_ACT_SWIGLU) put(F, D);
+    put(F, D);
+    put(D, F);
+    *n = i;
+}
+
+// Its scratch after the block's workspace: every projection's weights in the
+// storage dtype, each 256-byte aligned, in q8_shapes order.
+size_t q8_scratch_bytes(const blk_block_desc* d) {
+    int64_t rc[kQ8DequantMaxJobs][2];
+    int n = 0;
+    q8_shapes(d, rc, &n);
+    size_t total = 0;
+    for (int i = 0; i < n; ++i) total += align256(static_cast<size_t>(2 * rc[i][0] * rc[i][1]));
+    return total;
+}
+
 // Records an event after each kernel launch of blk_forward_ex and the kind
 // of each launch (see blk_forward_ex in blk.h).
 struct StepLog {
@@ -448,7 +485,9 @@ struct StepLog {
         return BLK_OK;
     }
     blk_status step(int kind) {
-        if (kinds && n < 10 && n + 1 < (n_events > 0 ? n_events : 11)) kinds[n] = kind;
+        // at most 12 (a block makes at most 9: OLMo-2's eight kernels and
+        // the Q8_0 weight expansion)
+        if (kinds && n < 12 && (n_events <= 0 || n + 1 < n_events)) kinds[n] = kind;
         ++n;
         if (events && n < n_events) return record(n);
         return BLK_OK;
@@ -930,6 +969,13 @@ blk_status blk_forward_workspace_size(const blk_block_desc* d, size_t* bytes) {
     return BLK_OK;
 }
 
+blk_status blk_forward_q8_0_workspace_size(const blk_block_desc* d, size_t* bytes) {
+    blk_status st = blk_forward_workspace_size(d, bytes);
+    if (st != BLK_OK) return st;
+    *bytes += q8_scratch_bytes(d);
+    return BLK_OK;
+}
+
 blk_status blk_forward(const blk_block_desc* d, const blk_block_weights* w, const void* x,
                        void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s) {
     return blk_forward_ex(d, w, x, y, workspace, ws_bytes, dt, s, nullptr, 0, nullptr, nullptr);
@@ -1014,6 +1060,17 @@ blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
     const Q8W* pq_o = q8 ? &wq_o : nullptr;
     const Q8W* pq_up = q8 ? &wq_up : nullptr;
     const Q8W* pq_down = q8 ? &wq_down : nullptr;
+    // the dense GEMMs' weights: w's, or Q8_0 weights expanded into the
+    // scratch after the workspace (dequantize-once path: a workspace of
+    // blk_forward_q8_0_workspace_size bytes and at least 512 tokens)
+    const void* W_qkv = w->w_qkv;
+    const void* W_o = w->w_o;
+    const void* W_gate = w->w_gate;
+    const void* W_up = w->w_up;
+    const void* W_down = w->w_down;
+    void* q8_scratch = q8 && T >= kQ8DequantMinTokens && ws_bytes >= L.total + q8_scratch_bytes(d)
+                           ? ws + L.total
+                           : nullptr;
     cudaError_t e;
     StepLog log{events, n_events, step_kinds, n_launches, cs};
     if ((st = log.begin()) != BLK_OK) return st;
@@ -1027,6 +1084,35 @@ blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
     do {                                                 \
         if ((st = log.step(kind)) != BLK_OK) return st;  \
     } while (0)
+    // dequantize-once path: every projection's codes expanded, in one launch,
+    // into the scratch; the GEMMs then run dense on them
+    if (q8_scratch) {
+        int64_t rc[kQ8DequantMaxJobs][2];
+        int n_jobs = 0;
+        q8_shapes(d, rc, &n_jobs);
+        const Q8W* src[kQ8DequantMaxJobs];
+        const void** dst[kQ8DequantMaxJobs];
+        int k = 0;
+        src[k] = pq_qkv, dst[k++] = &W_qkv;
+        src[k] = pq_o, dst[k++] = &W_o;
+        if (swiglu) src[k] = pq_up, dst[k++] = &W_gate;  // q8_shapes order: gate, then up
+        src[k] = pq_up, dst[k++] = &W_up;
+        src[k] = pq_down, dst[k++] = &W_down;
+        Q8DequantJob jobs[kQ8DequantMaxJobs];
+        uint8_t* at = static_cast<uint8_t*>(q8_scratch);
+        for (int i = 0; i < n_jobs; ++i) {
+            // SwiGLU's up weights are the second pair of wq_up
+            const bool second = swiglu && dst[i] == &W_up;
+            jobs[i] = Q8DequantJob{second ? src[i]->q2 : src[i]->q, second ? src[i]->d2 : src[i]->d,
+                                   at, rc[i][0], rc[i][1]};
+            *dst[i] = at;
+            at += align256(static_cast<size_t>(2 * rc[i][0] * rc[i][1]));
+        }
+        e = launch_q8_dequant(t, jobs, n_jobs, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "q8_0 dequantize launch");
+        BLK_STEP(BLK_STEP_Q8_DEQUANT);
+        pq_qkv = pq_o = pq_up = pq_down = nullptr;
+    }
 
     // 1. input norm (absent in the reordered post-norm block)
     const void* attn_in = x;
@@ -1038,7 +1124,7 @@ blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
         attn_in = n1;
     }
     // 2. projection (+bias), qk-norm, rotary, head split
-    st = run_qkv(&q, attn_in, w->w_qkv, w->b_qkv, w->q_norm_w, w->k_norm_w, qb, kb, vb, t, cs, ds,
+    st = run_qkv(&q, attn_in, W_qkv, w->b_qkv, w->q_norm_w, w->k_norm_w, qb, kb, vb, t, cs, ds,
                  &log, split, pq_qkv);
     if (st != BLK_OK) return st;
     // 3. causal attention (+ALiBi)
@@ -1050,16 +1136,16 @@ blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
     if (parallel) {
         // 4p. attn_out = o W_o^T (+b_o) kept in fp32; mlp on the same normed
         // input; y = x + attn_out + mlp
-        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
+        st = run_linear(t, EPI_LINEAR, ob, W_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
                         cs, ds, F32_OUT, split, pq_o);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
-        st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, attn_in, swiglu ? w->w_gate : w->w_up,
-                        swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
+        st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, attn_in, swiglu ? W_gate : W_up,
+                        swiglu ? W_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
                         split, pq_up);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_UP);
-        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, x, tmp, y, T, D, F, cs,
+        st = run_linear(t, EPI_LINEAR, ab, W_down, nullptr, w->b_down, x, tmp, y, T, D, F, cs,
                         ds, F32_RES2, split, pq_down);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
@@ -1068,7 +1154,7 @@ blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
     const void* mlp_in;
     if (pre) {
         // 4. h = x + o W_o^T (+b_o), fp32;  5. n2 = norm(h)
-        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, x, nullptr, hb, T, D, Hd, cs, ds,
+        st = run_linear(t, EPI_LINEAR, ob, W_o, nullptr, w->b_o, x, nullptr, hb, T, D, Hd, cs, ds,
                         F32_OUT, split, pq_o);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
@@ -1081,7 +1167,7 @@ blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
         // 4. a = o W_o^T (fp32: the RMS norm rescales it to unit size, so its
         // rounding would be magnified);  5. h = x + RMS(a) * w_post_attn
         // (fp32, and a storage copy for the MLP)
-        st = run_linear(t, EPI_LINEAR, ob, w->w_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
+        st = run_linear(t, EPI_LINEAR, ob, W_o, nullptr, w->b_o, nullptr, nullptr, tmp, T, D, Hd,
                         cs, ds, F32_OUT, split, pq_o);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_O_PROJ);
@@ -1092,21 +1178,21 @@ blk_status forward_impl(const blk_block_desc* d, const blk_block_weights* w,
         mlp_in = h16;
     }
     // 6. MLP up (+activation)
-    st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, mlp_in, swiglu ? w->w_gate : w->w_up,
-                    swiglu ? w->w_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
+    st = run_linear(t, swiglu ? EPI_SWIGLU : EPI_GELU, mlp_in, swiglu ? W_gate : W_up,
+                    swiglu ? W_up : nullptr, w->b_up, nullptr, nullptr, ab, T, F, D, cs, ds, 0,
                     split, pq_up);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_UP);
     if (pre) {
         // 7. y = h + a W_d^T (+b_d)
-        st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, hb, nullptr, y, T, D, F, cs,
+        st = run_linear(t, EPI_LINEAR, ab, W_down, nullptr, w->b_down, hb, nullptr, y, T, D, F, cs,
                         ds, F32_RES1, split, pq_down);
         if (st != BLK_OK) return st;
         BLK_STEP(BLK_STEP_MLP_DOWN);
         return log.end();
     }
     // 7. m = a W_d^T;  8. y = h + RMS(m) * w_post_mlp
-    st = run_linear(t, EPI_LINEAR, ab, w->w_down, nullptr, w->b_down, nullptr, nullptr, tmp, T, D, F,
+    st = run_linear(t, EPI_LINEAR, ab, W_down, nullptr, w->b_down, nullptr, nullptr, tmp, T, D, F,
                     cs, ds, F32_OUT, split, pq_down);
     if (st != BLK_OK) return st;
     BLK_STEP(BLK_STEP_MLP_DOWN);

@@ -408,7 +408,102 @@ __global__ void q8_quantize_kernel(const T* __restrict__ w, int64_t rows, int64_
     d[j * rows + n] = __float2half_rn(d32);
 }
 
+// Dequantize once: W[n, k] = q[n, k] * d[k/32, n] in the storage type,
+// written to memory for the dense GEMM (the path of large token counts,
+// where the W8A16 kernel would expand every weight tile once per 128-row
+// tile of x). The product is exact in fp32 and rounded once, as in the
+// converter warps, so the two paths see the same weights. A block covers 32
+// rows x 256 inputs of one matrix: the tile's 8 x 32 scales come in as
+// contiguous 64-byte runs through shared memory, and each thread expands one
+// 32-input block (two 16-byte code loads, 64 bytes written), eight threads
+// per row, so that a warp reads and writes whole 256-byte row segments. (One
+// thread per row and block, rows fastest, read 32 bytes from each of 32 rows
+// K bytes apart per warp and reached ~2.2 TB/s.) One launch takes all of a
+// block's matrices: the tiles of job i are blocks [tile0_i, tile0_{i+1}),
+// 256-input column tiles fastest so that consecutive blocks read on along
+// the same rows.
+constexpr int kDqRows = 32, kDqBlocks = 8;
+
+struct Q8DequantArgs {
+    Q8DequantJob job[kQ8DequantMaxJobs];
+    int64_t tile0[kQ8DequantMaxJobs];
+    int n_jobs;
+    int pdl;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kDqRows * kDqBlocks) q8_dequant_kernel(const Q8DequantArgs a) {
+    __shared__ float sc[kDqBlocks][kDqRows];
+    if (a.pdl) {  // launched for programmatic dependent launch
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    // this block's matrix, picked with static indices only (indexing the
+    // parameter arrays by a runtime value would copy them to local memory)
+    const int64_t t = blockIdx.x;
+    Q8DequantJob jb = a.job[0];
+    int64_t lt = t;
+#pragma unroll
+    for (int i = 1; i < kQ8DequantMaxJobs; ++i)
+        if (i < a.n_jobs && t >= a.tile0[i]) {
+            jb = a.job[i];
+            lt = t - a.tile0[i];
+        }
+    const int64_t nblk = jb.cols / 32;
+    const int64_t tiles_k = (nblk + kDqBlocks - 1) / kDqBlocks;
+    const int64_t n0 = (lt / tiles_k) * kDqRows;
+    const int64_t j0 = (lt % tiles_k) * kDqBlocks;
+    const __half* dsc = static_cast<const __half*>(jb.d);
+    {
+        const int jj = threadIdx.x / kDqRows, r = threadIdx.x % kDqRows;
+        const int64_t n = n0 + r, j = j0 + jj;
+        sc[jj][r] = n < jb.rows && j < nblk ? __half2float(dsc[j * jb.rows + n]) : 0.f;
+    }
+    __syncthreads();
+    const int r = threadIdx.x / kDqBlocks, jj = threadIdx.x % kDqBlocks;
+    const int64_t n = n0 + r, j = j0 + jj;
+    if (n >= jb.rows || j >= nblk) return;
+    const uint4* src = reinterpret_cast<const uint4*>(jb.q + n * jb.cols + j * 32);
+    const uint4 c[2] = {src[0], src[1]};
+    const float d = sc[jj][r];
+    T* dst = static_cast<T*>(jb.w) + n * jb.cols + j * 32;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint32_t lo = v & 1 ? (v & 2 ? c[1].z : c[0].z) : (v & 2 ? c[1].x : c[0].x);
+        const uint32_t hi = v & 1 ? (v & 2 ? c[1].w : c[0].w) : (v & 2 ? c[1].y : c[0].y);
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            f[e] = static_cast<float>(static_cast<int8_t>((lo >> (8 * e)) & 0xFFu)) * d;
+            f[4 + e] = static_cast<float>(static_cast<int8_t>((hi >> (8 * e)) & 0xFFu)) * d;
+        }
+        store8(dst + v * 8, f);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_q8_dequant(DType dt, const Q8DequantJob* jobs, int n_jobs, cudaStream_t s) {
+    if (n_jobs < 1 || n_jobs > kQ8DequantMaxJobs) return cudaErrorInvalidValue;
+    Q8DequantArgs a{};
+    int64_t tiles = 0;
+    for (int i = 0; i < n_jobs; ++i) {
+        a.job[i] = jobs[i];
+        a.tile0[i] = tiles;
+        const int64_t nblk = jobs[i].cols / 32;
+        tiles += (jobs[i].rows + kDqRows - 1) / kDqRows * ((nblk + kDqBlocks - 1) / kDqBlocks);
+    }
+    if (tiles == 0) return cudaSuccess;
+    if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    a.n_jobs = n_jobs;
+    a.pdl = pdl_allowed(s);
+    const dim3 grid(static_cast<unsigned>(tiles)), block(kDqRows * kDqBlocks);
+    if (dt == DType::F16)
+        (void)launch_pdl(a.pdl != 0, q8_dequant_kernel<__half>, grid, block, 0, s, a);
+    else
+        (void)launch_pdl(a.pdl != 0, q8_dequant_kernel<__nv_bfloat16>, grid, block, 0, s, a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_q8(DType dt, int epi, const void* a, const int8_t* q, const void* d,
                            const int8_t* q2, const void* d2, const GemmArgs& args,

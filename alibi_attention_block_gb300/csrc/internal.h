@@ -99,6 +99,18 @@ cudaError_t launch_gemm_q8(DType dt, int epi, const void* a, const int8_t* q, co
                            const RopeParams& rp, int num_sms, cudaStream_t s);
 // w [rows, cols] (storage dtype, cols % 32 == 0) -> codes q [rows, cols],
 // scales d [cols/32, rows] (fp16)
+// W = q * d in the storage type (see q8_dequant_kernel), for up to
+// kQ8DequantMaxJobs matrices in one launch: codes q [rows, cols], fp16
+// scales d [cols/32, rows], output w [rows, cols]; cols % 32 == 0, every
+// pointer 16-byte aligned.
+constexpr int kQ8DequantMaxJobs = 5;
+struct Q8DequantJob {
+    const int8_t* q;
+    const void* d;
+    void* w;
+    int64_t rows, cols;
+};
+cudaError_t launch_q8_dequant(DType dt, const Q8DequantJob* jobs, int n_jobs, cudaStream_t s);
 cudaError_t launch_q8_quantize(DType dt, const void* w, int64_t rows, int64_t cols, int8_t* q,
                                void* d, cudaStream_t s);
 

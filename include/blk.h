@@ -318,7 +318,8 @@ typedef enum {
     BLK_STEP_MLP_NORM = 6,     /* LN/RMS of h (sequential pre-norm) */
     BLK_STEP_MLP_UP = 7,       /* gate/up GEMM + SwiGLU, or up GEMM + bias + GELU */
     BLK_STEP_MLP_DOWN = 8,     /* down GEMM (+bias, +residuals) */
-    BLK_STEP_POST_MLP_NORM = 9 /* OLMo-2: y = h + RMS(mlp_out) */
+    BLK_STEP_POST_MLP_NORM = 9, /* OLMo-2: y = h + RMS(mlp_out) */
+    BLK_STEP_Q8_DEQUANT = 10   /* Q8_0 weights expanded for the dense GEMMs (blk_forward_q8_0) */
 } blk_step_kind;
 
 /* blk_forward, also reporting its kernel launches. If `events` is non-NULL
@@ -326,25 +327,43 @@ typedef enum {
  * is recorded on s before the first launch and events[i] right after launch
  * i, for i < n_events; the time between events[i-1] and events[i] is launch
  * i's duration on the stream. If step_kinds is non-NULL it receives the
- * blk_step_kind of each launch (room for n_events - 1 entries, at most 10 are
- * written). *n_launches (nullable) receives the number of launches. */
+ * blk_step_kind of each launch (room for n_events - 1 entries, or 12 when
+ * events is NULL; at most 12 are written, and a block makes at most 9
+ * launches).
+ * *n_launches (nullable) receives the number of launches. */
 blk_status blk_forward_ex(const blk_block_desc* d, const blk_block_weights* w, const void* x,
                           void* y, void* workspace, size_t ws_bytes, blk_dtype dt, blk_stream_t s,
                           void* const* events, int n_events, int32_t* step_kinds, int* n_launches);
 
 /* The block with Q8_0 projection weights (the q8 rows of "StableLM-2: partial
  * RoPE ...", section 3 Results and "OLMo-2 ...", section 4; format above):
- * blk_forward with every projection (QKV, output, MLP gate/up, down) run as
- * a W8A16 GEMM on its codes and scales. w holds the norms, biases, qk-norm
- * weights and ALiBi slopes as for blk_forward; its five projection slots
- * (w_qkv, w_o, w_gate, w_up, w_down) must be NULL, and q8 gives them, with
- * the same shapes ([out, in] codes, [in/32, out] scales; q_gate/d_gate NULL
- * unless the MLP is SwiGLU). hidden, n_heads * head_dim and intermediate must
- * be multiples of 32. Workspace, errors and everything else as blk_forward. */
+ * blk_forward with every projection (QKV, output, MLP gate/up, down) taken
+ * with weights q * d, each rounded once to dt. w holds the norms, biases,
+ * qk-norm weights and ALiBi slopes as for blk_forward; its five projection
+ * slots (w_qkv, w_o, w_gate, w_up, w_down) must be NULL, and q8 gives them,
+ * with the same shapes ([out, in] codes, [in/32, out] scales; q_gate/d_gate
+ * NULL unless the MLP is SwiGLU). hidden, n_heads * head_dim and
+ * intermediate must be multiples of 32.
+ * Two ways to run the projections, with the same weight values (sums may
+ * differ in fp32 accumulation order):
+ *   - W8A16 GEMMs that expand the codes on chip, tile by tile: with a
+ *     workspace of blk_forward_workspace_size bytes, or below 512 tokens;
+ *   - dequantize once: with at least 512 tokens and a workspace of
+ *     blk_forward_q8_0_workspace_size bytes, all projections' weights are
+ *     first expanded into the workspace's tail (one extra launch, step kind
+ *     BLK_STEP_Q8_DEQUANT), then multiplied by the dense GEMMs: at large
+ *     token counts the W8A16 kernel would expand every weight tile once per
+ *     128 tokens.
+ * Errors and everything else as blk_forward. */
 typedef struct {
     const int8_t *q_qkv, *q_o, *q_gate, *q_up, *q_down;  /* codes */
     const void *d_qkv, *d_o, *d_gate, *d_up, *d_down;    /* fp16 scales */
 } blk_q8_weights;
+/* Workspace bytes of blk_forward_q8_0's dequantize-once path:
+ * blk_forward_workspace_size plus every projection's weights in the storage
+ * dtype (QKV, output, gate for SwiGLU, up, down; each 256-byte aligned).
+ * Errors as blk_forward_workspace_size. */
+blk_status blk_forward_q8_0_workspace_size(const blk_block_desc* d, size_t* bytes);
 blk_status blk_forward_q8_0(const blk_block_desc* d, const blk_block_weights* w,
                             const blk_q8_weights* q8, const void* x, void* y, void* workspace,
                             size_t ws_bytes, blk_dtype dt, blk_stream_t s);

@@ -166,6 +166,24 @@ def test_forward_workspace_check(lib):
     assert need.value == 2 * T * (7 * D + 4 * 256 + F) + split
 
 
+def test_forward_q8_0_workspace_size(lib):
+    """The dequantize-once path's workspace: the block's, then every
+    projection's weights in the storage dtype (QKV, output, gate for SwiGLU,
+    up, down), each 256-byte aligned."""
+    base, q8 = C.c_size_t(0), C.c_size_t(0)
+    D, qkv = 256, 3 * 4 * 64
+    al = lambda b: -(-b // 256) * 256
+    for kw, F, n_up in ((dict(), 688, 2), (dict(act=_abi.BLK_ACT_GELU_TANH), 688, 1),
+                        (dict(intermediate=2048), 2048, 2)):
+        d = _block(**kw)
+        assert lib.blk_forward_workspace_size(C.byref(d), C.byref(base)) == _abi.BLK_OK
+        assert lib.blk_forward_q8_0_workspace_size(C.byref(d), C.byref(q8)) == _abi.BLK_OK
+        want = al(2 * qkv * D) + al(2 * D * 256) + n_up * al(2 * F * D) + al(2 * D * F)
+        assert q8.value - base.value == want
+    bad = _block(intermediate=12)
+    assert lib.blk_forward_q8_0_workspace_size(C.byref(bad), C.byref(q8)) == _abi.BLK_EINVAL
+
+
 def test_mlp_validation(lib):
     d = _abi.MlpDesc(128, 256, 688, _abi.BLK_ACT_SWIGLU)
     st = lib.blk_mlp(C.byref(d), FAKE, None, FAKE, None, FAKE, None, None, None, FAKE, FAKE,

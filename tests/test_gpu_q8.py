@@ -7,7 +7,8 @@
   dequantized weight d * q, on codes and scales made by the oracle (so the
   GEMM is checked independently of the GPU quantizer), ragged m, n and k.
 - blk_forward_q8_0: every block variant with Q8_0 projections against the
-  oracle block on the dequantized weights, small and full size."""
+  oracle block on the dequantized weights, small and full size, by both of
+  its paths (W8A16 GEMMs; weights expanded once for the dense GEMM)."""
 import numpy as np
 import pytest
 import torch
@@ -93,20 +94,27 @@ def test_linear_q8_0_matches_gpu_quantizer_path():
 PROJ = {"qkv": "w_qkv", "o": "w_o", "gate": "w_gate", "up": "w_up", "down": "w_down"}
 
 Q8_SMALL = {
-    "stablelm2_small": scaled(BLOCK_CONFIGS["stablelm2_1p6b"], batch=2, seq=200, hidden=256,
+    "stablelm2_small": scaled(BLOCK_CONFIGS["stablelm2_1p6b"], batch=2, seq=260, hidden=256,
                               n_heads=4, n_kv_heads=4, intermediate=704),
     "bloom_small": scaled(BLOCK_CONFIGS["bloom_560m"], batch=2, seq=256, hidden=256, n_heads=4,
                           n_kv_heads=4, intermediate=1024),
     "olmo2_small": scaled(BLOCK_CONFIGS["olmo2_1b"], batch=2, seq=300, hidden=256, n_heads=2,
                           n_kv_heads=2, intermediate=512),
-    "stablelm2_12b_small": scaled(BLOCK_CONFIGS["stablelm2_12b"], batch=1, seq=260, hidden=320,
+    "stablelm2_12b_small": scaled(BLOCK_CONFIGS["stablelm2_12b"], batch=2, seq=260, hidden=320,
                                   n_heads=8, n_kv_heads=2, intermediate=512),
 }
 
 
-def _q8_block(cfg, x, w):
-    """GPU block with Q8_0 projections (oracle-made codes) and the oracle
-    block on the dequantized weights."""
+# blk_forward_q8_0's two ways to run the projections, chosen by the workspace
+# size (every case here has at least 512 tokens): W8A16 GEMMs that expand the
+# codes on chip, or the weights expanded once into the workspace's tail and
+# multiplied by the dense GEMM
+PATHS = {"w8a16": blk.forward_workspace_size, "dequant": blk.forward_q8_0_workspace_size}
+
+
+def _q8_inputs(cfg, w):
+    """The dense slots on the GPU, oracle-made Q8_0 codes and scales, and the
+    oracle's dequantized weights."""
     dense = {k: to_dev(t) for k, t in w.items() if k not in PROJ.values()}
     q8, deq = {}, dict(w)
     for name, slot in PROJ.items():
@@ -116,28 +124,46 @@ def _q8_block(cfg, x, w):
         q8["q_" + name] = torch.from_numpy(qo).cuda()
         q8["d_" + name] = torch.from_numpy(np.ascontiguousarray(do.T)).cuda()
         deq[slot] = oracle.q8_0_dequantize(qo, do)
-    y = blk.forward_q8_0(cfg, dense, q8, to_dev(x))
+    return dense, q8, deq
+
+
+def _q8_run(cfg, x, dense, q8, path):
+    assert cfg.tokens >= 512  # below it both workspaces take the W8A16 GEMMs
+    ws = torch.empty(PATHS[path](cfg, cfg.batch, cfg.seq), dtype=torch.uint8, device="cuda")
+    y = blk.forward_q8_0(cfg, dense, q8, to_dev(x), workspace=ws)
     blk.check_device_status()
-    return y, deq
+    return y
 
 
+def _q8_block(cfg, x, w, path="w8a16"):
+    """GPU block with Q8_0 projections (oracle-made codes) and the oracle
+    block on the dequantized weights."""
+    dense, q8, deq = _q8_inputs(cfg, w)
+    return _q8_run(cfg, x, dense, q8, path), deq
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("name", sorted(Q8_SMALL))
-def test_block_q8_small(name):
+def test_block_q8_small(name, path):
     cfg = Q8_SMALL[name]
     x, w = workloads.block_inputs(cfg)
-    y, deq = _q8_block(cfg, x, w)
+    y, deq = _q8_block(cfg, x, w, path)
     ref = oracle.block_forward(cfg, x, deq)["y"]
     tol = 5e-2 if cfg.norm_place == "post" else 2e-2   # post-norm: the bf16 storage floor
-    check(y, ref, f"q8 block {name}", unit_scale=True, abs_tol=tol, storage=cfg.dtype)
+    check(y, ref, f"q8 block {name} ({path})", unit_scale=True, abs_tol=tol, storage=cfg.dtype)
 
 
 def test_block_q8_full_size_sampled_rows():
-    """The StableLM-2-1.6B block with Q8_0 projections at full size, on 48
-    seeded rows the oracle evaluates one by one."""
+    """The StableLM-2-1.6B block with Q8_0 projections at full size, both
+    paths, on 48 seeded rows the oracle evaluates one by one."""
     cfg = BLOCK_CONFIGS["stablelm2_1p6b"]
     x, w = workloads.block_inputs(cfg)
-    y, deq = _q8_block(cfg, x, w)
+    dense, q8, deq = _q8_inputs(cfg, w)
     rows = workloads.sample_rows(cfg.tokens, 48, seed=cfg.seed)
     ref = oracle.block_forward(cfg, x, deq, rows=rows)["y"]
-    got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
-    check(got, ref, "q8 stablelm2_1p6b sampled rows", unit_scale=True, storage=cfg.dtype)
+    idx = torch.as_tensor(rows, device="cuda")
+    for path in sorted(PATHS):
+        y = _q8_run(cfg, x, dense, q8, path)
+        got = y.reshape(cfg.tokens, cfg.hidden)[idx]
+        check(got, ref, f"q8 stablelm2_1p6b sampled rows ({path})", unit_scale=True,
+              storage=cfg.dtype)
