@@ -465,7 +465,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 // p = 2^(logit - m) in the storage type, and the row sum; P is
                 // held in registers until the previous PV has read P_x
                 const uint64_t mul2 = f2_pack(ALIBI ? 1.f : scale_l2, ALIBI ? 1.f : scale_l2);
-                const uint64_t neg2 = f2_pack(sk - m_used, sk - m_used);
+                const float off = ALIBI ? sk - m_used : -m_used;
+                const uint64_t neg2 = f2_pack(off, off);
                 uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
                 uint32_t pk[kTK / 2];
 #pragma unroll

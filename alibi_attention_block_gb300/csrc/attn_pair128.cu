@@ -54,7 +54,12 @@ struct Cfg {
     static constexpr int kStages = 2;
     static constexpr int kOffKV = 2 * kQBytes;         // Q_A, Q_B
     static constexpr int kOffBar = kOffKV + kStages * 2 * kKVBytes;
-    static constexpr int kSmem = kOffBar + 256 + 1024;
+    // ALiBi: per softmax warpgroup an mbarrier (its four warps' arrivals)
+    // and two 128-float tables slope*log2(e)*i (i = key column within a
+    // tile), one per item parity
+    static constexpr int kOffTabBar = kOffBar + 256;
+    static constexpr int kOffBias = kOffTabBar + 16;
+    static constexpr int kSmem = kOffBias + 2 * 2 * kTK * 4 + 1024;
     static constexpr uint32_t kColP = 128;             // P_x at kColP + 64 x
     static constexpr uint32_t kColO = 256;             // O_x at kColO + D x
     static constexpr uint32_t kTmemCols = 512;
@@ -98,6 +103,12 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
     constexpr int kStages = Cfg::kStages;
+    // With ALiBi the key tiles are walked from the diagonal down: the bias
+    // +slope*j is largest there, so the row max is set by the first tile and
+    // the O rescale (max grown past 2^8) stays rare; walked upwards, the max
+    // rises by slope*128*log2(e) per tile, past 2^8 on most tiles for
+    // slopes above 1/23.
+    constexpr bool kRev = ALIBI;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const uint32_t sQ = smem_u32(smem);     // Q_x at x tiles
@@ -131,6 +142,8 @@ __global__ void __launch_bounds__(kP128Threads, 1)
             mbar_init(q_full(x), 1);
             mbar_init(q_empty(x), 1);
         }
+        if (ALIBI)
+            for (int x = 0; x < 2; ++x) mbar_init(sQ + Cfg::kOffTabBar + 8u * x, 4);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(k_full(i), 1);
             mbar_init(v_full(i), 1);
@@ -181,6 +194,7 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                 }
                 const int nkv = c.n_kv();
                 for (int j = 0; j < nkv && ok; ++j, ++gkv) {
+                    const int kt = kRev ? nkv - 1 - j : j;  // key tile of shared step j
                     const int st = gkv % kStages;
                     const uint32_t ph = (gkv / kStages) & 1;
                     const uint32_t sK = sKV + (2 * st) * Cfg::kKVBytes;
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                     mbar_expect_tx(k_full(st), Cfg::kKVBytes);
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
-                        tma_load_3d_hint(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, j * kTK,
+                        tma_load_3d_hint(sK + sub * kTK * 128, &tmK, k_full(st), sub * 64, kt * kTK,
                                     c.b * a.Hk + c.g, pol_kv);
                     if (!mbar_wait_inl(v_empty(st), ph ^ 1u, a.err)) {
                         ok = false;
@@ -201,7 +215,7 @@ __global__ void __launch_bounds__(kP128Threads, 1)
 #pragma unroll
                     for (int sub = 0; sub < Cfg::kSub; ++sub)
                         tma_load_3d_hint(sK + Cfg::kKVBytes + sub * kTK * 128, &tmV, v_full(st),
-                                    sub * 64, j * kTK, c.b * a.Hk + c.g, pol_kv);
+                                    sub * 64, kt * kTK, c.b * a.Hk + c.g, pol_kv);
                 }
                 c.next(a, nq, np, n_items);
             }
@@ -258,12 +272,13 @@ __global__ void __launch_bounds__(kP128Threads, 1)
             int gkv = 0;
             int itq[2] = {0, 0};
             bool ok = true;
-            auto s_step = [&](int x, int j, int nx, int gj) -> bool {
-                // QK^T of key tile j for query tile x (K slot gj already waited)
-                if (j >= nx) return true;
-                if (j == 0 && !mbar_wait_inl(q_full(x), itq[x] & 1, a.err)) return false;
+            auto s_step = [&](int x, int j, int lo, int hi, int gj) -> bool {
+                // QK^T of shared step j for query tile x, whose steps are
+                // [lo, hi) (K slot gj already waited)
+                if (j < lo || j >= hi) return true;
+                if (j == lo && !mbar_wait_inl(q_full(x), itq[x] & 1, a.err)) return false;
                 if (!issue_s(x, gj % kStages)) return false;
-                if (j == nx - 1) {
+                if (j == hi - 1) {
                     tc_commit(q_empty(x));
                     ++itq[x];
                 }
@@ -271,9 +286,13 @@ __global__ void __launch_bounds__(kP128Threads, 1)
             };
             while (ok && c.valid) {
                 const int nA = c.nA, nB = c.nB, nkv = c.n_kv();
-                // key tile 0: S_A(0), S_B(0)
+                // each tile's shared steps: its first n key tiles in key order,
+                // its last n when the walk runs down from the diagonal
+                const int loA = kRev ? nkv - nA : 0, hiA = kRev ? nkv : nA;
+                const int loB = kRev ? nkv - nB : 0, hiB = kRev ? nkv : nB;
+                // step 0: S_A(0), S_B(0) (where the tiles take part)
                 if (!mbar_wait_inl(k_full(gkv % kStages), (gkv / kStages) & 1, a.err)) break;
-                if (!s_step(0, 0, nA, gkv) || !s_step(1, 0, nB, gkv)) break;
+                if (!s_step(0, 0, loA, hiA, gkv) || !s_step(1, 0, loB, hiB, gkv)) break;
                 tc_commit(k_empty(gkv % kStages));
                 for (int j = 0; j < nkv; ++j) {
                     const int gj = gkv + j;
@@ -289,19 +308,19 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                         break;
                     }
                     // PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-                    if (j < nA && !issue_pv(0, stj, j == 0)) {
+                    if (j >= loA && j < hiA && !issue_pv(0, stj, j == loA)) {
                         ok = false;
                         break;
                     }
-                    if (more && !s_step(0, j + 1, nA, gj + 1)) {
+                    if (more && !s_step(0, j + 1, loA, hiA, gj + 1)) {
                         ok = false;
                         break;
                     }
-                    if (j < nB && !issue_pv(1, stj, j == 0)) {
+                    if (j >= loB && j < hiB && !issue_pv(1, stj, j == loB)) {
                         ok = false;
                         break;
                     }
-                    if (more && !s_step(1, j + 1, nB, gj + 1)) {
+                    if (more && !s_step(1, j + 1, loB, hiB, gj + 1)) {
                         ok = false;
                         break;
                     }
@@ -329,6 +348,7 @@ __global__ void __launch_bounds__(kP128Threads, 1)
         bool pend = false;
         float pend_l = 0.f;
         int64_t pend_row = -1;
+        int n_done = 0;  // items this warpgroup has started (ALiBi table parity)
         // O / l of the previous item, 32 columns at a time, once its last PV
         // has completed
         auto flush = [&]() {
@@ -360,12 +380,28 @@ __global__ void __launch_bounds__(kP128Threads, 1)
             float m_used = -INFINITY;
             float l = 0.f;
             float slope_l2 = 0.f;
+            uint32_t bias_tab = 0;
             if constexpr (ALIBI) {
                 const float slope = a.slopes ? a.slopes[c.h]
                                              : exp2f(-8.0f * static_cast<float>(c.h + 1) /
                                                      static_cast<float>(a.H));
                 slope_l2 = slope * kLog2e;
+                // the item's column bias table, in the buffer the warpgroup's
+                // previous item did not use (its last readers may still be on
+                // that item); each warp's arrival publishes its 32 entries,
+                // and no warp reads before all four have arrived
+                const int off = Cfg::kOffBias + (2 * x + (n_done & 1)) * kTK * 4;
+                reinterpret_cast<float*>(smem + off)[row] = slope_l2 * static_cast<float>(row);
+                bias_tab = sQ + off;
+                const uint32_t tab_bar = sQ + Cfg::kOffTabBar + 8u * x;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tab_bar);
+                if (!mbar_wait_inl(tab_bar, n_done & 1, a.err)) {
+                    ok = false;
+                    break;
+                }
             }
+            ++n_done;
             for (int j = 0; j < nx; ++j, ++g) {
                 if (!mbar_wait_inl(s_full(x), g & 1, a.err)) {
                     ok = false;
@@ -377,15 +413,32 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_free);
-                const int kbase = j * kTK;
+                const int kt = kRev ? nx - 1 - j : j;  // key tile of this step
+                const int kbase = kt * kTK;
+                // ALiBi: u = s*scale*log2(e) + slope*log2(e)*i, one paired FMA
+                // per two scores from the column table; the tile's uniform
+                // part slope*log2(e)*kbase joins the max and the exponent
+                // (entry 1 of the table is slope*log2(e) itself: read back, so
+                // that the slope holds no register across the tile loop)
+                const float sk =
+                    ALIBI ? ld_shared_f32(bias_tab + 4) * static_cast<float>(kbase) : 0.f;
                 if constexpr (ALIBI) {
-                    const float sk = slope_l2 * static_cast<float>(kbase);
+                    const uint64_t sc2 = f2_pack(scale_l2, scale_l2);
 #pragma unroll
-                    for (int i = 0; i < kTK; ++i)
-                        r[i] = __float_as_uint(fmaf(__uint_as_float(r[i]), scale_l2,
-                                                    fmaf(slope_l2, static_cast<float>(i), sk)));
+                    for (int i = 0; i < kTK; i += 4) {
+                        uint64_t c01, c23;
+                        ld_shared_v2_u64(bias_tab + i * 4, c01, c23);
+                        float u0, u1, u2, u3;
+                        ffma2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), sc2, c01, u0, u1);
+                        ffma2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]), sc2, c23, u2,
+                              u3);
+                        r[i] = __float_as_uint(u0);
+                        r[i + 1] = __float_as_uint(u1);
+                        r[i + 2] = __float_as_uint(u2);
+                        r[i + 3] = __float_as_uint(u3);
+                    }
                 }
-                if (j == qt || kbase + kTK > a.S) {
+                if (kt == qt || kbase + kTK > a.S) {
                     const int lim = min(qpos, a.S - 1) - kbase;
 #pragma unroll
                     for (int i = 0; i < kTK; ++i)
@@ -401,13 +454,15 @@ __global__ void __launch_bounds__(kP128Threads, 1)
                 }
                 float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
                 if constexpr (!ALIBI) mx *= scale_l2;
+                if constexpr (ALIBI) mx += sk;
                 float corr = 1.f;
                 if (mx > m_used + kRescaleThreshold) {
                     corr = ex2_approx(m_used - mx);
                     m_used = mx;
                 }
                 const uint64_t mul2 = f2_pack(ALIBI ? 1.f : scale_l2, ALIBI ? 1.f : scale_l2);
-                const uint64_t neg2 = f2_pack(-m_used, -m_used);
+                const float off = ALIBI ? sk - m_used : -m_used;
+                const uint64_t neg2 = f2_pack(off, off);
                 uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
                 uint32_t pk[kTK / 2];
 #pragma unroll

@@ -220,6 +220,10 @@ ATTN_CASES = [
     (2, 16, 4, 1536, 128, False),  # more items than SMs at head_dim 128, GQA
     (1, 3, 3, 640, 128, False),    # odd tile count: the last pair has one query tile
     (1, 4, 4, 256, 128, True),
+    # ALiBi (key tiles walked from the diagonal down) with more items than
+    # SMs, an odd tile count (the last pair has one query tile) and a ragged S
+    (2, 16, 16, 1100, 64, True),
+    (2, 16, 16, 1100, 128, True),
     (1, 4, 1, 300, 160, False),
     (2, 2, 2, 129, 160, False),
     # GQA-packed tiles (the group's query heads in the rows of one tile)
