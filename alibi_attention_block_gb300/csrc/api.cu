@@ -198,7 +198,7 @@ bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uin
 
 bool make_tmap_2d_plain(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes,
                         const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                        uint32_t box_rows) {
+                        uint32_t box_rows, bool swizzle128) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -206,7 +206,8 @@ bool make_tmap_2d_plain(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

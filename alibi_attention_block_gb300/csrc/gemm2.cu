@@ -42,7 +42,7 @@ constexpr int kPairABytes = kBM * kBK * 2;    // this CTA's 128 rows of A
 constexpr int kPairBBytes = (kPairBN / 2) * kBK * 2;  // this CTA's half of B
 constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
 constexpr int kPairOffBar = kPairStages * kPairStageBytes;
-constexpr int kPairOffEpi = kPairOffBar + 256;
+constexpr int kPairOffEpi = kPairOffBar + 1024;  // staging boxes 1024-byte aligned (swizzle)
 constexpr int kPairSmem = kPairOffEpi + kEpiWarps * 32 * 128 + 1024;
 constexpr uint32_t kPairTmemCols = 2 * kPairBN;  // two accumulators
 
@@ -50,7 +50,10 @@ template <typename T, int EPI, int ROT, bool SPLIT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs g,
+                     const __grid_constant__ CUtensorMap tmB2,
+                     const __grid_constant__ CUtensorMap tmO,
+                     const __grid_constant__ CUtensorMap tmO2,
+                     const __grid_constant__ CUtensorMap tmO3, const GemmArgs g,
                      const __grid_constant__ RopeParams rp) {
     constexpr int BN = kPairBN;
     constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
@@ -230,13 +233,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (run) {
                 epilogue_tile<T, BN, EPI, ROT, SPLIT>(g, rp, tbase, m0 + row, nt,
                                                       stg0 + ew * (32 * 128), lane,
-                                                      m0 + quarter * 32, part, un.q, row, half);
+                                                      m0 + quarter * 32, part, un.q, row, half,
+                                                      g.tma_out ? &tmO : nullptr, &tmO2, &tmO3);
                 if (cnt && lane == 0) *cnt = 0u;  // every segment has arrived: ready for reuse
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_lead0 + 8u * acc);
         }
+        // the warp's TMA stores have read their staging boxes and written
+        // the output before the CTA ends
+        if (lane == 0) bulk_wait<0>();
     }
     // every MMA of the pair has completed (both epilogues consumed the last
     // accumulators) and every cross-CTA signal has landed
@@ -271,8 +278,8 @@ int max_pairs(const void* kern, const cudaLaunchConfig_t& cfg_in, int num_sms) {
 
 template <typename T, int EPI, int ROT = 0>
 cudaError_t launch_pair_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
-                            const GemmArgs& g, const RopeParams& rp, int num_sms,
-                            cudaStream_t s) {
+                            const CUtensorMap (&to)[3], const GemmArgs& g, const RopeParams& rp,
+                            int num_sms, cudaStream_t s) {
     constexpr int kBNOut = EPI == EPI_SWIGLU ? kPairBN / 2 : kPairBN;
     constexpr bool kCanSplit = EPI != EPI_SWIGLU;
     auto kern = gemm_pair_kernel<T, EPI, ROT, false>;
@@ -319,30 +326,55 @@ cudaError_t launch_pair_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const 
             R * 2 * sp <= kGemmSplitSlots && R * 2 * kEpiWarps <= kGemmSplitCounters) {
             ga.split_s = static_cast<int>(sp);
             ga.split_base = static_cast<int>((rounds - 1) * G);
-            return cudaLaunchKernelEx(&cfg, kern_split, ta, tb, tb2, ga, rp);
+            return cudaLaunchKernelEx(&cfg, kern_split, ta, tb, tb2, to[0], to[1], to[2], ga, rp);
         }
     }
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, ga, rp);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, to[0], to[1], to[2], ga, rp);
 }
 
 template <typename T>
 cudaError_t launch_pair_t(DType dt, int epi, const void* a, const void* b, const void* b2,
                           const GemmArgs& g, const RopeParams& rp, int num_sms, cudaStream_t s) {
-    CUtensorMap ta, tb, tb2;
+    CUtensorMap ta, tb, tb2, to[3];
     if (!make_tmap_2d(&ta, dt, a, g.M, g.K, kBM)) return cudaErrorInvalidValue;
     if (!make_tmap_2d(&tb, dt, b, g.N, g.K, kPairBN / 2)) return cudaErrorInvalidValue;
     tb2 = tb;
     if (epi == EPI_SWIGLU && !make_tmap_2d(&tb2, dt, b2, g.N, g.K, kPairBN / 2))
         return cudaErrorInvalidValue;
+    // TMA stores of the epilogue's staged boxes (32 rows x 64 16-bit values,
+    // 128-byte swizzle): the [M, N] output of LINEAR, GELU and SWIGLU, or
+    // QKV's q, k, v ([B * heads, S, d]) when a box holds 64 columns of one
+    // head (head_dim % 64 == 0) and 32 positions of one sequence (S % 32 ==
+    // 0). fp32 outputs keep their staged per-warp stores of whole lines;
+    // they measured faster than the TMA's.
+    GemmArgs gt = g;
+    gt.tma_out = 0;
+    to[0] = to[1] = to[2] = ta;
+    const CUtensorMapDataType ty =
+        dt == DType::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (epi == EPI_QKV) {
+        if (g.d % 64 == 0 && g.S > 0 && g.S % 32 == 0 && g.M % g.S == 0) {
+            const uint64_t B = static_cast<uint64_t>(g.M / g.S);
+            if (!make_tmap_3d(&to[0], dt, g.q, B * g.H, g.S, g.d, 32) ||
+                !make_tmap_3d(&to[1], dt, g.k, B * g.Hk, g.S, g.d, 32) ||
+                !make_tmap_3d(&to[2], dt, g.v, B * g.Hk, g.S, g.d, 32))
+                return cudaErrorInvalidValue;
+            gt.tma_out = 1;
+        }
+    } else if (!(epi == EPI_LINEAR && g.out_f32)) {
+        if (!make_tmap_2d_plain(&to[0], ty, 2, g.out, g.M, g.N, 64, 32, true))
+            return cudaErrorInvalidValue;
+        gt.tma_out = 1;
+    }
     switch (epi) {
-        case EPI_LINEAR: return launch_pair_cfg<T, EPI_LINEAR>(ta, tb, tb2, g, rp, num_sms, s);
-        case EPI_SWIGLU: return launch_pair_cfg<T, EPI_SWIGLU>(ta, tb, tb2, g, rp, num_sms, s);
-        case EPI_GELU: return launch_pair_cfg<T, EPI_GELU>(ta, tb, tb2, g, rp, num_sms, s);
+        case EPI_LINEAR: return launch_pair_cfg<T, EPI_LINEAR>(ta, tb, tb2, to, gt, rp, num_sms, s);
+        case EPI_SWIGLU: return launch_pair_cfg<T, EPI_SWIGLU>(ta, tb, tb2, to, gt, rp, num_sms, s);
+        case EPI_GELU: return launch_pair_cfg<T, EPI_GELU>(ta, tb, tb2, to, gt, rp, num_sms, s);
         case EPI_QKV:
             switch (rp.span) {
-                case 0: return launch_pair_cfg<T, EPI_QKV, 0>(ta, tb, tb2, g, rp, num_sms, s);
-                case 16: return launch_pair_cfg<T, EPI_QKV, 16>(ta, tb, tb2, g, rp, num_sms, s);
-                case 32: return launch_pair_cfg<T, EPI_QKV, 32>(ta, tb, tb2, g, rp, num_sms, s);
+                case 0: return launch_pair_cfg<T, EPI_QKV, 0>(ta, tb, tb2, to, gt, rp, num_sms, s);
+                case 16: return launch_pair_cfg<T, EPI_QKV, 16>(ta, tb, tb2, to, gt, rp, num_sms, s);
+                case 32: return launch_pair_cfg<T, EPI_QKV, 32>(ta, tb, tb2, to, gt, rp, num_sms, s);
                 default: return cudaErrorInvalidValue;
             }
         default: return cudaErrorInvalidValue;

@@ -107,6 +107,51 @@ __device__ __forceinline__ void store_chunk_f32(const GemmArgs& g, uint32_t stg,
     __syncwarp();
 }
 
+// One thread's 32 output values of one row into its warp's staging box of
+// 32 rows x 128 bytes, laid out for a TMA store with the 128-byte swizzle
+// (16-byte piece p of row r at r * 128 + ((p ^ (r & 7)) << 4), the box
+// 1024-byte aligned): 16-bit values as pieces p0 .. p0 + 3 (half a box row),
+// fp32 values as all eight pieces.
+template <typename T>
+__device__ __forceinline__ void stage_row(uint32_t stg, int r, int p0, bool f32,
+                                          const float (&o)[32]) {
+    const uint32_t row = stg + r * 128;
+    if (f32) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            st_shared_v4(row + ((v ^ (r & 7)) << 4), __float_as_uint(o[4 * v]),
+                         __float_as_uint(o[4 * v + 1]), __float_as_uint(o[4 * v + 2]),
+                         __float_as_uint(o[4 * v + 3]));
+    } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            st_shared_v4(row + (((p0 + v) ^ (r & 7)) << 4),
+                         dt_traits<T>::pack2(o[8 * v], o[8 * v + 1]),
+                         dt_traits<T>::pack2(o[8 * v + 2], o[8 * v + 3]),
+                         dt_traits<T>::pack2(o[8 * v + 4], o[8 * v + 5]),
+                         dt_traits<T>::pack2(o[8 * v + 6], o[8 * v + 7]));
+    }
+}
+
+// Around one staged box: before its first chunk is written, the previous
+// box's store has read the staging buffer; after its last, the writes are
+// made visible to the TMA and one lane stores the box (x, y: its first
+// column and row; a box wholly past N or M is skipped, a partial one is
+// clipped by the TMA).
+__device__ __forceinline__ void stage_begin(int lane) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+}
+__device__ __forceinline__ void stage_store(const CUtensorMap* tmo, uint32_t stg, int lane, int x,
+                                            int y, const GemmArgs& g) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && x < g.N && y < g.M) {
+        tma_store_2d(tmo, stg, x, y);
+        bulk_commit();
+    }
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
 __device__ __forceinline__ float gelu_tanh_f(float z) {
@@ -114,11 +159,18 @@ __device__ __forceinline__ float gelu_tanh_f(float z) {
     return 0.5f * z * (1.0f + tanhf(k0 * (z + 0.044715f * z * z * z)));
 }
 
+// tmo: the output's tensor map for TMA stores of staged boxes (16-bit
+// outputs of LINEAR, GELU, SWIGLU: [M, N]; QKV: q, with tmo_k and tmo_v, each
+// [B * heads, S, d]; stg then a 1024-byte-aligned 4 KB staging box), or
+// nullptr for per-thread stores.
 template <typename T, int BN, int EPI, int ROT, bool SPLIT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParams& rp,
                                               uint32_t tbase, int m, int nt, uint32_t stg,
                                               int lane, int m_base, const float* part, int self,
-                                              int trow, int half) {
+                                              int trow, int half,
+                                              const CUtensorMap* tmo = nullptr,
+                                              const CUtensorMap* tmo_k = nullptr,
+                                              const CUtensorMap* tmo_v = nullptr) {
     // this warp's half of the tile's 32-column chunks
     constexpr int kChunks = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 32;
     const int c_begin = half * (kChunks / 2), c_end = c_begin + kChunks / 2;
@@ -131,6 +183,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             tmem_ld32(tbase + c * 32, gr);
             tmem_ld32(tbase + kHalf + c * 32, ur);
             const int n0 = nt * kHalf + c * 32;
+            if (tmo) {
+                // two chunks per box (64 columns of 16-bit values)
+                float o[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+                const int k = c - c_begin;
+                if ((k & 1) == 0) stage_begin(lane);
+                stage_row<T>(stg, lane, (k & 1) * 4, false, o);
+                if ((k & 1) == 1 || c + 1 == c_end)
+                    stage_store(tmo, stg, lane, nt * kHalf + (c_begin + (k & ~1)) * 32, m_base, g);
+                continue;
+            }
             if (!row_ok || n0 >= g.N) continue;
             float o[32];
 #pragma unroll
@@ -181,10 +246,69 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                     }
                 }
             }
-            T* base = static_cast<T*>(which == 0 ? g.q : (which == 1 ? g.k : g.v));
             const int nheads = which == 0 ? g.H : g.Hk;
+            if (tmo) {
+                // two chunks (64 columns of one head: head_dim % 64 == 0) per
+                // box of the warp's 32 positions (S % 32 == 0: one sequence)
+                const int k = c - c_begin;
+                if ((k & 1) == 0) stage_begin(lane);
+                stage_row<T>(stg, lane, (k & 1) * 4, false, o);
+                if ((k & 1) == 1) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && m_base < g.M) {
+                        const int b0 = m_base / g.S;
+                        tma_store_3d(which == 0 ? tmo : (which == 1 ? tmo_k : tmo_v), stg,
+                                     dd0 - 32, m_base - b0 * g.S, b0 * nheads + head);
+                        bulk_commit();
+                    }
+                }
+                continue;
+            }
+            T* base = static_cast<T*>(which == 0 ? g.q : (which == 1 ? g.k : g.v));
             T* dst = base + ((static_cast<int64_t>(b) * nheads + head) * g.S + s) * d + dd0;
             store_row32(dst, o, 32);
+        }
+    } else if (tmo) {
+        // TMA stores of staged boxes: fp32 output one chunk per box (32
+        // columns), 16-bit output two (64 columns); a chunk past N is staged
+        // as it is and clipped by the store
+        const bool f32 = EPI == EPI_LINEAR && g.out_f32;
+#pragma unroll 1
+        for (int c = c_begin; c < c_end; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c * 32, r);
+            const int n0 = nt * BN + c * 32;
+            const int valid = g.N - n0;
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+            if (valid > 0) {
+                if constexpr (SPLIT)
+                    if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
+                if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
+                if constexpr (EPI == EPI_GELU) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
+                }
+                const int64_t off = static_cast<int64_t>(m) * g.N + n0;
+                if (row_ok && g.res1) {
+                    if (g.res1_f32) add_row32(static_cast<const float*>(g.res1) + off, o, valid);
+                    else add_row32(static_cast<const T*>(g.res1) + off, o, valid);
+                }
+                if (row_ok && g.res2) {
+                    if (g.res2_f32) add_row32(static_cast<const float*>(g.res2) + off, o, valid);
+                    else add_row32(static_cast<const T*>(g.res2) + off, o, valid);
+                }
+            }
+            const int k = c - c_begin;
+            const bool first = f32 || (k & 1) == 0;
+            const bool last = f32 || (k & 1) == 1 || c + 1 == c_end;
+            if (first) stage_begin(lane);
+            stage_row<T>(stg, lane, f32 ? 0 : (k & 1) * 4, f32, o);
+            if (last)
+                stage_store(tmo, stg, lane, f32 ? n0 : nt * BN + (c_begin + (k & ~1)) * 32,
+                            m_base, g);
         }
     } else {
 #pragma unroll 1

@@ -74,6 +74,7 @@ struct GemmArgs {
     unsigned* split_cnt;
     int split_s;          // segments per split unit (set by launch_gemm; 1 = none)
     int split_base;       // first split unit
+    int tma_out;          // pair GEMM: the output goes out by TMA stores (set by its launcher)
 };
 // scratch of a split GEMM: kGemmSplitSlots partial 128 x 256 fp32 tiles, then
 // kGemmSplitCounters counters
@@ -192,11 +193,12 @@ blk_status report_error_status(blk_status st, const char* fmt, ...);
 // 2D row-major [rows, cols] map with a {64, box_rows} box and 128B swizzle.
 bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uint64_t cols,
                   uint32_t box_rows);
-// 2D row-major [rows, cols] map of any element type, no swizzle, with a
-// {box_cols, box_rows} box.
+// 2D row-major [rows, cols] map of any element type with a {box_cols,
+// box_rows} box: no swizzle, or the 128-byte swizzle (box rows of 128 bytes,
+// shared-memory side 1024-byte aligned).
 bool make_tmap_2d_plain(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes,
                         const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                        uint32_t box_rows);
+                        uint32_t box_rows, bool swizzle128 = false);
 // 3D [planes, rows, cols] map with a {64, box_rows, 1} box and 128B swizzle.
 bool make_tmap_3d(CUtensorMap* m, DType dt, const void* base, uint64_t planes, uint64_t rows,
                   uint64_t cols, uint32_t box_rows);
