@@ -213,17 +213,18 @@ bool make_tmap_2d_plain(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_
 }
 
 bool make_tmap_3d(CUtensorMap* m, DType dt, const void* base, uint64_t planes, uint64_t rows,
-                  uint64_t cols, uint32_t box_rows) {
+                  uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {cols, rows, planes};
     const cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
-    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t box[3] = {box_cols, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(m, dt == DType::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                           3, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

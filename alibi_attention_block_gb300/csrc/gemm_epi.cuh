@@ -133,6 +133,20 @@ __device__ __forceinline__ void stage_row(uint32_t stg, int r, int p0, bool f32,
     }
 }
 
+// One thread's 32 16-bit values as one 64-byte row of a 32 x 64-byte staging
+// box laid out for a TMA store with the 64-byte swizzle (16-byte piece p of
+// row r at r * 64 + ((p ^ ((r >> 1) & 3)) << 4), the box 512-byte aligned).
+template <typename T>
+__device__ __forceinline__ void stage_row64(uint32_t stg, int r, const float (&o)[32]) {
+    const uint32_t row = stg + r * 64;
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        st_shared_v4(row + ((v ^ ((r >> 1) & 3)) << 4), dt_traits<T>::pack2(o[8 * v], o[8 * v + 1]),
+                     dt_traits<T>::pack2(o[8 * v + 2], o[8 * v + 3]),
+                     dt_traits<T>::pack2(o[8 * v + 4], o[8 * v + 5]),
+                     dt_traits<T>::pack2(o[8 * v + 6], o[8 * v + 7]));
+}
+
 // Around one staged box: before its first chunk is written, the previous
 // box's store has read the staging buffer; after its last, the writes are
 // made visible to the TMA and one lane stores the box (x, y: its first
@@ -247,6 +261,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 }
             }
             const int nheads = which == 0 ? g.H : g.Hk;
+            if (tmo && g.tma_out == 2) {
+                // one chunk (32 columns of one head) per box of the warp's 32
+                // positions (S % 32 == 0: one sequence)
+                stage_begin(lane);
+                stage_row64<T>(stg, lane, o);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && m_base < g.M) {
+                    const int b0 = m_base / g.S;
+                    tma_store_3d(which == 0 ? tmo : (which == 1 ? tmo_k : tmo_v), stg, dd0,
+                                 m_base - b0 * g.S, b0 * nheads + head);
+                    bulk_commit();
+                }
+                continue;
+            }
             if (tmo) {
                 // two chunks (64 columns of one head: head_dim % 64 == 0) per
                 // box of the warp's 32 positions (S % 32 == 0: one sequence)

@@ -74,7 +74,9 @@ struct GemmArgs {
     unsigned* split_cnt;
     int split_s;          // segments per split unit (set by launch_gemm; 1 = none)
     int split_base;       // first split unit
-    int tma_out;          // pair GEMM: the output goes out by TMA stores (set by its launcher)
+    // pair GEMM: the output goes out by TMA stores (set by its launcher): 1
+    // in boxes of 64 columns, 2 (QKV at head_dim % 64 != 0) of 32
+    int tma_out;
 };
 // scratch of a split GEMM: kGemmSplitSlots partial 128 x 256 fp32 tiles, then
 // kGemmSplitCounters counters
@@ -199,8 +201,10 @@ bool make_tmap_2d(CUtensorMap* m, DType dt, const void* base, uint64_t rows, uin
 bool make_tmap_2d_plain(CUtensorMap* m, CUtensorMapDataType type, uint32_t elem_bytes,
                         const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
                         uint32_t box_rows, bool swizzle128 = false);
-// 3D [planes, rows, cols] map with a {64, box_rows, 1} box and 128B swizzle.
+// 3D [planes, rows, cols] map of 16-bit values with a {box_cols, box_rows, 1}
+// box: 64 columns (128-byte rows) with the 128-byte swizzle, or 32 columns
+// (64-byte rows) with the 64-byte swizzle.
 bool make_tmap_3d(CUtensorMap* m, DType dt, const void* base, uint64_t planes, uint64_t rows,
-                  uint64_t cols, uint32_t box_rows);
+                  uint64_t cols, uint32_t box_rows, uint32_t box_cols = 64);
 
 }  // namespace blk

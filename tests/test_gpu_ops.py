@@ -131,6 +131,14 @@ QKV_CASES = {
     "rms_full_h32_d128_bias": (1, 43, 256, 32, 8, 128, "stacked", "rms_full", 128, 5e5, True),
     "rms_full_d64_r0": (2, 33, 256, 4, 2, 64, "stacked", "rms_full", 0, 1e4, False),
     "ln_per_head_d96_r24_bias": (1, 90, 192, 2, 1, 96, "stacked", "ln_per_head", 24, 1e4, True),
+    # the projection's TMA stores into q/k/v (S % 32 == 0, more than 128
+    # tokens: CTA-pair GEMM): boxes of 64 columns (head_dim 64, 128; stacked
+    # and interleaved; M = 320 leaves the last pair tile part past M), and
+    # of 32 columns at head_dim 160
+    "tma_boxes_d64_rope16": (2, 256, 256, 4, 4, 64, "stacked", "none", 16, 1e4, True),
+    "tma_boxes_interleaved": (2, 192, 256, 4, 4, 64, "head_interleaved", "none", 0, 1e4, True),
+    "tma_boxes_d128_rms_full": (2, 160, 256, 2, 2, 128, "stacked", "rms_full", 128, 5e5, False),
+    "tma_boxes_d160_gqa": (1, 256, 320, 8, 2, 160, "stacked", "ln_per_head", 40, 1e4, True),
 }
 
 
