@@ -45,19 +45,30 @@ struct DecCfg {
     static constexpr int kSmem = kWarps * kWarpBytes;
 };
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(DecodeArgs a) {
+// HS > 1 (head_dim 128, G >= 2): a block of HS warps shares one item and
+// its ring, each warp taking G / HS of the kv head's query heads, so each
+// warp does that share of the per-key work and an SM holds HS times the
+// warps for the same ring space (the kernel is bound by the latency of its
+// dependent work there, not by the bytes in flight).
+template <typename T, int D, int G, int HS>
+__global__ void __launch_bounds__(HS == 1 ? 32 * DecCfg<D>::kWarps : 32 * HS)
+    decode_partial_kernel(DecodeArgs a) {
     using Cfg = DecCfg<D>;
+    static_assert(HS == 1 || G % HS == 0, "head split: whole heads per warp");
+    constexpr int kQW = HS == 1 ? Cfg::kWarps : HS;  // warps of the block
+    constexpr int GW = G / HS;     // query heads of this warp
     constexpr int kCols = D / 32;  // output columns per lane
     constexpr int kChunks = D / 8; // 16-byte pieces per row
-    __shared__ __align__(16) float qs[Cfg::kWarps][G][D];  // each warp's queries, pre-scaled (log2)
+    __shared__ __align__(16) float qs[kQW][GW][D];  // each warp's queries, pre-scaled (log2)
     extern __shared__ __align__(128) uint8_t dsm[];
     const int lane = threadIdx.x & 31;
     const int wl = threadIdx.x / 32;
-    const int64_t wid = static_cast<int64_t>(blockIdx.x) * Cfg::kWarps + wl;
+    const int64_t wid = HS == 1 ? static_cast<int64_t>(blockIdx.x) * Cfg::kWarps + wl
+                                : static_cast<int64_t>(blockIdx.x);
     const int64_t total = static_cast<int64_t>(a.B) * a.Hk * a.parts;
-    if (wid >= total) return;  // whole warps exit together
-    const uint32_t ring = smem_u32(dsm) + wl * Cfg::kWarpBytes;
+    if (wid >= total) return;  // whole warps (for HS = 2 the whole block) exit together
+    const uint32_t ring = smem_u32(dsm) + (HS == 1 ? wl * Cfg::kWarpBytes : 0);
+    const int h0 = HS == 1 ? 0 : wl * GW;  // this warp's first query head of the group
     const int part = static_cast<int>(wid % a.parts);
     const int bg = static_cast<int>(wid / a.parts);
     const int b = bg / a.Hk;
@@ -70,19 +81,19 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
     const int j1 = min(n, j0 + per);
     const int nblk = j1 > j0 ? (j1 - j0 + 31) / 32 : 0;
     const float qscale = a.scale * kLog2eDec;
-    const T* qp = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.H + g * G) * D;
-    for (int i = lane; i < G * D / 8; i += 32) {
+    const T* qp = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.H + g * G + h0) * D;
+    for (int i = lane; i < GW * D / 8; i += 32) {
         float f[8];
         load8(qp + i * 8, f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) qs[wl][(i * 8) / D][(i * 8) % D + e] = f[e] * qscale;
     }
-    float slope[G];
+    float slope[GW];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < GW; ++h) {
         slope[h] = 0.f;
         if (a.alibi) {
-            const int hq = g * G + h;
+            const int hq = g * G + h0 + h;
             const float sl = a.slopes ? a.slopes[hq]
                                       : exp2f(-8.0f * static_cast<float>(hq + 1) /
                                               static_cast<float>(a.H));
@@ -95,12 +106,14 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
     // copy key block i into its stage: K rows with their 16-byte pieces
     // XOR-swizzled by row (conflict-free when lane l reads row l), V rows
     // plain (lanes read one row together); rows past the range are zeros
+    // (HS = 2: the block's 64 threads share the copies)
     auto issue = [&](int i) {
         if (i < nblk) {
             const int jb = j0 + i * 32;
             const uint32_t st = ring + (i % Cfg::kStages) * Cfg::kStageBytes;
 #pragma unroll
-            for (int q = lane; q < 32 * kChunks; q += 32) {
+            for (int q = HS == 1 ? lane : static_cast<int>(threadIdx.x); q < 32 * kChunks;
+                 q += 32 * HS) {
                 const int r = q / kChunks, c = q % kChunks;
                 const bool ok = jb + r < j1;
                 const int64_t src = static_cast<int64_t>(ok ? jb + r : j0) * D + c * 8;
@@ -110,9 +123,9 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
         }
         cp_async_commit();  // one group per block index, empty past the end
     };
-    float m[G], l[G], acc[G][kCols];
+    float m[GW], l[GW], acc[GW][kCols];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < GW; ++h) {
         m[h] = -INFINITY;
         l[h] = 0.f;
 #pragma unroll
@@ -120,13 +133,15 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
     }
 #pragma unroll
     for (int i = 0; i < Cfg::kStages - 1; ++i) issue(i);
-    __syncwarp();
+    if (HS == 1) __syncwarp();
+    else __syncthreads();  // the queries of both warps are in place
     const float qpos = static_cast<float>(n - 1);
     const uint32_t qs_addr = smem_u32(&qs[wl][0][0]);
     for (int i = 0; i < nblk; ++i) {
         issue(i + Cfg::kStages - 1);
-        cp_async_wait<Cfg::kStages - 1>();  // block i has landed (this lane's copies)
-        __syncwarp();                       // ... and every lane's
+        cp_async_wait<Cfg::kStages - 1>();  // block i has landed (this thread's copies)
+        if (HS == 1) __syncwarp();          // ... and every lane's
+        else __syncthreads();               // ... and every thread's of the block
         const uint32_t st = ring + (i % Cfg::kStages) * Cfg::kStageBytes;
         const int jb = j0 + i * 32;
         const int j = jb + lane;
@@ -134,9 +149,9 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
         // scores of key j against the G queries (log2 domain): paired
         // (f32x2) FMAs over even and odd dims, the queries read 16 bytes at
         // a time (the same address in every lane: a broadcast)
-        uint64_t sc2[G];
+        uint64_t sc2[GW];
 #pragma unroll
-        for (int h = 0; h < G; ++h) sc2[h] = f2_pack(0.f, 0.f);
+        for (int h = 0; h < GW; ++h) sc2[h] = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) {
             const uint4 kv = ld_shared_u4(st + lane * (D * 2) + ((c ^ (lane & 7)) << 4));
@@ -148,7 +163,7 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
                 k2[e2] = f2_pack(kf.x, kf.y);
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < GW; ++h) {
                 uint64_t q0, q1, q2, q3;
                 ld_shared_v2_u64(qs_addr + (h * D + c * 8) * 4, q0, q1);
                 ld_shared_v2_u64(qs_addr + (h * D + c * 8 + 4) * 4, q2, q3);
@@ -158,15 +173,15 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
                 ffma2_acc(sc2[h], q3, k2[3]);
             }
         }
-        float sc[G];
+        float sc[GW];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
+        for (int h = 0; h < GW; ++h) {
             float lo, hi;
             f2_unpack(sc2[h], lo, hi);
             sc[h] = lo + hi;
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
+        for (int h = 0; h < GW; ++h) {
             float s = valid ? sc[h] - slope[h] * (qpos - static_cast<float>(j)) : -INFINITY;
             float mb = s;
 #pragma unroll
@@ -206,20 +221,21 @@ __global__ void __launch_bounds__(32 * DecCfg<D>::kWarps) decode_partial_kernel(
                 vf[3] = f1.y;
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < GW; ++h) {
                 const float pt = __shfl_sync(0xffffffffu, sc[h], t);
 #pragma unroll
                 for (int c = 0; c < kCols; ++c) acc[h][c] = fmaf(pt, vf[c], acc[h][c]);
             }
         }
-        __syncwarp();  // the stage is refilled by the next issue
+        if (HS == 1) __syncwarp();  // the stage is refilled by the next issue
+        else __syncthreads();      // (both warps done with it)
     }
     cp_async_wait<0>();
     // (max, sum, output) of this part for each query head; an empty part
     // (j0 >= n) writes max = -inf, sum = 0
-    float* rec = a.ws + (static_cast<int64_t>(b) * a.H + g * G) * a.parts * (D + 2);
+    float* rec = a.ws + (static_cast<int64_t>(b) * a.H + g * G + h0) * a.parts * (D + 2);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < GW; ++h) {
         float* r = rec + (static_cast<int64_t>(h) * a.parts + part) * (D + 2);
         if (lane == 0) {
             r[0] = m[h];
@@ -258,15 +274,21 @@ __global__ void __launch_bounds__(kDecThreads) decode_combine_kernel(DecodeArgs 
 
 template <typename T, int D, int G>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
-    const int64_t warps = static_cast<int64_t>(a.B) * a.Hk * a.parts;
-    auto kern = decode_partial_kernel<T, D, G>;
+    const int64_t items = static_cast<int64_t>(a.B) * a.Hk * a.parts;
+    constexpr int kW = DecCfg<D>::kWarps;
+    // head_dim 128 with G >= 2: a block of two warps per item sharing one
+    // ring (four, each with a quarter of the heads, measured slower: every
+    // warp reads all of the block's K rows from shared memory)
+    constexpr int HS = (D == 128 && G >= 2) ? 2 : 1;
+    constexpr int kSmem = HS == 1 ? DecCfg<D>::kSmem : DecCfg<D>::kWarpBytes;
+    auto kern = decode_partial_kernel<T, D, G, HS>;
     {
-        const cudaError_t e =
-            set_smem_attr_once(reinterpret_cast<const void*>(kern), DecCfg<D>::kSmem);
+        const cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), kSmem);
         if (e != cudaSuccess) return e;
     }
-    constexpr int kW = DecCfg<D>::kWarps;
-    kern<<<static_cast<unsigned>((warps + kW - 1) / kW), 32 * kW, DecCfg<D>::kSmem, s>>>(a);
+    const int64_t blocks = HS == 1 ? (items + kW - 1) / kW : items;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    kern<<<static_cast<unsigned>(blocks), HS == 1 ? 32 * kW : 32 * HS, kSmem, s>>>(a);
     const int64_t cw = static_cast<int64_t>(a.B) * a.H;
     decode_combine_kernel<T, D><<<static_cast<unsigned>((cw + 3) / 4), kDecThreads, 0, s>>>(a);
     return cudaGetLastError();

@@ -19,6 +19,11 @@ CASES = [
     (1, 16, 16, 1024, 64, [1000], True),
     (4, 32, 32, 2048, 64, [2048, 1, 1500, 64], False),
     (2, 8, 1, 700, 128, [700, 33], False),
+    # head_dim 128 with grouped heads: two warps per item share its K/V ring,
+    # each with half of the group's query heads
+    (2, 4, 2, 513, 128, [513, 64], True),
+    (2, 32, 8, 4096, 128, [4096, 1], False),
+    (2, 4, 4, 300, 128, [300, 17], False),   # MHA at head_dim 128: one warp per item
 ]
 
 
