@@ -37,13 +37,26 @@ namespace {
 using namespace gemm;
 
 constexpr int kPairBN = 256;                 // MMA N: output columns (or gate|up rows)
-constexpr int kPairStages = 6;
-constexpr int kPairABytes = kBM * kBK * 2;    // this CTA's 128 rows of A
-constexpr int kPairBBytes = (kPairBN / 2) * kBK * 2;  // this CTA's half of B
-constexpr int kPairStageBytes = kPairABytes + kPairBBytes;
-constexpr int kPairOffBar = kPairStages * kPairStageBytes;
-constexpr int kPairOffEpi = kPairOffBar + 1024;  // staging boxes 1024-byte aligned (swizzle)
-constexpr int kPairSmem = kPairOffEpi + kEpiWarps * 32 * 128 + 1024;
+constexpr int kBoxBytes = kBM * 64 * 2;      // one 64-column swizzled box of 128 rows
+
+// The mainloop's k-block and ring depth, by epilogue: 128 inputs (two
+// 64-column boxes per operand, eight MMAs per barrier round trip) in three
+// 64 KB stages for QKV, SwiGLU and GELU; 64 inputs in six 32 KB stages for
+// LINEAR. Same-box A/B: qkv 128.0 -> 121.3 us, gate/up 209.5 -> 200.0,
+// Bloom's GELU up 71.0 -> 67.5 with 128; but o_proj 59.5 -> 61.7 and down
+// 121.4 -> 127.0 (their heavier residual epilogues want the finer ring).
+template <int EPI>
+struct PairK {
+    static constexpr int kBKp = EPI == EPI_LINEAR ? 64 : 128;
+    static constexpr int kBoxes = kBKp / 64;
+    static constexpr int kStages = EPI == EPI_LINEAR ? 6 : 3;
+    static constexpr int kABytes = kBM * kBKp * 2;             // this CTA's 128 rows of A
+    static constexpr int kBBytes = (kPairBN / 2) * kBKp * 2;   // this CTA's half of B
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kOffBar = kStages * kStageBytes;
+    static constexpr int kOffEpi = kOffBar + 1024;  // staging boxes 1024-byte aligned (swizzle)
+    static constexpr int kSmem = kOffEpi + kEpiWarps * 32 * 128 + 1024;
+};
 constexpr uint32_t kPairTmemCols = 2 * kPairBN;  // two accumulators
 
 template <typename T, int EPI, int ROT, bool SPLIT>
@@ -58,6 +71,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr int BN = kPairBN;
     constexpr int kBNOut = EPI == EPI_SWIGLU ? BN / 2 : BN;
     constexpr int kPM = 2 * kBM;  // output rows per pair tile
+    using PK = PairK<EPI>;
+    constexpr int kPairStages = PK::kStages;
+    constexpr int kPairABytes = PK::kABytes;
+    constexpr int kPairStageBytes = PK::kStageBytes;
+    constexpr int kPairOffBar = PK::kOffBar;
+    constexpr int kPairOffEpi = PK::kOffEpi;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const uint32_t sbase = smem_u32(smem);
@@ -102,7 +121,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int num_units = m_units * n_tiles;
     const int unit0 = static_cast<int>(blockIdx.x) / 2;
     const int unit_step = static_cast<int>(gridDim.x) / 2;
-    const int kb_count = (g.K + kBK - 1) / kBK;
+    const int kb_count = (g.K + PK::kBKp - 1) / PK::kBKp;
     const int num_work =
         SPLIT ? g.split_base + (num_units - g.split_base) * g.split_s : num_units;
     auto tile_of = [&](int u, int& mt, int& nt) {
@@ -130,8 +149,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t sa = sbase + stage * kPairStageBytes;
                     const uint32_t fb = full_lead0 + 8u * stage;
                     if (lead) mbar_expect_tx(full(stage), 2 * kPairStageBytes);
-                    tma_load_2d_pair(sa, &tmA, fb, kb * kBK, arow);
-                    tma_load_2d_pair(sa + kPairABytes, mb, fb, kb * kBK, brow);
+#pragma unroll
+                    for (int bx = 0; bx < PK::kBoxes; ++bx) {
+                        tma_load_2d_pair(sa + bx * kBoxBytes, &tmA, fb, kb * PK::kBKp + bx * 64, arow);
+                        tma_load_2d_pair(sa + kPairABytes + bx * kBoxBytes, mb, fb,
+                                         kb * PK::kBKp + bx * 64, brow);
+                    }
                     if (++stage == kPairStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -166,9 +189,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint64_t ad = da0 + stage * kStageStep;
                     const uint64_t bd = db0 + stage * kStageStep;
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        tc_mma_ss_pair(d_tmem, ad + k * 2, bd + k * 2, idesc,
+                    for (int k = 0; k < PK::kBKp / 16; ++k) {
+                        const uint64_t off = (k / 4) * (kBoxBytes >> 4) + (k % 4) * 2;
+                        tc_mma_ss_pair(d_tmem, ad + off, bd + off, idesc,
                                        (kb > un.kb0 || k != 0) ? 1u : 0u);
+                    }
                     tc_commit_pair(empty0[0] + 8u * stage);
                     tc_commit_pair(empty0[1] + 8u * stage);
                     if (++stage == kPairStages) {
@@ -284,6 +309,7 @@ cudaError_t launch_pair_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const 
     constexpr bool kCanSplit = EPI != EPI_SWIGLU;
     auto kern = gemm_pair_kernel<T, EPI, ROT, false>;
     auto kern_split = gemm_pair_kernel<T, EPI, ROT, kCanSplit>;
+    constexpr int kPairSmem = PairK<EPI>::kSmem;
     cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), kPairSmem);
     if (e == cudaSuccess && kCanSplit)
         e = set_smem_attr_once(reinterpret_cast<const void*>(kern_split), kPairSmem);
@@ -321,8 +347,10 @@ cudaError_t launch_pair_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const 
         const int64_t rounds = (units + G - 1) / G;
         const int64_t R = units - (rounds - 1) * G;
         const int64_t sp = 2;
-        const int64_t kb_count = (g.K + kBK - 1) / kBK;
-        if (rounds >= 2 && R * sp <= G && kb_count >= sp * kSplitMinKb &&
+        // (kSplitMinKb counts 64-wide k-blocks)
+        const int64_t kbw = PairK<EPI>::kBKp;
+        const int64_t kb_count = (g.K + kbw - 1) / kbw;
+        if (rounds >= 2 && R * sp <= G && kb_count * kbw >= sp * kSplitMinKb * kBK &&
             R * 2 * sp <= kGemmSplitSlots && R * 2 * kEpiWarps <= kGemmSplitCounters) {
             ga.split_s = static_cast<int>(sp);
             ga.split_base = static_cast<int>((rounds - 1) * G);
