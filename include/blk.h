@@ -13,7 +13,15 @@
  *     allocates no device memory, frees nothing and never synchronises a
  *     stream (blk_check_device_status is the one call that does, by design).
  *   - Work is enqueued on the caller's stream `s` (a cudaStream_t; NULL is the
- *     legacy default stream) and runs asynchronously.
+ *     legacy default stream) and runs asynchronously. Stream order holds as
+ *     for any kernel: each call's first kernel reads nothing before the work
+ *     enqueued ahead of it on `s` has completed. Outside stream capture the
+ *     hot-path kernels are launched with programmatic stream serialization,
+ *     so a kernel may begin its set-up (shared memory, barriers, TMEM)
+ *     while the previous one drains; it waits for that grid's completion
+ *     (griddepcontrol.wait) before its first global access. A kernel the
+ *     caller enqueues after a call is ordered as usual, unless the caller
+ *     launches it with the same attribute.
  *   - Row-major, contiguous, 16-byte-aligned tensors. Linear weights follow the
  *     torch convention W[out, in], y = x W^T + b (nnterp "stablelm" Printout).
  *   - Storage dtype `dt` is fp16 or bf16 for every tensor of a call, except
