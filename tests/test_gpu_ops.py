@@ -87,6 +87,21 @@ def test_linear_persistent_multi_wave():
     check(y[torch.as_tensor(rows, device="cuda")], ref, "linear multi-wave")
 
 
+@pytest.mark.parametrize("m,n,k", [(5000, 1000, 512), (2304, 2560, 320), (300, 1536, 256)])
+def test_linear_partial_last_round(m, n, k):
+    """Several rounds of 256 x 256 output tiles with a partial last one (80 =
+    76 + 4 and 90 = 76 + 14 tiles on 76 CTA pairs) and a single partial round
+    of 12 tiles, ragged in M and N, with bias and a residual."""
+    seed = m + n + k
+    x = draw((m, k), "bf16", seed)
+    w = draw((n, k), "bf16", seed + 1, "w")
+    bias = draw((n,), "bf16", seed + 2, "b")
+    r1 = draw((m, n), "bf16", seed + 3)
+    y = blk.linear(to_dev(x), to_dev(w), to_dev(bias), to_dev(r1))
+    ref = oracle.linear(f64(x), f64(w), f64(bias)) + f64(r1)
+    check(y, ref, f"linear last round {m}x{n}x{k}")
+
+
 # -------------------------------------------------------------------- MLP --
 @pytest.mark.parametrize("dt", DTYPES)
 @pytest.mark.parametrize("act,T,D,F", [("swiglu", 128, 256, 688), ("swiglu", 300, 512, 1024),
