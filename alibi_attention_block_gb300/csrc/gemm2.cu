@@ -128,6 +128,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mt = g.n_fastest ? u / n_tiles : u % m_units;
         nt = g.n_fastest ? u % n_tiles : u / m_units;
     };
+    // With a bias (LINEAR, GELU, QKV), a tile's accumulator starts as the
+    // bias row, written into TMEM by the epilogue warps once it is free,
+    // before the tile's first MMA (which then accumulates): the epilogue no
+    // longer adds it. The TMEM-empty barriers then carry one more arrival
+    // each, the first two before any tile. Split segments start from zero
+    // and take the bias in the last one's epilogue, as before.
+    const bool pre = EPI != EPI_SWIGLU && g.bias != nullptr;
+    auto preloaded = [&](int v) {
+        return pre && v < num_work && !(SPLIT && g.split_s > 1 && v >= g.split_base);
+    };
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
@@ -177,7 +187,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int v = unit0; v < num_work && ok; v += unit_step, ++it) {
                 const Unit un = decode_unit<SPLIT>(g, v, kb_count);
                 const int acc = it & 1;
-                if (!mbar_wait_cluster(tempty(acc), ((it >> 1) & 1) ^ 1u, g.err)) break;
+                const uint32_t tpar = pre ? ((it >> 1) & 1) : (((it >> 1) & 1) ^ 1u);
+                if (!mbar_wait_cluster(tempty(acc), tpar, g.err)) break;
+                const bool start = !preloaded(v);  // the first MMA overwrites
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = un.kb0; kb < un.kb1; ++kb) {
@@ -192,7 +204,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int k = 0; k < PK::kBKp / 16; ++k) {
                         const uint64_t off = (k / 4) * (kBoxBytes >> 4) + (k % 4) * 2;
                         tc_mma_ss_pair(d_tmem, ad + off, bd + off, idesc,
-                                       (kb > un.kb0 || k != 0) ? 1u : 0u);
+                                       (kb > un.kb0 || k != 0 || !start) ? 1u : 0u);
                     }
                     tc_commit_pair(empty0[0] + 8u * stage);
                     tc_commit_pair(empty0[1] + 8u * stage);
@@ -214,6 +226,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row = quarter * 32 + lane;
         const uint32_t stg0 = sbase + kPairOffEpi;
         const uint32_t tempty_lead0 = peer_addr(tempty(0), 0);
+        const uint32_t lane_q = static_cast<uint32_t>(quarter * 32) << 16;
+        auto preload = [&](int v, int acc) {
+            const Unit u2 = decode_unit<SPLIT>(g, v, kb_count);
+            int mt2, nt2;
+            tile_of(u2.u, mt2, nt2);
+            preload_bias<T, BN>(g, tmem_base + acc * BN + lane_q, nt2, half);
+        };
+        if (pre) {
+            // the first two tiles' accumulators
+            for (int a = 0; a < 2; ++a) {
+                if (preloaded(unit0 + a * unit_step)) preload(unit0 + a * unit_step, a);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tempty_lead0 + 8u * a);
+            }
+        }
         int it = 0;
         for (int v = unit0; v < num_work; v += unit_step, ++it) {
             const Unit un = decode_unit<SPLIT>(g, v, kb_count);
@@ -259,11 +287,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 epilogue_tile<T, BN, EPI, ROT, SPLIT>(g, rp, tbase, m0 + row, nt,
                                                       stg0 + ew * (32 * 128), lane,
                                                       m0 + quarter * 32, part, un.q, row, half,
-                                                      g.tma_out ? &tmO : nullptr, &tmO2, &tmO3);
+                                                      g.tma_out ? &tmO : nullptr, &tmO2, &tmO3,
+                                                      preloaded(v));
                 if (cnt && lane == 0) *cnt = 0u;  // every segment has arrived: ready for reuse
             }
             tc_fence_before();
             __syncwarp();
+            // the accumulator's next tile (two on) starts as its bias row
+            if (preloaded(v + 2 * unit_step)) {
+                preload(v + 2 * unit_step, acc);
+                tc_fence_before();
+                __syncwarp();
+            }
             if (lane == 0) mbar_arrive_cluster(tempty_lead0 + 8u * acc);
         }
         // the warp's TMA stores have read their staging boxes and written

@@ -166,6 +166,49 @@ __device__ __forceinline__ void stage_store(const CUtensorMap* tmo, uint32_t stg
     }
 }
 
+// A tile's accumulator started as its bias row, for this thread's lane of
+// TMEM and its half of the tile's 32-column chunks (columns past N start at
+// zero), before the tile's MMAs accumulate onto it. Every lane reads the
+// same bias words (one transaction per warp each), two chunks' words in
+// flight at a time.
+template <typename T, int NB>
+__device__ __forceinline__ void preload_bias_batch(const GemmArgs& g, uint32_t tbase, int n00,
+                                                   int c0) {
+    const T* bp = static_cast<const T*>(g.bias);
+    uint4 w[NB][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const int n0 = n00 + (c0 + b) * 32;
+        const int valid = g.N - n0;
+        const uint4* p = reinterpret_cast<const uint4*>(bp + n0);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) w[b][v] = v * 8 < valid ? p[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint32_t u[4] = {w[b][v].x, w[b][v].y, w[b][v].z, w[b][v].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = dt_traits<T>::unpack2(u[e]);
+                r[8 * v + 2 * e] = __float_as_uint(f.x);
+                r[8 * v + 2 * e + 1] = __float_as_uint(f.y);
+            }
+        }
+        tmem_st32_nowait(tbase + (c0 + b) * 32, r);
+    }
+}
+template <typename T, int BN>
+__device__ __forceinline__ void preload_bias(const GemmArgs& g, uint32_t tbase, int nt, int half) {
+    constexpr int kC = BN / 64;  // this warp's chunks, two at a time
+    const int c0 = half * kC;
+#pragma unroll 1
+    for (int b = 0; b < kC; b += 2) preload_bias_batch<T, 2>(g, tbase, nt * BN, c0 + b);
+    tmem_st_wait();
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
 __device__ __forceinline__ float gelu_tanh_f(float z) {
@@ -184,7 +227,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                                               int trow, int half,
                                               const CUtensorMap* tmo = nullptr,
                                               const CUtensorMap* tmo_k = nullptr,
-                                              const CUtensorMap* tmo_v = nullptr) {
+                                              const CUtensorMap* tmo_v = nullptr,
+                                              bool bias_in_acc = false) {
     // this warp's half of the tile's 32-column chunks
     constexpr int kChunks = (EPI == EPI_SWIGLU ? BN / 2 : BN) / 32;
     const int c_begin = half * (kChunks / 2), c_end = c_begin + kChunks / 2;
@@ -232,7 +276,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
             if constexpr (SPLIT)
                 if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
-            if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, 32);
+            if (g.bias && !bias_in_acc) add_row32(static_cast<const T*>(g.bias) + n0, o, 32);
             int which, head, dd0;
             if (g.interleaved) {
                 head = n0 / (3 * d);
@@ -315,7 +359,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             if (valid > 0) {
                 if constexpr (SPLIT)
                     if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
-                if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
+                if (g.bias && !bias_in_acc) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
                 if constexpr (EPI == EPI_GELU) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
@@ -352,7 +396,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
             if constexpr (SPLIT)
                 if (part) add_partials<BN>(o, part, g.split_s, self, c * 32, trow);
-            if (g.bias) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
+            if (g.bias && !bias_in_acc) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
             if constexpr (EPI == EPI_GELU) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
