@@ -211,9 +211,14 @@ __device__ __forceinline__ void preload_bias(const GemmArgs& g, uint32_t tbase, 
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
+// GELU, tanh form: 0.5 z (1 + tanh(u)), u = sqrt(2/pi) (z + 0.044715 z^3).
+// Since 0.5 (1 + tanh(u)) = 1 / (1 + e^(-2u)), it is computed as
+// z / (1 + 2^(-2 u log2(e))): one ex2.approx and one fast division instead
+// of a tanh (z -> -inf: the denominator overflows and the result is -0).
 __device__ __forceinline__ float gelu_tanh_f(float z) {
-    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
-    return 0.5f * z * (1.0f + tanhf(k0 * (z + 0.044715f * z * z * z)));
+    constexpr float kNeg2UL2e = -2.0f * 0.7978845608028654f * 1.4426950408889634f;
+    const float t = kNeg2UL2e * fmaf(0.044715f * z, z * z, z);
+    return __fdividef(z, 1.0f + ex2_approx(t));
 }
 
 // tmo: the output's tensor map for TMA stores of staged boxes (16-bit

@@ -128,6 +128,26 @@ def test_mlp(dt, act, T, D, F):
     check(y, m + f64(res), f"mlp {act}")
 
 
+def test_mlp_gelu_large_preactivations():
+    """GELU(tanh) where the up projection's outputs reach the hundreds: the
+    epilogue's exponential overflows for large negative inputs (the result
+    must go to zero, not NaN) and vanishes for large positive ones."""
+    T, D, F = 200, 256, 1024
+    x = draw((T, D), "fp16", 7, scale=60.0)
+    w_up = draw((F, D), "fp16", 8, "w")
+    w_down = draw((D, F), "fp16", 9, "w")
+    b_up = draw((F,), "fp16", 10, "b")
+    b_down = draw((D,), "fp16", 11, "b")
+    res = draw((T, D), "fp16", 12)
+    y = blk.mlp(to_dev(x), to_dev(w_up), to_dev(w_down), b_up=to_dev(b_up), b_down=to_dev(b_down),
+                res1=to_dev(res), act="gelu_tanh")
+    w = {"w_up": f64(w_up), "w_down": f64(w_down), "b_up": f64(b_up), "b_down": f64(b_down)}
+    pre = f64(x) @ f64(w_up).T + f64(b_up)
+    assert np.abs(pre).max() > 60.0, np.abs(pre).max()  # the regime this test is for
+    _, m = oracle.mlp(f64(x), w, "gelu_tanh")
+    check(y, m + f64(res), "mlp gelu large pre-activations")
+
+
 # -------------------------------------------------------------------- QKV --
 QKV_CASES = {
     # name: (B, S, D, H, Hk, d, layout, qk_norm, r, base, bias)
