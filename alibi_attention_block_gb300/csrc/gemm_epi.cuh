@@ -209,16 +209,51 @@ __device__ __forceinline__ void preload_bias(const GemmArgs& g, uint32_t tbase, 
     tmem_st_wait();
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// (a0 b0, a1 b1) in one instruction.
+__device__ __forceinline__ void fmul2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-// GELU, tanh form: 0.5 z (1 + tanh(u)), u = sqrt(2/pi) (z + 0.044715 z^3).
-// Since 0.5 (1 + tanh(u)) = 1 / (1 + e^(-2u)), it is computed as
-// z / (1 + 2^(-2 u log2(e))): one ex2.approx and one fast division instead
-// of a tanh (z -> -inf: the denominator overflows and the result is -0).
-__device__ __forceinline__ float gelu_tanh_f(float z) {
-    constexpr float kNeg2UL2e = -2.0f * 0.7978845608028654f * 1.4426950408889634f;
-    const float t = kNeg2UL2e * fmaf(0.044715f * z, z * z, z);
-    return __fdividef(z, 1.0f + ex2_approx(t));
+// silu(g) u for two elements: g u / (1 + 2^(-g log2(e))), in paired f32x2
+// arithmetic with ex2.approx and an approximate reciprocal (g -> -inf: the
+// denominator overflows, its reciprocal is 0, and so is the result).
+__device__ __forceinline__ void swiglu2(float g0, float g1, float u0, float u1, float& o0,
+                                        float& o1) {
+    constexpr float kNegL2e = -1.4426950408889634f;
+    const uint64_t one2 = f2_pack(1.0f, 1.0f);
+    float t0, t1, d0, d1, p0, p1;
+    fmul2(g0, g1, kNegL2e, kNegL2e, t0, t1);
+    ffma2(ex2_approx(t0), ex2_approx(t1), one2, one2, d0, d1);
+    fmul2(g0, g1, u0, u1, p0, p1);
+    fmul2(p0, p1, rcp_approx(d0), rcp_approx(d1), o0, o1);
+}
+
+// GELU, tanh form, for two elements: 0.5 z (1 + tanh(u)) with u = sqrt(2/pi)
+// (z + 0.044715 z^3). Since 0.5 (1 + tanh(u)) = 1 / (1 + e^(-2u)), it is
+// z / (1 + 2^t), t = -2 sqrt(2/pi) log2(e) z (1 + 0.044715 z^2): one
+// ex2.approx and one approximate reciprocal per element instead of a tanh,
+// the rest in paired f32x2 arithmetic (z -> -inf: the result goes to 0).
+__device__ __forceinline__ void gelu2(float z0, float z1, float& o0, float& o1) {
+    constexpr float kT = -2.0f * 0.7978845608028654f * 1.4426950408889634f;
+    const uint64_t one2 = f2_pack(1.0f, 1.0f);
+    float q0, q1, w0, w1, t0, t1, d0, d1;
+    fmul2(z0, z1, z0, z1, q0, q1);
+    ffma2(q0, q1, f2_pack(0.044715f, 0.044715f), one2, q0, q1);
+    fmul2(z0, z1, kT, kT, w0, w1);
+    fmul2(w0, w1, q0, q1, t0, t1);
+    ffma2(ex2_approx(t0), ex2_approx(t1), one2, one2, d0, d1);
+    fmul2(z0, z1, rcp_approx(d0), rcp_approx(d1), o0, o1);
 }
 
 // tmo: the output's tensor map for TMA stores of staged boxes (16-bit
@@ -250,8 +285,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 // two chunks per box (64 columns of 16-bit values)
                 float o[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    o[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+                for (int i = 0; i < 32; i += 2)
+                    swiglu2(__uint_as_float(gr[i]), __uint_as_float(gr[i + 1]), __uint_as_float(ur[i]),
+                            __uint_as_float(ur[i + 1]), o[i], o[i + 1]);
                 const int k = c - c_begin;
                 if ((k & 1) == 0) stage_begin(lane);
                 stage_row<T>(stg, lane, (k & 1) * 4, false, o);
@@ -262,8 +298,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             if (!row_ok || n0 >= g.N) continue;
             float o[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                o[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+            for (int i = 0; i < 32; i += 2)
+                swiglu2(__uint_as_float(gr[i]), __uint_as_float(gr[i + 1]), __uint_as_float(ur[i]),
+                        __uint_as_float(ur[i + 1]), o[i], o[i + 1]);
             store_row32(static_cast<T*>(g.out) + static_cast<int64_t>(m) * g.N + n0, o, g.N - n0);
         }
     } else if constexpr (EPI == EPI_QKV) {
@@ -367,7 +404,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 if (g.bias && !bias_in_acc) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
                 if constexpr (EPI == EPI_GELU) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
+                    for (int i = 0; i < 32; i += 2) gelu2(o[i], o[i + 1], o[i], o[i + 1]);
                 }
                 const int64_t off = static_cast<int64_t>(m) * g.N + n0;
                 if (row_ok && g.res1) {
@@ -404,7 +441,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
             if (g.bias && !bias_in_acc) add_row32(static_cast<const T*>(g.bias) + n0, o, valid);
             if constexpr (EPI == EPI_GELU) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = gelu_tanh_f(o[i]);
+                for (int i = 0; i < 32; i += 2) gelu2(o[i], o[i + 1], o[i], o[i + 1]);
             }
             const int64_t off = static_cast<int64_t>(m) * g.N + n0;
             if (row_ok && g.res1) {
