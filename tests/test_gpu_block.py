@@ -137,6 +137,27 @@ def test_block_split_gemm_rounds():
     check(got, ref, "split GEMM rounds", unit_scale=True, abs_tol=_abs_tol(cfg), storage=cfg.dtype)
 
 
+def test_block_split_gemm_rounds_with_bias():
+    """The same split last round with a down-projection bias (Bloom-shaped:
+    GELU MLP with biases, ALiBi): 24 x 4 = 96 units of 128 k-blocks, the
+    last round's 20 (rows 1024 on in column tile 3) split along K. Whole
+    tiles start their accumulators at the bias row; split segments start at
+    zero and the last to arrive adds the bias once. Checked against the
+    oracle on sampled rows and bit for bit run to run."""
+    cfg = scaled(BLOCK_CONFIGS["bloom_560m"], batch=3, seq=2048, hidden=1024, n_heads=16,
+                 n_kv_heads=16, intermediate=8192)
+    x, w = workloads.block_inputs(cfg)
+    y = _gpu_forward(cfg, x, w)
+    y2 = _gpu_forward(cfg, x, w)
+    assert torch.equal(y, y2)
+    rows = np.array(sorted({int(r) for r in workloads.sample_rows(cfg.tokens, 24, seed=cfg.seed)}
+                           | {0, 1023, 1024, 2047, 2048, 4095, 4096, 6143}))
+    ref = oracle.block_forward(cfg, x, w, rows=rows)["y"]
+    got = y.reshape(cfg.tokens, cfg.hidden)[torch.as_tensor(rows, device=y.device)]
+    check(got, ref, "split GEMM rounds with bias", unit_scale=True, abs_tol=_abs_tol(cfg),
+          storage=cfg.dtype)
+
+
 @pytest.mark.parametrize("name", ["stablelm2_1p6b", "bloom_560m", "olmo2_1b", "stablelm2_12b"])
 def test_block_full_size_sampled_rows(name):
     """Each full-size block, launched as bench.py times it, on 48 seeded
