@@ -416,16 +416,14 @@ cudaError_t launch_pair_t(DType dt, int epi, const void* a, const void* b, const
     const CUtensorMapDataType ty =
         dt == DType::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (epi == EPI_QKV) {
-        // boxes of 64 columns when head_dim % 64 == 0, else of 32 (64-byte
-        // swizzle) when head_dim % 32 == 0 (the 12B model's 160)
+        // boxes of 32 columns (64-byte swizzle) when head_dim % 32 == 0
         if (g.d % 32 == 0 && g.S > 0 && g.S % 32 == 0 && g.M % g.S == 0) {
             const uint64_t B = static_cast<uint64_t>(g.M / g.S);
-            const uint32_t bc = g.d % 64 == 0 ? 64 : 32;
-            if (!make_tmap_3d(&to[0], dt, g.q, B * g.H, g.S, g.d, 32, bc) ||
-                !make_tmap_3d(&to[1], dt, g.k, B * g.Hk, g.S, g.d, 32, bc) ||
-                !make_tmap_3d(&to[2], dt, g.v, B * g.Hk, g.S, g.d, 32, bc))
+            if (!make_tmap_3d(&to[0], dt, g.q, B * g.H, g.S, g.d, 32, 32) ||
+                !make_tmap_3d(&to[1], dt, g.k, B * g.Hk, g.S, g.d, 32, 32) ||
+                !make_tmap_3d(&to[2], dt, g.v, B * g.Hk, g.S, g.d, 32, 32))
                 return cudaErrorInvalidValue;
-            gt.tma_out = bc == 64 ? 1 : 2;
+            gt.tma_out = 2;
         }
     } else if (!(epi == EPI_LINEAR && g.out_f32)) {
         if (!make_tmap_2d_plain(&to[0], ty, 2, g.out, g.M, g.N, 64, 32, true))

@@ -347,36 +347,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const RopeParam
                 }
             }
             const int nheads = which == 0 ? g.H : g.Hk;
-            if (tmo && g.tma_out == 2) {
+            if (tmo) {
                 // one chunk (32 columns of one head) per box of the warp's 32
-                // positions (S % 32 == 0: one sequence)
-                stage_begin(lane);
-                stage_row64<T>(stg, lane, o);
+                // positions (S % 32 == 0: one sequence), two 2 KB boxes of
+                // the warp's staging area in turn, so a box is staged while
+                // the previous one's store still reads
+                const uint32_t sb = stg + ((c - c_begin) & 1) * 2048;
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                stage_row64<T>(sb, lane, o);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && m_base < g.M) {
                     const int b0 = m_base / g.S;
-                    tma_store_3d(which == 0 ? tmo : (which == 1 ? tmo_k : tmo_v), stg, dd0,
+                    tma_store_3d(which == 0 ? tmo : (which == 1 ? tmo_k : tmo_v), sb, dd0,
                                  m_base - b0 * g.S, b0 * nheads + head);
                     bulk_commit();
-                }
-                continue;
-            }
-            if (tmo) {
-                // two chunks (64 columns of one head: head_dim % 64 == 0) per
-                // box of the warp's 32 positions (S % 32 == 0: one sequence)
-                const int k = c - c_begin;
-                if ((k & 1) == 0) stage_begin(lane);
-                stage_row<T>(stg, lane, (k & 1) * 4, false, o);
-                if ((k & 1) == 1) {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && m_base < g.M) {
-                        const int b0 = m_base / g.S;
-                        tma_store_3d(which == 0 ? tmo : (which == 1 ? tmo_k : tmo_v), stg,
-                                     dd0 - 32, m_base - b0 * g.S, b0 * nheads + head);
-                        bulk_commit();
-                    }
                 }
                 continue;
             }

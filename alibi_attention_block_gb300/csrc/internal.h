@@ -75,7 +75,7 @@ struct GemmArgs {
     int split_s;          // segments per split unit (set by launch_gemm; 1 = none)
     int split_base;       // first split unit
     // pair GEMM: the output goes out by TMA stores (set by its launcher): 1
-    // in boxes of 64 columns, 2 (QKV at head_dim % 64 != 0) of 32
+    // in boxes of 64 columns, 2 (QKV) of 32
     int tma_out;
 };
 // scratch of a split GEMM: kGemmSplitSlots partial 128 x 256 fp32 tiles, then
